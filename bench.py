@@ -1,0 +1,438 @@
+"""Benchmark of the paged decode step on the mixed-length serving batch.
+
+Workload (seeded, synthetic; no dataset): an OPT-13B-shaped attention layer,
+40 heads x head_dim 128, fp16, block size 16, 256 sequences whose prompt
+lengths are lognormal (median 200, cap 1536) and whose outputs are lognormal
+(median 250), total context capped at 2048, block tables fragmented across a
+shuffled pool, contexts over 512 tokens on the split-context path.  The
+batch runs as a steady-state continuous batch: every step appends one token
+to every sequence; a sequence that reaches its drawn total length is freed
+and replaced by a newly drawn one, so the length mix stays stationary over
+thousands of steps.  (A newcomer's prompt K/V is not written -- prefill is
+another kernel -- its blocks keep the finite values of earlier occupants.)
+
+One step = the whole hot path: host block manager (pa_alloc_slots, table
+export), one packed metadata upload, copy-on-write copies (none in this
+workload), the slot write of the new K/V, and decode attention (split +
+merge).  ``value`` is K/V token positions attended per second
+(sum of context lengths / step time), inputs resident in HBM (the K/V
+working set, ~2.8 GB, is far larger than L2, so no L2 flush is needed).
+``e2e`` repeats the step with q / k / v uploaded from pinned host memory and
+the output read back to host every step, wall-clock timed.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn seq-tokens/s (1 GB300) + achieved HBM GB/s vs ~8 TB/s peak"
+UNIT = "seq-tokens/s"
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_traffic(kernel_src: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        if d.get("kernel_sha256") == h:
+            return d
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.out.seek(0)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _pool_setup(pk, w):
+    desc = pk.PoolDesc(w.num_blocks, w.block_size, num_layers=1, num_heads=w.num_heads,
+                       head_dim=w.head_dim, partition_tokens=w.split_tokens,
+                       free_order=w.free_order)
+    pool = pk.pa_pool_create(desc)
+    for i, n in enumerate(w.prompt_lens):
+        pk.pa_seq_add(pool, i, n, want_slots=False)
+    return desc, pool
+
+
+class SteadyBatch:
+    """Host side of the continuous batch: replaces finished sequences."""
+
+    def __init__(self, pk, pool, w, rng):
+        self.pk, self.pool, self.rng = pk, pool, rng
+        self.held = np.array(w.prompt_lens, np.int64)
+        self.target = np.array(w.targets, np.int64)
+        self.next_id = len(w.prompt_lens)
+        self.replaced = 0
+
+    def admit(self, ids):
+        from paged_kv_cache_106_gb300.workloads import draw_mixed_sequence
+        for i in np.nonzero(self.held >= self.target)[0]:
+            self.pk.pa_seq_free(self.pool, int(ids[i]))
+            prompt, target = draw_mixed_sequence(self.rng)
+            self.pk.pa_seq_add(self.pool, self.next_id, prompt, want_slots=False)
+            ids[i] = self.next_id
+            self.next_id += 1
+            self.held[i], self.target[i] = prompt, target
+            self.replaced += 1
+
+    def appended(self):
+        self.held += 1
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_106_gb300 as pk
+    from paged_kv_cache_106_gb300 import workloads as wl
+    from paged_kv_cache_106_gb300.step import DecodeStepRunner
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    w = wl.mixed_b256(batch=args.batch, steady_state=True)
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    desc, pool = _pool_setup(pk, w)
+    ids = np.arange(len(w.prompt_lens), dtype=np.int32)
+    S = len(ids)
+    max_blocks = -(-wl.CTX_CAP // B)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed + 1000 * rank)
+    kc = torch.empty((w.num_blocks, H, B, D), dtype=torch.float16, device=dev)
+    vc = torch.empty_like(kc)
+    kc.normal_(generator=gen)
+    vc.normal_(generator=gen)
+    q = torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+    k_new = torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+    v_new = torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+    out = torch.empty((S, H, D), dtype=torch.float16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    runner = DecodeStepRunner(pool, desc, ids, max_blocks, device=dev, stream=stream)
+    runner.ids = ids                       # the batch edits ids in place on replacement
+    batch = SteadyBatch(pk, pool, w, np.random.default_rng(w.seed + 7 + rank))
+    merge = pk.pa_decode_workspace_bytes(S, max_blocks, desc) > 0
+    bytes_fixed = S * H * D * 2 * 2       # q read + o written
+
+    def step(ev_pair=None, stats=None):
+        batch.admit(ids)
+        n_cp = runner.prepare()
+        batch.appended()
+        ctx = runner.ctx_host.astype(np.int64)
+        runner.copy_blocks([kc], [vc])
+        runner.write_kv(k_new, v_new, kc, vc)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        runner.attention(out, q, kc, vc, w.scale)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+        if stats is not None:
+            stats["tokens"] += int(ctx.sum())
+            nblk = (ctx + B - 1) // B
+            stats["attn_bytes"] += int(ctx.sum()) * H * D * 2 * 2 + int(nblk.sum()) * 4 + S * 4 \
+                + bytes_fixed
+            stats["launches"] += 2 + (1 if merge else 0) + (1 if n_cp else 0)
+            stats["copies"] += n_cp
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    stats = {"tokens": 0, "attn_bytes": 0, "launches": 0, "copies": 0}
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i], stats)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t0.elapsed_time(t1) / 1e3
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    assert runner.status.item() == 0, f"device status {runner.status.item()}"
+
+    # ---- e2e: host buffers, H2D of q/k/v and D2H of o inside every step
+    h_q = torch.empty((S, H, D), dtype=torch.float16, pin_memory=True)
+    h_k = torch.empty_like(h_q).pin_memory()
+    h_v = torch.empty_like(h_q).pin_memory()
+    h_o = torch.empty_like(h_q).pin_memory()
+    h_q.copy_(q.cpu()), h_k.copy_(k_new.cpu()), h_v.copy_(v_new.cpu())
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    e2e_tokens = 0
+    meta_bytes = runner.nbytes
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    w0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            q.copy_(h_q, non_blocking=True)
+            k_new.copy_(h_k, non_blocking=True)
+            v_new.copy_(h_v, non_blocking=True)
+            st = {"tokens": 0, "attn_bytes": 0, "launches": 0, "copies": 0}
+            step(None, st)
+            e2e_tokens += st["tokens"]
+            h_o.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_time = time.perf_counter() - w0
+
+    # ---- reduce over ranks: max time, summed work
+    tot = torch.tensor([stats["tokens"], e2e_tokens], dtype=torch.float64, device=dev)
+    mx = torch.tensor([elapsed, e2e_time], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    tokens_all, e2e_tokens_all = tot.tolist()
+    elapsed_max, e2e_max = mx.tolist()
+
+    if rank == 0:
+        peak, peak_kind = _peaks()
+        attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
+        achieved = stats["attn_bytes"] / args.steps / attn_avg_s / 1e9
+        src = os.path.join(ROOT, "paged_kv_cache_106_gb300", "csrc", "decode_attention.cu")
+        traffic = _kernel_traffic(src)
+        line = {
+            "metric": METRIC,
+            "value": tokens_all / elapsed_max,
+            "unit": UNIT,
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": elapsed_max * 1e3 / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16 (fp32 accumulate)",
+            "data": "synthetic (seeded N(0,1) fp16 K/V/q; lognormal length mix)",
+            "config": {
+                "workload": f"mixed-length serving batch, OPT-13B-shaped layer 40x128, block 16, "
+                            f"batch {S}/GPU, ctx<=2048, split>512, steady-state continuous batch",
+                "batch_per_gpu": S, "num_heads": H, "head_dim": D, "block_size": B,
+                "partition_tokens": w.split_tokens, "pool_blocks": w.num_blocks,
+                "mean_ctx": stats["tokens"] / args.steps / S,
+                "sequences_replaced": batch.replaced,
+                "l2": "working set ~%.1f GB per step >> 129 MB L2, no flush"
+                      % (stats["attn_bytes"] / args.steps / 1e9),
+                "parallelism": f"replicas x{ws} (sequences independent, no collective)",
+            },
+            "gpu_launches": stats["launches"],
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "paged_decode_kernel + paged_merge_kernel (pa_decode_attention)",
+                "achieved": achieved,
+                "peak": peak,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "unit": "GB/s",
+                "frac": achieved / peak,
+                "frac_of_nominal_7900": achieved / 7900.0,
+                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                "algorithmic_bytes_per_launch": stats["attn_bytes"] / args.steps,
+                "attn_ms_per_launch": attn_avg_s * 1e3,
+                "attn_share_of_step": attn_avg_s / (elapsed_max / args.steps),
+            },
+            "decode_tokens_per_s": ws * S * args.steps / elapsed_max,
+            "e2e": {
+                "value": e2e_tokens_all / e2e_max,
+                "unit": UNIT,
+                "h2d_bytes_per_step": 3 * S * H * D * 2 + meta_bytes,
+                "d2h_bytes_per_step": S * H * D * 2,
+                "steps": e2e_steps,
+                "timing": "wall clock, stream synchronised every step",
+            },
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds, args.cpu_seqs)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    pk.pa_pool_destroy(pool)
+
+
+def _oracle_sample(n_seqs):
+    """Host data for the first n_seqs sequences of the same workload, laid
+    out by the oracle's own block manager."""
+    from paged_kv_cache_106_gb300 import workloads as wl
+    from oracle.alloc import BlockManager
+
+    w = wl.mixed_b256(steady_state=True)
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    m = BlockManager(w.num_blocks, B, w.free_order)
+    for i, n in enumerate(w.prompt_lens):
+        m.add(i, n)
+    ids = list(range(n_seqs))
+    m.alloc_slots(list(range(len(w.prompt_lens))))
+    used = sorted({b for s in ids for b in m.block_table(s)})
+    kc = np.empty((w.num_blocks, H, B, D), np.float16)   # untouched pages stay unbacked
+    vc = np.empty_like(kc)
+    rng = wl.value_rng(w, 2)
+    for b in used:
+        kc[b] = wl.normal_f16(rng, (H, B, D))
+        vc[b] = wl.normal_f16(rng, (H, B, D))
+    mb = -(-wl.CTX_CAP // B)
+    tables = np.array(m.padded_tables(ids, mb), np.int32)
+    ctx = np.array([m.num_tokens(s) for s in ids], np.int32)
+    q = wl.normal_f16(rng, (n_seqs, H, D))
+    return q, kc, vc, tables, ctx, w.scale
+
+
+def cpu_baseline(seconds: float, n_seqs: int):
+    from oracle import attention as oa
+
+    q, kc, vc, tables, ctx, scale = _oracle_sample(n_seqs)
+    oa.paged_attention(q[:1], kc, vc, tables[:1], ctx[:1], scale)       # build + warm
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oa.paged_attention(q, kc, vc, tables, ctx, scale)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": passes * int(ctx.sum()) / dt, "unit": UNIT, "cores": oa.max_threads(),
+            "kind": "oracle",
+            "sample": f"first {n_seqs} of the 256 sequences (sum ctx {int(ctx.sum())}), "
+                      f"{passes} passes in {dt:.1f} s, fp64 C + OpenMP"}
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores, as the reference arm."""
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    from oracle import attention as oa
+
+    q, kc, vc, tables, ctx, scale = _oracle_sample(args.ref_seqs)
+    for _ in range(args.warmup):
+        oa.paged_attention(q, kc, vc, tables, ctx, scale)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oa.paged_attention(q, kc, vc, tables, ctx, scale)
+    dt = time.perf_counter() - t0
+    value = args.steps * int(ctx.sum()) / dt
+    sample = (f"first {args.ref_seqs} of the 256 sequences of the mixed batch (sum ctx "
+              f"{int(ctx.sum())}) per step; fp64 C oracle, OpenMP")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": "mixed-length serving batch (bounded sample)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oa.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=256)
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seqs", type=int, default=32)
+    ap.add_argument("--ref-seqs", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 paged KV cache decode-step library
+ * (libpagedkv.so).
+ *
+ * The library implements the data-parallel hot path of PagedAttention:
+ * a host-side block manager (free-block queue, per-block reference counts,
+ * per-sequence block tables with #filled, fork / append / free,
+ * copy-on-write of shared last blocks) and three sm_103a CUDA kernels that
+ * consume its output -- the fused slot write, the fused block copy and
+ * single-query paged decode attention with an optional split-context merge.
+ *
+ * Sources for the operations (pages are cited by title and section):
+ *   [review]   "Efficient Memory Management for Large Language Model Serving
+ *              with PagedAttention" paper review, mz-moonzoo.tistory.com/116
+ *   [tutorial] "KV 캐시 관리와 PagedAttention" (KV cache management and
+ *              PagedAttention), llm-systems-engineering.pages.dev/posts/paged-kv-cache
+ *   [teardown] vLLM PagedAttention teardown, arcyou.ai/ko/teardowns/vllm-paged-attention
+ *   [notes]    PagedAttention notes, unpurerationalist.github.io/posts/2026/11/3919429635
+ *
+ * Conventions
+ *   - Every function returns PA_OK (0) or a PA_ERR_* code; no exception or
+ *     longjmp crosses the ABI.  pa_last_error_string() describes the last
+ *     failure of the calling thread.
+ *   - Host pointers are marked (host), device pointers (device).  The caller
+ *     owns every buffer it passes, host or device, and the CUDA stream
+ *     (passed as void*, a cudaStream_t; NULL = the legacy default stream).
+ *     The library owns only the pa_pool object.
+ *   - Device calls validate their scalar arguments and pointer alignment on
+ *     the host, then enqueue work on the stream and return; they do not
+ *     synchronise.  Problems found by a kernel (a block id or slot outside
+ *     the pool, a wait that ran out) are reported through the optional
+ *     device status word: the kernel skips the bad access and stores the
+ *     error code there if it still holds 0.  The status word is never reset
+ *     by the library.
+ *   - Host block-manager calls are synchronous and not thread-safe for one
+ *     pool; different pools are independent.
+ *   - Cache layout, one K and one V array per layer, fp16:
+ *       cache[num_blocks][num_heads][block_size][head_dim]
+ *     so that one (block, head) pair is block_size*head_dim*2 contiguous
+ *     bytes.  New keys / values, queries and outputs are [n][num_heads][head_dim].
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define PA_OK                0
+#define PA_ERR_INVALID_ARG   1  /* bad scalar, shape, alignment or capacity    */
+#define PA_ERR_OUT_OF_BLOCKS 2  /* free queue cannot cover the request          */
+#define PA_ERR_NO_SEQ        3  /* unknown sequence id / id already in use      */
+#define PA_ERR_CUDA          4  /* a CUDA runtime call or launch failed         */
+#define PA_ERR_TIMEOUT       5  /* (device status) a bounded wait ran out       */
+#define PA_ERR_BAD_BLOCK     6  /* (device status) block id / slot outside pool */
+
+#define PA_DTYPE_F16 0
+
+/* Default split-context partition: a context longer than this many tokens
+ * is split into partitions of this size whose partial results are merged. */
+#define PA_DEFAULT_PARTITION_TOKENS 512
+
+/* Pool geometry, shared by the block manager and the device calls.
+ *   num_blocks        physical blocks in the pool (>= 0)
+ *   block_size        tokens per block B: 4, 8, 16 or 32 for the device calls
+ *                     (any value >= 1 for the host block manager)
+ *   num_layers        layers whose caches share the block ids (>= 1)
+ *   num_heads         attention heads H (>= 1)
+ *   head_dim          D: 8, 16, 32, 64, 128 or 256 for the device calls
+ *   dtype             PA_DTYPE_F16 (the only one)
+ *   partition_tokens  split-context partition size in tokens; 0 selects
+ *                     PA_DEFAULT_PARTITION_TOKENS; otherwise a positive
+ *                     multiple of block_size (a value at least as long as
+ *                     every context turns the split off)
+ *   free_order        (host, optional) initial order of the free-block queue,
+ *                     a permutation of 0..num_blocks-1; NULL = 0,1,2,...
+ *                     Read by pa_pool_create only.                          */
+typedef struct pa_pool_desc {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_layers;
+    int32_t num_heads;
+    int32_t head_dim;
+    int32_t dtype;
+    int32_t partition_tokens;
+    int32_t reserved;
+    const int32_t *free_order;
+} pa_pool_desc;
+
+typedef struct pa_pool pa_pool;
+
+/* Text of the calling thread's last error ("" if none).  The pointer stays
+ * valid until the thread's next failing call. */
+const char *pa_last_error_string(void);
+
+/* ---- host block manager ---------------------------------------------------
+ * A fixed pool of equal-size physical blocks, sized once at creation; new
+ * blocks are taken from the head of a FIFO free queue ([teardown]
+ * "PagedAttention" section; [review] §4.2).  Each sequence has a block table
+ * mapping its logical blocks to physical blocks; only its last block may be
+ * partly filled ([review] §4.3; [notes] §3.3).  Token position p of a sequence
+ * is stored in slot  table[p / B] * B + p % B  ([tutorial] Fig. 2). */
+
+/* Create a pool from *desc.  *out receives the handle.
+ * Errors: PA_ERR_INVALID_ARG (bad geometry, free_order not a permutation). */
+int pa_pool_create(const pa_pool_desc *desc, pa_pool **out);
+
+/* Destroy a pool (NULL is accepted). */
+int pa_pool_destroy(pa_pool *pool);
+
+/* Admit sequence seq_id with a prompt of n_tokens tokens: takes
+ * ceil(n_tokens / B) blocks from the free queue, in queue order
+ * ([review] §4.3, 7-token prompt example; [tutorial] Fig. 1).
+ * slots_out (host, optional, n_tokens entries) receives the slot of each
+ * prompt token.  All-or-nothing.
+ * Errors: PA_ERR_NO_SEQ (id in use), PA_ERR_OUT_OF_BLOCKS, PA_ERR_INVALID_ARG. */
+int pa_seq_add(pa_pool *pool, int32_t seq_id, int32_t n_tokens, int64_t *slots_out);
+
+/* fork: the child gets a copy of the parent's block table and length, and
+ * every block's reference count goes up by one ([notes] §4.2 fork;
+ * [review] §5 "Fork").  Errors: PA_ERR_NO_SEQ (no parent / child exists). */
+int pa_seq_fork(pa_pool *pool, int32_t parent, int32_t child);
+
+/* free: every block of the sequence loses one reference; a block whose count
+ * reaches 0 goes to the tail of the free queue.  Blocks are released from the
+ * sequence's last block backwards ([tutorial] "returning blocks after a
+ * request ends"; [notes] §3.4.2, §4.2; [teardown] tail blocks go first).
+ * Errors: PA_ERR_NO_SEQ. */
+int pa_seq_free(pa_pool *pool, int32_t seq_id);
+
+/* append, for a batch: one new token for each of seq_ids[0..n_seqs), handled
+ * in the order given ([review] §4.3 steps 1-2; [tutorial] Fig. 3, Fig. 6):
+ *   - no block yet, or the last block is full (shared or not): take a new
+ *     block from the free queue and append it to the table (no copy);
+ *   - last block partly filled and shared (count > 1): copy-on-write -- take
+ *     a new block, emit the pair (old, new) to copies_out, decrement the old
+ *     block's count and point the table's last entry at the new block;
+ *   - otherwise write in place.
+ * The token's slot goes to slot_mapping_out[i] (host, n_seqs entries).
+ * copies_out (host, copies_cap x 2 int32: src, dst) receives the block copies
+ * that must run (pa_copy_blocks) before the slot write (pa_write_kv);
+ * *n_copies_out their number.  A sequence may appear once per call.
+ * All-or-nothing: on PA_ERR_OUT_OF_BLOCKS (the queue cannot cover every new
+ * block) or a too-small copies_cap (PA_ERR_INVALID_ARG) nothing changes
+ * ([teardown]: allocate_slots reports failure, which the scheduler answers by
+ * preempting).  Errors: PA_ERR_NO_SEQ, PA_ERR_INVALID_ARG, PA_ERR_OUT_OF_BLOCKS. */
+int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                   int64_t *slot_mapping_out, int32_t *copies_out, int32_t copies_cap,
+                   int32_t *n_copies_out);
+
+/* Export block tables and context lengths for a batch, in the layout the
+ * attention kernel reads: tables_out (host, n_seqs x max_blocks int32,
+ * row-major) gets each sequence's physical block ids, padded with -1;
+ * ctx_lens_out (host, n_seqs int32) gets each sequence's token count.
+ * Errors: PA_ERR_NO_SEQ, PA_ERR_INVALID_ARG (a table longer than max_blocks;
+ * the outputs are then unspecified). */
+int pa_get_block_tables(const pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                        int32_t max_blocks, int32_t *tables_out, int32_t *ctx_lens_out);
+
+/* Introspection.  pa_seq_info: token count and table length of a sequence.
+ * pa_pool_num_free: blocks in the free queue.  pa_pool_free_queue: the
+ * queue from head to tail into out (host, cap entries), *n_out = its length
+ * (PA_ERR_INVALID_ARG if cap is too small).  pa_pool_refcounts: every
+ * block's reference count into out (host, num_blocks entries). */
+int pa_seq_info(const pa_pool *pool, int32_t seq_id, int32_t *num_tokens, int32_t *num_blocks);
+int pa_pool_num_free(const pa_pool *pool, int32_t *n_free);
+int pa_pool_free_queue(const pa_pool *pool, int32_t *out, int32_t cap, int32_t *n_out);
+int pa_pool_refcounts(const pa_pool *pool, int32_t *out);
+
+/* ---- device kernels -------------------------------------------------------
+ * All pointers below are device pointers unless marked (host).  Tensors must
+ * be contiguous and 16-byte aligned; desc supplies the geometry (its
+ * free_order is ignored).  status (device, optional, one int32) receives the
+ * first error a kernel detects; NULL disables reporting but not the checks. */
+
+/* Fused reshape and block write ([review] §5.1 (1); [notes] §4.1): for every
+ * token t < n_tokens and head h,
+ *     k_cache[slot / B][h][slot % B][:] = k[t][h][:],  same for v,
+ * with slot = slot_mapping[t] (int64).  A negative slot skips the token;
+ * a slot >= num_blocks * B is skipped and reported as PA_ERR_BAD_BLOCK.
+ * k, v: [n_tokens][num_heads][head_dim] fp16.  One layer per call.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_CUDA. */
+int pa_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32_t n_tokens,
+                void *k_cache, void *v_cache, const pa_pool_desc *desc,
+                int32_t *status, void *stream);
+
+/* Fused block copy for copy-on-write ([review] §5.1 (3); [notes] §4.1): for
+ * every pair (src, dst) in pairs (device, n_pairs x 2 int32) and every layer
+ * l < num_layers, block dst of k_caches[l] and v_caches[l] becomes a copy of
+ * block src, in one launch.  k_caches / v_caches are (host) arrays of
+ * num_layers device pointers (num_layers <= 128).  The destinations must be
+ * distinct and no destination may be the source of another pair (true of the
+ * pairs pa_alloc_slots emits: every destination is a newly taken block).
+ * Pairs outside the pool are skipped and reported as PA_ERR_BAD_BLOCK.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_CUDA. */
+int pa_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_layers,
+                   const int32_t *pairs, int32_t n_pairs, const pa_pool_desc *desc,
+                   int32_t *status, void *stream);
+
+/* Bytes of device workspace pa_decode_attention needs for a batch of n_seqs
+ * sequences whose tables have max_blocks columns (0 when no context can be
+ * longer than one partition). */
+size_t pa_decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_pool_desc *desc);
+
+/* Single-query paged decode attention ([notes] §3.1 blockwise attention
+ * equation; [review] §4.1 and §5.1 (2); [tutorial] Fig. 4): for every
+ * sequence s < n_seqs and head h,
+ *     o[s][h] = sum_{p < ctx} softmax_p(scale * q[s][h] . k_p) v_p,
+ * where k_p, v_p are read from physical block block_tables[s][p / B] at
+ * offset p % B and ctx = ctx_lens[s] counts every stored token of the
+ * sequence, the one written in this step included.  Slots past ctx are never
+ * used.  ctx = 0 gives o = 0.  Contexts longer than partition_tokens are
+ * split into partitions whose partial (max, sum, unnormalised output) go to
+ * the workspace and are merged by a second kernel; results agree with the
+ * unsplit sum to rounding.
+ *   out, q        [n_seqs][num_heads][head_dim] fp16
+ *   k_cache, v_cache  one layer, layout above
+ *   block_tables  [n_seqs][max_blocks] int32 (entries past ceil(ctx/B) unread)
+ *   ctx_lens      [n_seqs] int32, each <= max_blocks * B
+ *   workspace     >= pa_decode_workspace_bytes(n_seqs, max_blocks, desc)
+ *                 bytes, 256-byte aligned (may be NULL when that is 0); its
+ *                 contents need no initialisation and are not preserved.
+ * Errors: PA_ERR_INVALID_ARG, PA_ERR_CUDA. */
+int pa_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,
+                        int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
+                        int32_t *status, const pa_pool_desc *desc, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,261 @@
+"""GB300 paged KV cache decode step: thin Python binding of libpagedkv.so.
+
+Every function here has the name of the C entry point it calls
+(``include/pagedkv.h``) and only marshals arguments: host arrays go in as
+numpy arrays, device buffers as CUDA torch tensors (or raw device addresses),
+streams as torch streams (default: torch's current stream).  All the work --
+block management on the host, slot write, block copy and decode attention on
+the GPU -- runs in the library.  There is no fallback: if the library is
+missing, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_OUT_OF_BLOCKS = 2
+PA_ERR_NO_SEQ = 3
+PA_ERR_CUDA = 4
+PA_ERR_TIMEOUT = 5
+PA_ERR_BAD_BLOCK = 6
+PA_DTYPE_F16 = 0
+PA_DEFAULT_PARTITION_TOKENS = 512
+
+_ERR_NAMES = {1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_OUT_OF_BLOCKS", 3: "PA_ERR_NO_SEQ",
+              4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_BAD_BLOCK"}
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{_ERR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class OutOfBlocks(PagedKVError):
+    pass
+
+
+class pa_pool_desc(ctypes.Structure):
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_layers", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("partition_tokens", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("free_order", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or python paged_kv_cache_106_gb300/_build.py)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "pa_last_error_string": (ctypes.c_char_p, []),
+        "pa_pool_create": (i32, [P(pa_pool_desc), P(vp)]),
+        "pa_pool_destroy": (i32, [vp]),
+        "pa_seq_add": (i32, [vp, i32, i32, vp]),
+        "pa_seq_fork": (i32, [vp, i32, i32]),
+        "pa_seq_free": (i32, [vp, i32]),
+        "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
+        "pa_get_block_tables": (i32, [vp, i32, vp, i32, vp, vp]),
+        "pa_seq_info": (i32, [vp, i32, P(i32), P(i32)]),
+        "pa_pool_num_free": (i32, [vp, P(i32)]),
+        "pa_pool_free_queue": (i32, [vp, vp, i32, P(i32)]),
+        "pa_pool_refcounts": (i32, [vp, vp]),
+        "pa_write_kv": (i32, [vp, vp, vp, i32, vp, vp, P(pa_pool_desc), vp, vp]),
+        "pa_copy_blocks": (i32, [vp, vp, i32, vp, i32, P(pa_pool_desc), vp, vp]),
+        "pa_decode_workspace_bytes": (sz, [i32, i32, P(pa_pool_desc)]),
+        "pa_decode_attention": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, vp, sz,
+                                      vp, P(pa_pool_desc), vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+LIB_PATH = _LIB_PATH
+
+
+def pa_last_error_string() -> str:
+    return _lib.pa_last_error_string().decode()
+
+
+def _check(rc: int):
+    if rc != PA_OK:
+        msg = pa_last_error_string()
+        if rc == PA_ERR_OUT_OF_BLOCKS:
+            raise OutOfBlocks(rc, msg)
+        raise PagedKVError(rc, msg)
+
+
+def _host_i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _dev(x):
+    """Device address of a CUDA tensor (or an int address / None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class PoolDesc:
+    """Holds a pa_pool_desc (and keeps its free_order array alive)."""
+
+    def __init__(self, num_blocks, block_size, num_layers=1, num_heads=1, head_dim=8,
+                 partition_tokens=0, free_order=None):
+        self._free = None if free_order is None else _host_i32(free_order)
+        self.c = pa_pool_desc(int(num_blocks), int(block_size), int(num_layers), int(num_heads),
+                              int(head_dim), PA_DTYPE_F16, int(partition_tokens), 0,
+                              None if self._free is None else
+                              self._free.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
+
+    def __getattr__(self, name):
+        return getattr(self.__dict__["c"], name)
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+# ---------------------------------------------------------------- host calls
+def pa_pool_create(desc: PoolDesc):
+    h = ctypes.c_void_p()
+    _check(_lib.pa_pool_create(desc.ref, ctypes.byref(h)))
+    return h
+
+
+def pa_pool_destroy(pool) -> None:
+    _check(_lib.pa_pool_destroy(pool))
+
+
+def pa_seq_add(pool, seq_id: int, n_tokens: int, want_slots: bool = True):
+    slots = np.empty(max(int(n_tokens), 0), np.int64) if want_slots else None
+    _check(_lib.pa_seq_add(pool, int(seq_id), int(n_tokens),
+                           None if slots is None else slots.ctypes.data))
+    return slots
+
+
+def pa_seq_fork(pool, parent: int, child: int) -> None:
+    _check(_lib.pa_seq_fork(pool, int(parent), int(child)))
+
+
+def pa_seq_free(pool, seq_id: int) -> None:
+    _check(_lib.pa_seq_free(pool, int(seq_id)))
+
+
+def pa_alloc_slots(pool, seq_ids, copies_cap: int | None = None, slot_out=None, copies_out=None):
+    """Returns (slot_mapping int64[n], copies int32[n_copies, 2])."""
+    ids = _host_i32(seq_ids)
+    n = ids.shape[0]
+    cap = n if copies_cap is None else int(copies_cap)
+    slots = np.empty(n, np.int64) if slot_out is None else slot_out
+    copies = np.empty((max(cap, 1), 2), np.int32) if copies_out is None else copies_out
+    nc = ctypes.c_int32(0)
+    _check(_lib.pa_alloc_slots(pool, n, ids.ctypes.data, slots.ctypes.data, copies.ctypes.data,
+                               cap, ctypes.byref(nc)))
+    return slots, copies[: nc.value]
+
+
+def pa_get_block_tables(pool, seq_ids, max_blocks: int, tables_out=None, ctx_out=None):
+    """Returns (tables int32[n, max_blocks] padded with -1, ctx_lens int32[n])."""
+    ids = _host_i32(seq_ids)
+    n = ids.shape[0]
+    tables = np.empty((n, max_blocks), np.int32) if tables_out is None else tables_out
+    ctx = np.empty(n, np.int32) if ctx_out is None else ctx_out
+    _check(_lib.pa_get_block_tables(pool, n, ids.ctypes.data, int(max_blocks),
+                                    tables.ctypes.data, ctx.ctypes.data))
+    return tables, ctx
+
+
+def pa_seq_info(pool, seq_id: int):
+    nt, nb = ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.pa_seq_info(pool, int(seq_id), ctypes.byref(nt), ctypes.byref(nb)))
+    return nt.value, nb.value
+
+
+def pa_pool_num_free(pool) -> int:
+    n = ctypes.c_int32()
+    _check(_lib.pa_pool_num_free(pool, ctypes.byref(n)))
+    return n.value
+
+
+def pa_pool_free_queue(pool, num_blocks: int):
+    out = np.empty(max(int(num_blocks), 1), np.int32)
+    n = ctypes.c_int32()
+    _check(_lib.pa_pool_free_queue(pool, out.ctypes.data, int(num_blocks), ctypes.byref(n)))
+    return out[: n.value]
+
+
+def pa_pool_refcounts(pool, num_blocks: int):
+    out = np.empty(max(int(num_blocks), 1), np.int32)
+    _check(_lib.pa_pool_refcounts(pool, out.ctypes.data))
+    return out[: int(num_blocks)]
+
+
+# -------------------------------------------------------------- device calls
+def pa_write_kv(k, v, slot_mapping, k_cache, v_cache, desc: PoolDesc, status=None,
+                stream=None, n_tokens: int | None = None) -> None:
+    n = int(slot_mapping.shape[0]) if n_tokens is None else int(n_tokens)
+    _check(_lib.pa_write_kv(_dev(k), _dev(v), _dev(slot_mapping), n, _dev(k_cache),
+                            _dev(v_cache), desc.ref, _dev(status), _stream(stream)))
+
+
+def pa_copy_blocks(k_caches, v_caches, pairs, desc: PoolDesc, status=None, stream=None,
+                   n_pairs: int | None = None) -> None:
+    L = len(k_caches)
+    kp = (ctypes.c_void_p * L)(*[_dev(x) for x in k_caches])
+    vp = (ctypes.c_void_p * L)(*[_dev(x) for x in v_caches])
+    n = int(pairs.shape[0]) if n_pairs is None else int(n_pairs)
+    _check(_lib.pa_copy_blocks(kp, vp, L, _dev(pairs), n, desc.ref, _dev(status),
+                               _stream(stream)))
+
+
+def pa_decode_workspace_bytes(n_seqs: int, max_blocks: int, desc: PoolDesc) -> int:
+    return int(_lib.pa_decode_workspace_bytes(int(n_seqs), int(max_blocks), desc.ref))
+
+
+def pa_decode_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, scale: float,
+                        desc: PoolDesc, workspace=None, status=None, stream=None,
+                        n_seqs: int | None = None, max_blocks: int | None = None) -> None:
+    n = int(q.shape[0]) if n_seqs is None else int(n_seqs)
+    mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_attention(_dev(out), _dev(q), _dev(k_cache), _dev(v_cache),
+                                    _dev(block_tables), _dev(ctx_lens), n, mb,
+                                    ctypes.c_float(scale), _dev(workspace), ws_bytes,
+                                    _dev(status), desc.ref, _stream(stream)))

@@ -1,0 +1,85 @@
+"""Builds libpagedkv.so in-tree with nvcc for sm_103a.
+
+Each translation unit compiles in its own nvcc process (in parallel), then
+one link step produces ``paged_kv_cache_106_gb300/libpagedkv.so`` with the
+CUDA runtime linked statically, so the library loads (and its host-only
+block-manager calls work) on machines without a GPU.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+LIB = os.path.join(PKG, "libpagedkv.so")
+OBJ = os.path.join(PKG, "_build")
+HEADERS = [os.path.join(ROOT, "include", "pagedkv.h")]
+SOURCES = ["pool.cpp", "api.cpp", "write_kv.cu", "copy_blocks.cu", "decode_attention.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc_path() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libpagedkv.so")
+
+
+def _inputs():
+    srcs = [os.path.join(CSRC, s) for s in SOURCES]
+    deps = srcs + HEADERS + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                             if f.endswith((".h", ".cuh"))]
+    return srcs, deps
+
+
+def _stale(out, deps) -> bool:
+    if not os.path.exists(out):
+        return True
+    t = os.path.getmtime(out)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: bool = False) -> str:
+    """Compile and link the library; returns its path.  ``extra_flags`` go to
+    every nvcc compile (e.g. ``-DPA_TUNE_WARPS=4``); with ``out`` the library
+    is written elsewhere (objects go to a directory next to it)."""
+    out = out or LIB
+    objdir = OBJ if out == LIB else out + ".objs"
+    srcs, deps = _inputs()
+    if not force and not extra_flags and not _stale(out, deps + [os.path.abspath(__file__)]):
+        return out
+    os.makedirs(objdir, exist_ok=True)
+    nvcc = nvcc_path()
+    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=default",
+              "--expt-relaxed-constexpr", *ARCH, *extra_flags]
+
+    def compile_one(src):
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
+        cmd = [nvcc, *common, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{res.stdout}\n{res.stderr}")
+        if verbose and res.stderr:
+            print(res.stderr, file=sys.stderr)
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError(f"nvcc link failed:\n{res.stdout}\n{res.stderr}")
+    os.replace(tmp, out)
+    return out
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True))

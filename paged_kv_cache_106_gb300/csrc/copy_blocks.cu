@@ -1,0 +1,90 @@
+// Fused block copy (vLLM paper review, mz-moonzoo.tistory.com/116, §5.1 (3);
+// PagedAttention notes, unpurerationalist.github.io, §4.1): the copies that
+// copy-on-write asks for -- whole physical blocks, every layer, keys and
+// values -- in one launch instead of one cudaMemcpyAsync per block.
+//
+// grid = (vector chunk, pair, layer * 2 + {K, V}); each thread moves 16-byte
+// vectors of one block of one layer's K or V cache.  A block of one layer is
+// H * B * D * 2 contiguous bytes in the cache layout [num_blocks][H][B][D].
+#include <cuda_runtime.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pagedkv {
+
+namespace {
+
+constexpr int kMaxLayers = 128;
+
+struct LayerPtrs {
+    uint4 *k[kMaxLayers];
+    uint4 *v[kMaxLayers];
+};
+
+constexpr int kVecPerThread = 4;
+
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(const __grid_constant__ LayerPtrs ptrs, const int32_t *__restrict__ pairs,
+                   int32_t n_pairs, int64_t vec_per_block, int32_t num_blocks, int32_t *status) {
+    const int layer = blockIdx.z >> 1;
+    uint4 *cache = (blockIdx.z & 1) ? ptrs.v[layer] : ptrs.k[layer];
+    for (int32_t pi = blockIdx.y; pi < n_pairs; pi += gridDim.y) {
+        const int32_t src = pairs[2 * pi];
+        const int32_t dst = pairs[2 * pi + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) report(status, PA_ERR_BAD_BLOCK);
+            continue;
+        }
+        const uint4 *s = cache + (int64_t)src * vec_per_block;
+        uint4 *d = cache + (int64_t)dst * vec_per_block;
+        const int64_t base = (int64_t)blockIdx.x * blockDim.x * kVecPerThread + threadIdx.x;
+        uint4 tmp[kVecPerThread];
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int64_t e = base + (int64_t)u * blockDim.x;
+            if (e < vec_per_block) tmp[u] = s[e];
+        }
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int64_t e = base + (int64_t)u * blockDim.x;
+            if (e < vec_per_block) d[e] = tmp[u];
+        }
+    }
+}
+
+}  // namespace
+
+int launch_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_layers,
+                       const int32_t *pairs, int32_t n_pairs, const pa_pool_desc *d,
+                       int32_t *status, void *stream) {
+    std::string why;
+    if (!d) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL desc");
+    if (!device_geometry_ok(d, &why))
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: %s", why.c_str());
+    if (n_pairs < 0 || num_layers < 1 || num_layers > kMaxLayers)
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: n_pairs=%d, num_layers=%d (1..%d)",
+                    n_pairs, num_layers, kMaxLayers);
+    if (n_pairs == 0) return PA_OK;
+    if (!k_caches || !v_caches || !pairs) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL pointer");
+    LayerPtrs lp{};
+    for (int l = 0; l < num_layers; ++l) {
+        if (!k_caches[l] || !v_caches[l] || (reinterpret_cast<uintptr_t>(k_caches[l]) & 15) ||
+            (reinterpret_cast<uintptr_t>(v_caches[l]) & 15))
+            return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: layer %d cache NULL or misaligned", l);
+        lp.k[l] = static_cast<uint4 *>(k_caches[l]);
+        lp.v[l] = static_cast<uint4 *>(v_caches[l]);
+    }
+    const int64_t vec_per_block = (int64_t)d->num_heads * d->block_size * d->head_dim / 8;
+    const int64_t per_cta = 256 * kVecPerThread;
+    dim3 grid((unsigned)((vec_per_block + per_cta - 1) / per_cta),
+              (unsigned)(n_pairs < 65535 ? n_pairs : 65535), (unsigned)(2 * num_layers));
+    copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        lp, pairs, n_pairs, vec_per_block, d->num_blocks, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "pa_copy_blocks: launch: %s", cudaGetErrorString(e));
+    return PA_OK;
+}
+
+}  // namespace pagedkv

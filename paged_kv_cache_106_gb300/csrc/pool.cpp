@@ -1,0 +1,294 @@
+// Host-side block manager of the paged KV cache: a fixed pool of physical
+// blocks, a FIFO free-block queue, a reference count per physical block and
+// one block table per sequence, with fork / append / free and copy-on-write
+// of a shared, partly filled last block.
+//
+// Steps follow the pages:
+//  - pool sized once, blocks taken from the head of a free queue (vLLM
+//    teardown, arcyou.ai, "PagedAttention" section; vLLM paper review,
+//    mz-moonzoo.tistory.com/116, §4.2);
+//  - on-demand growth: a prompt of n tokens takes ceil(n/B) blocks; a new
+//    token fills the last block's free slot, else a new block is appended
+//    (review §4.3 decoding example; KV cache management and PagedAttention
+//    tutorial, llm-systems-engineering.pages.dev, Fig. 1-3);
+//  - slot of position p: table[p / B] * B + p % B (tutorial, Fig. 2);
+//  - copy-on-write on a shared partly filled last block, a shared full block
+//    is never copied, the last holder writes in place (tutorial, Fig. 5-6;
+//    PagedAttention notes, unpurerationalist.github.io, §3.4.1);
+//  - free drops one reference per block and returns blocks at count 0, tail
+//    blocks first (tutorial, "returning blocks"; notes §3.4.2, §4.2;
+//    teardown, "when blocks run out");
+//  - an allocation the queue cannot cover fails with no change (teardown:
+//    allocate_slots returns None).
+//
+// A sequence's #filled is kept as its token count: every table entry but
+// the last holds B tokens, the last holds num_tokens - (entries - 1) * B.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+#include "pa_internal.h"
+
+namespace {
+
+struct Seq {
+    std::vector<int32_t> table;
+    int32_t num_tokens = 0;
+};
+
+}  // namespace
+
+struct pa_pool {
+    int32_t num_blocks = 0;
+    int32_t block_size = 1;
+    pa_pool_desc desc{};
+    // FIFO free queue as a ring over num_blocks entries.
+    std::vector<int32_t> ring;
+    int64_t head = 0;
+    int64_t count = 0;
+    std::vector<int32_t> ref;
+    std::unordered_map<int32_t, Seq> seqs;
+
+    int32_t pop_free() {
+        int32_t b = ring[(size_t)(head % num_blocks)];
+        head = (head + 1) % num_blocks;
+        --count;
+        ref[b] = 1;
+        return b;
+    }
+    void push_free(int32_t b) {
+        ring[(size_t)((head + count) % num_blocks)] = b;
+        ++count;
+    }
+    void release(int32_t b) {
+        if (--ref[b] == 0) push_free(b);
+    }
+    int32_t last_filled(const Seq &s) const {
+        return s.num_tokens - (int32_t)(s.table.size() - 1) * block_size;
+    }
+};
+
+using pagedkv::fail;
+
+extern "C" {
+
+int pa_pool_create(const pa_pool_desc *desc, pa_pool **out) {
+    if (!desc || !out) return fail(PA_ERR_INVALID_ARG, "pa_pool_create: NULL argument");
+    *out = nullptr;
+    if (desc->num_blocks < 0 || desc->block_size < 1 || desc->num_layers < 1 ||
+        desc->num_heads < 1 || desc->head_dim < 1 || desc->dtype != PA_DTYPE_F16)
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_pool_create: bad geometry (num_blocks=%d block_size=%d num_layers=%d "
+                    "num_heads=%d head_dim=%d dtype=%d)",
+                    desc->num_blocks, desc->block_size, desc->num_layers, desc->num_heads,
+                    desc->head_dim, desc->dtype);
+    pa_pool *p = new (std::nothrow) pa_pool();
+    if (!p) return fail(PA_ERR_INVALID_ARG, "pa_pool_create: out of host memory");
+    p->num_blocks = desc->num_blocks;
+    p->block_size = desc->block_size;
+    p->desc = *desc;
+    p->desc.free_order = nullptr;
+    p->ring.resize((size_t)desc->num_blocks);
+    p->ref.assign((size_t)desc->num_blocks, 0);
+    if (desc->free_order) {
+        std::vector<char> seen((size_t)desc->num_blocks, 0);
+        for (int32_t i = 0; i < desc->num_blocks; ++i) {
+            int32_t b = desc->free_order[i];
+            if (b < 0 || b >= desc->num_blocks || seen[(size_t)b]) {
+                delete p;
+                return fail(PA_ERR_INVALID_ARG,
+                            "pa_pool_create: free_order is not a permutation (entry %d = %d)", i,
+                            b);
+            }
+            seen[(size_t)b] = 1;
+            p->ring[(size_t)i] = b;
+        }
+    } else {
+        for (int32_t i = 0; i < desc->num_blocks; ++i) p->ring[(size_t)i] = i;
+    }
+    p->count = desc->num_blocks;
+    *out = p;
+    return PA_OK;
+}
+
+int pa_pool_destroy(pa_pool *pool) {
+    delete pool;
+    return PA_OK;
+}
+
+int pa_seq_add(pa_pool *pool, int32_t seq_id, int32_t n_tokens, int64_t *slots_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_add: NULL pool");
+    if (n_tokens < 0) return fail(PA_ERR_INVALID_ARG, "pa_seq_add: n_tokens < 0");
+    if (pool->seqs.count(seq_id))
+        return fail(PA_ERR_NO_SEQ, "pa_seq_add: sequence %d already exists", seq_id);
+    const int32_t B = pool->block_size;
+    int64_t need = ((int64_t)n_tokens + B - 1) / B;
+    if (need > pool->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "pa_seq_add: need %lld blocks, %lld free",
+                    (long long)need, (long long)pool->count);
+    Seq s;
+    s.table.reserve((size_t)need);
+    for (int64_t i = 0; i < need; ++i) s.table.push_back(pool->pop_free());
+    s.num_tokens = n_tokens;
+    if (slots_out)
+        for (int32_t p = 0; p < n_tokens; ++p)
+            slots_out[p] = (int64_t)s.table[(size_t)(p / B)] * B + p % B;
+    pool->seqs.emplace(seq_id, std::move(s));
+    return PA_OK;
+}
+
+int pa_seq_fork(pa_pool *pool, int32_t parent, int32_t child) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_fork: NULL pool");
+    auto it = pool->seqs.find(parent);
+    if (it == pool->seqs.end()) return fail(PA_ERR_NO_SEQ, "pa_seq_fork: no sequence %d", parent);
+    if (pool->seqs.count(child))
+        return fail(PA_ERR_NO_SEQ, "pa_seq_fork: sequence %d already exists", child);
+    Seq c = it->second;
+    for (int32_t b : c.table) ++pool->ref[(size_t)b];
+    pool->seqs.emplace(child, std::move(c));
+    return PA_OK;
+}
+
+int pa_seq_free(pa_pool *pool, int32_t seq_id) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_free: NULL pool");
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end()) return fail(PA_ERR_NO_SEQ, "pa_seq_free: no sequence %d", seq_id);
+    const std::vector<int32_t> &t = it->second.table;
+    for (size_t i = t.size(); i-- > 0;) pool->release(t[i]);
+    pool->seqs.erase(it);
+    return PA_OK;
+}
+
+int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                   int64_t *slot_mapping_out, int32_t *copies_out, int32_t copies_cap,
+                   int32_t *n_copies_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: NULL pool");
+    if (n_seqs < 0 || (n_seqs > 0 && (!seq_ids || !slot_mapping_out)) || copies_cap < 0 ||
+        (copies_cap > 0 && !copies_out))
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: bad arguments");
+    const int32_t B = pool->block_size;
+    // Dry run: the blocks and copies this call needs.  Only the reference
+    // counts of shared last blocks change between the sequences of one call
+    // (each sequence appears once, new blocks belong to one sequence), so
+    // tracking those decrements reproduces the real pass exactly.
+    std::vector<Seq *> seq(static_cast<size_t>(n_seqs));
+    std::unordered_set<int32_t> ids;
+    std::unordered_map<int32_t, int32_t> dec;
+    ids.reserve((size_t)n_seqs * 2);
+    int64_t need = 0;
+    int32_t n_copies = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        auto it = pool->seqs.find(seq_ids[i]);
+        if (it == pool->seqs.end())
+            return fail(PA_ERR_NO_SEQ, "pa_alloc_slots: no sequence %d", seq_ids[i]);
+        if (!ids.insert(seq_ids[i]).second)
+            return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: sequence %d listed twice",
+                        seq_ids[i]);
+        Seq &s = it->second;
+        seq[(size_t)i] = &s;
+        if (s.table.empty() || pool->last_filled(s) == B) {
+            ++need;
+        } else {
+            int32_t last = s.table.back();
+            int32_t &d = dec[last];
+            if (pool->ref[(size_t)last] - d > 1) {
+                ++need;
+                ++n_copies;
+                ++d;
+            }
+        }
+    }
+    if (need > pool->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "pa_alloc_slots: need %lld blocks, %lld free",
+                    (long long)need, (long long)pool->count);
+    if (n_copies > copies_cap)
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: %d copies needed, copies_cap is %d",
+                    n_copies, copies_cap);
+    // Real pass.
+    int32_t c = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        Seq &s = *seq[(size_t)i];
+        if (s.table.empty() || pool->last_filled(s) == B) {
+            s.table.push_back(pool->pop_free());
+        } else {
+            int32_t last = s.table.back();
+            if (pool->ref[(size_t)last] > 1) {
+                int32_t nb = pool->pop_free();
+                copies_out[2 * c] = last;
+                copies_out[2 * c + 1] = nb;
+                ++c;
+                --pool->ref[(size_t)last];
+                s.table.back() = nb;
+            }
+        }
+        int32_t off = s.num_tokens - (int32_t)(s.table.size() - 1) * B;
+        slot_mapping_out[i] = (int64_t)s.table.back() * B + off;
+        ++s.num_tokens;
+    }
+    if (n_copies_out) *n_copies_out = c;
+    return PA_OK;
+}
+
+int pa_get_block_tables(const pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                        int32_t max_blocks, int32_t *tables_out, int32_t *ctx_lens_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_get_block_tables: NULL pool");
+    if (n_seqs < 0 || max_blocks < 0 ||
+        (n_seqs > 0 && (!seq_ids || (max_blocks > 0 && !tables_out))))
+        return fail(PA_ERR_INVALID_ARG, "pa_get_block_tables: bad arguments");
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        auto it = pool->seqs.find(seq_ids[i]);
+        if (it == pool->seqs.end())
+            return fail(PA_ERR_NO_SEQ, "pa_get_block_tables: no sequence %d", seq_ids[i]);
+        const Seq &s = it->second;
+        if ((int64_t)s.table.size() > max_blocks)
+            return fail(PA_ERR_INVALID_ARG,
+                        "pa_get_block_tables: sequence %d has %zu blocks > max_blocks %d",
+                        seq_ids[i], s.table.size(), max_blocks);
+        int32_t *row = tables_out + (int64_t)i * max_blocks;
+        size_t n = s.table.size();
+        if (n) std::memcpy(row, s.table.data(), n * sizeof(int32_t));
+        for (int32_t j = (int32_t)n; j < max_blocks; ++j) row[j] = -1;
+        if (ctx_lens_out) ctx_lens_out[i] = s.num_tokens;
+    }
+    return PA_OK;
+}
+
+int pa_seq_info(const pa_pool *pool, int32_t seq_id, int32_t *num_tokens, int32_t *num_blocks) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_info: NULL pool");
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end()) return fail(PA_ERR_NO_SEQ, "pa_seq_info: no sequence %d", seq_id);
+    if (num_tokens) *num_tokens = it->second.num_tokens;
+    if (num_blocks) *num_blocks = (int32_t)it->second.table.size();
+    return PA_OK;
+}
+
+int pa_pool_num_free(const pa_pool *pool, int32_t *n_free) {
+    if (!pool || !n_free) return fail(PA_ERR_INVALID_ARG, "pa_pool_num_free: NULL argument");
+    *n_free = (int32_t)pool->count;
+    return PA_OK;
+}
+
+int pa_pool_free_queue(const pa_pool *pool, int32_t *out, int32_t cap, int32_t *n_out) {
+    if (!pool || (!out && cap > 0) || cap < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_pool_free_queue: bad arguments");
+    if (n_out) *n_out = (int32_t)pool->count;
+    if (pool->count > cap)
+        return fail(PA_ERR_INVALID_ARG, "pa_pool_free_queue: cap %d < queue length %lld", cap,
+                    (long long)pool->count);
+    for (int64_t i = 0; i < pool->count; ++i)
+        out[i] = pool->ring[(size_t)((pool->head + i) % pool->num_blocks)];
+    return PA_OK;
+}
+
+int pa_pool_refcounts(const pa_pool *pool, int32_t *out) {
+    if (!pool || (!out && pool->num_blocks > 0))
+        return fail(PA_ERR_INVALID_ARG, "pa_pool_refcounts: NULL argument");
+    if (pool->num_blocks)
+        std::memcpy(out, pool->ref.data(), sizeof(int32_t) * (size_t)pool->num_blocks);
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,108 @@
+"""One decode step of a batch through the library, as a serving loop runs it.
+
+Per step (vLLM paper review, mz-moonzoo.tistory.com/116, §4.3 global
+execution loop; §4.6: the scheduler hands block tables to the worker):
+
+1. ``pa_alloc_slots``      host block manager: one slot per sequence, plus
+                           the copy-on-write pairs;
+2. ``pa_get_block_tables`` host: tables and context lengths for the batch;
+3. one pinned host -> device copy carrying slot mapping, context lengths,
+   block tables and copy pairs (double-buffered staging, so the host can
+   prepare step t+1 while the GPU still runs step t);
+4. ``pa_copy_blocks``      copy-on-write copies, every layer (only if any);
+5. per layer ``pa_write_kv`` then ``pa_decode_attention``.
+
+Everything is enqueued on one stream.  This module only sequences library
+calls and owns the staging buffers; the work runs in libpagedkv.so.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (PoolDesc, pa_alloc_slots, pa_copy_blocks, pa_decode_attention,
+               pa_decode_workspace_bytes, pa_get_block_tables, pa_write_kv)
+
+
+def _align(x, a=256):
+    return (x + a - 1) // a * a
+
+
+class DecodeStepRunner:
+    def __init__(self, pool, desc: PoolDesc, seq_ids, max_blocks: int, device="cuda",
+                 stream: torch.cuda.Stream | None = None):
+        self.pool = pool
+        self.desc = desc
+        self.ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        self.S = int(self.ids.shape[0])
+        self.max_blocks = int(max_blocks)
+        self.device = torch.device(device)
+        self.stream = stream or torch.cuda.current_stream(self.device)
+        S, MB = self.S, self.max_blocks
+        # packed metadata: slots int64[S] | ctx int32[S] | tables int32[S, MB] | copies int32[S, 2]
+        self.off_slots = 0
+        self.off_ctx = _align(8 * S)
+        self.off_tab = self.off_ctx + _align(4 * S)
+        self.off_cp = self.off_tab + _align(4 * S * MB)
+        self.nbytes = self.off_cp + _align(8 * S)
+        self.host = [torch.empty(self.nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        self.events = [None, None]
+        self.dev = torch.empty(self.nbytes, dtype=torch.uint8, device=self.device)
+        self.d_slots = self.dev[self.off_slots:self.off_slots + 8 * S].view(torch.int64)
+        self.d_ctx = self.dev[self.off_ctx:self.off_ctx + 4 * S].view(torch.int32)
+        self.d_tables = self.dev[self.off_tab:self.off_tab + 4 * S * MB].view(torch.int32).view(S, MB)
+        self.d_copies = self.dev[self.off_cp:self.off_cp + 8 * S].view(torch.int32).view(S, 2)
+        ws = pa_decode_workspace_bytes(S, MB, desc)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device) if ws else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.n_copies = 0
+        self.ctx_host = None
+        self.i = 0
+
+    def _views(self, buf):
+        a = buf.numpy()
+        S, MB = self.S, self.max_blocks
+        return (a[self.off_slots:self.off_slots + 8 * S].view(np.int64),
+                a[self.off_ctx:self.off_ctx + 4 * S].view(np.int32),
+                a[self.off_tab:self.off_tab + 4 * S * MB].view(np.int32).reshape(S, MB),
+                a[self.off_cp:self.off_cp + 8 * S].view(np.int32).reshape(S, 2))
+
+    def prepare(self) -> int:
+        """Host bookkeeping for one step and the upload of its metadata."""
+        k = self.i & 1
+        self.i += 1
+        if self.events[k] is not None:
+            self.events[k].synchronize()     # staging buffer k no longer in flight
+        slots, ctx, tables, copies = self._views(self.host[k])
+        _, cp = pa_alloc_slots(self.pool, self.ids, copies_cap=self.S, slot_out=slots,
+                               copies_out=copies)
+        self.n_copies = int(cp.shape[0])
+        pa_get_block_tables(self.pool, self.ids, self.max_blocks, tables_out=tables, ctx_out=ctx)
+        self.ctx_host = ctx
+        with torch.cuda.stream(self.stream):
+            self.dev.copy_(self.host[k], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(self.stream)
+        self.events[k] = ev
+        return self.n_copies
+
+    def copy_blocks(self, k_caches, v_caches):
+        if self.n_copies:
+            pa_copy_blocks(k_caches, v_caches, self.d_copies, self.desc, status=self.status,
+                           stream=self.stream, n_pairs=self.n_copies)
+
+    def write_kv(self, k_new, v_new, k_cache, v_cache):
+        pa_write_kv(k_new, v_new, self.d_slots, k_cache, v_cache, self.desc, status=self.status,
+                    stream=self.stream)
+
+    def attention(self, out, q, k_cache, v_cache, scale: float):
+        pa_decode_attention(out, q, k_cache, v_cache, self.d_tables, self.d_ctx, scale, self.desc,
+                            workspace=self.workspace, status=self.status, stream=self.stream)
+
+    def step(self, q, k_new, v_new, out, k_caches, v_caches, scale: float):
+        """A whole decode step over all layers (lists of per-layer tensors)."""
+        self.prepare()
+        self.copy_blocks(k_caches, v_caches)
+        for l in range(len(k_caches)):
+            self.write_kv(k_new[l], v_new[l], k_caches[l], v_caches[l])
+            self.attention(out[l], q[l], k_caches[l], v_caches[l], scale)

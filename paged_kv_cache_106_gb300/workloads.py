@@ -63,6 +63,8 @@ class DecodeWorkload:
     shared_prefix: list = field(default_factory=list)
     decode_steps: int = 1
     split_tokens: int = 512            # context partition of the split path
+    # total length at which each root sequence finishes (steady-state runs)
+    targets: list = field(default_factory=list)
 
     @property
     def scale(self) -> float:
@@ -132,21 +134,40 @@ def parallel_sampling(seed: int = 108, prompts: int = 16, samples: int = 4,
     )
 
 
-def mixed_b256(seed: int = 109, batch: int = 256, growth_steps: int = 64) -> DecodeWorkload:
-    """Mixed-length serving batch; the pool leaves room for ``growth_steps`` more tokens."""
+def mixed_b256(seed: int = 109, batch: int = 256, growth_steps: int = 64,
+               steady_state: bool = False) -> DecodeWorkload:
+    """Mixed-length serving batch.
+
+    Each sequence sits at a uniformly drawn point 1..output of its
+    generation; its target (prompt + output, capped at 2048) is where it
+    finishes.  The pool leaves room for ``growth_steps`` more tokens per
+    sequence, or, with ``steady_state``, for every sequence at the cap (so a
+    continuous batch that replaces finished sequences never runs out).
+    """
     rng = _rng(seed)
     prompt = _lognormal_lengths(rng, batch, 200, 1536)
     output = _lognormal_lengths(rng, batch, 250, 1 << 30)
-    # each sequence sits at a uniformly drawn point 1..output of its generation
     done = np.array([rng.integers(1, o, endpoint=True) for o in output], dtype=np.int64)
     ctx = np.minimum(prompt + done, CTX_CAP)
-    need = sum(_blocks(c + growth_steps, DEFAULT_BLOCK) for c in ctx)
-    nb = int(math.ceil(1.25 * need))
+    target = np.minimum(prompt + output, CTX_CAP)
+    if steady_state:
+        nb = batch * _blocks(CTX_CAP, DEFAULT_BLOCK)
+    else:
+        need = sum(_blocks(c + growth_steps, DEFAULT_BLOCK) for c in ctx)
+        nb = int(math.ceil(1.25 * need))
     return DecodeWorkload(
         name="mixed_b256", seed=seed, num_heads=OPT13B_HEADS, head_dim=OPT13B_HEAD_DIM,
         block_size=DEFAULT_BLOCK, num_layers=1, num_blocks=nb,
         free_order=_free_order(rng, nb), prompt_lens=[int(c) - 1 for c in ctx],
+        targets=[int(t) for t in target],
     )
+
+
+def draw_mixed_sequence(rng: np.random.Generator):
+    """A newly admitted sequence of the mixed batch: (prompt length, target length)."""
+    prompt = int(_lognormal_lengths(rng, 1, 200, 1536)[0])
+    output = int(_lognormal_lengths(rng, 1, 250, 1 << 30)[0])
+    return prompt, min(prompt + output, CTX_CAP)
 
 
 def full_40l(pool_bytes: int, seed: int = 110, beam: bool = False,

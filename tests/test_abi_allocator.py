@@ -1,0 +1,202 @@
+"""The C-ABI block manager (libpagedkv.so, host calls only -- no GPU needed)
+against the pages' worked examples and, operation by operation, against the
+oracle's block manager: slots, copy pairs, block tables, token counts,
+reference counts and the free queue must be identical (bit-exact indexing)."""
+import random
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_106_gb300 as pk
+from oracle.alloc import BlockManager, OutOfBlocks
+from tests.allocator_replay import load, replay
+from tests.conftest import ROOT
+
+GOLDEN = ["tutorial_fig1_4_block_table.json", "review_s4_3_decoding.json",
+          "tutorial_fig5_6_cow.json", "tutorial_full_shared_block.json"]
+
+
+def declared_functions():
+    src = open(f"{ROOT}/include/pagedkv.h").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\**\s*(pa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    names = declared_functions()
+    assert len(names) >= 16, names
+    out = subprocess.run(["nm", "-D", "--defined-only", pk.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    # and the binding binds each of them under the same name
+    for n in names:
+        assert callable(getattr(pk, n)), n
+
+
+class AbiAdapter:
+    def __init__(self, doc):
+        self.nb = doc["num_blocks"]
+        self.desc = pk.PoolDesc(doc["num_blocks"], doc["block_size"], free_order=doc["free_order"])
+        self.p = pk.pa_pool_create(self.desc)
+
+    def add(self, s, n):
+        return pk.pa_seq_add(self.p, s, n).tolist()
+
+    def fork(self, a, b):
+        pk.pa_seq_fork(self.p, a, b)
+
+    def free(self, s):
+        pk.pa_seq_free(self.p, s)
+
+    def alloc_slots(self, seqs):
+        slots, copies = pk.pa_alloc_slots(self.p, seqs)
+        return slots.tolist(), copies.tolist()
+
+    def table(self, s):
+        nt, nb = pk.pa_seq_info(self.p, s)
+        t, _ = pk.pa_get_block_tables(self.p, [s], max(nb, 1))
+        return t[0, :nb].tolist()
+
+    def filled(self, s):
+        nt, nb = pk.pa_seq_info(self.p, s)
+        B = self.desc.block_size
+        return [B] * (nb - 1) + [nt - (nb - 1) * B] if nb else []
+
+    def ref(self, b):
+        return int(pk.pa_pool_refcounts(self.p, self.nb)[b])
+
+    def free_queue(self):
+        return pk.pa_pool_free_queue(self.p, self.nb).tolist()
+
+
+@pytest.mark.parametrize("name", GOLDEN)
+def test_golden_examples_through_abi(golden_dir, name):
+    doc = load(golden_dir, name)
+    replay(doc, AbiAdapter(doc))
+
+
+def _compare(abi: AbiAdapter, m: BlockManager, live):
+    assert abi.free_queue() == list(m.free_queue)
+    assert pk.pa_pool_refcounts(abi.p, abi.nb).tolist() == m.ref
+    assert pk.pa_pool_num_free(abi.p) == len(m.free_queue)
+    if live:
+        ids = sorted(live)
+        mb = max(1, max(len(m.block_table(s)) for s in ids))
+        t, ctx = pk.pa_get_block_tables(abi.p, ids, mb)
+        assert t.tolist() == m.padded_tables(ids, mb)
+        assert ctx.tolist() == [m.num_tokens(s) for s in ids]
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_lockstep_with_oracle(seed):
+    rng = random.Random(1000 + seed)
+    B = rng.choice([1, 2, 3, 4, 16])
+    nb = rng.randint(0, 40)
+    order = list(range(nb))
+    rng.shuffle(order)
+    doc = {"num_blocks": nb, "block_size": B, "free_order": order}
+    abi = AbiAdapter(doc)
+    m = BlockManager(nb, B, order)
+    live, nxt = set(), 0
+    for _ in range(400):
+        r = rng.random()
+        if r < 0.2 or not live:
+            n = rng.randint(0, 4 * B)
+            try:
+                exp = m.add(nxt, n)
+            except OutOfBlocks:
+                with pytest.raises(pk.OutOfBlocks):
+                    abi.add(nxt, n)
+            else:
+                assert abi.add(nxt, n) == exp
+                live.add(nxt)
+            nxt += 1
+        elif r < 0.35:
+            p = rng.choice(sorted(live))
+            m.fork(p, nxt)
+            abi.fork(p, nxt)
+            live.add(nxt)
+            nxt += 1
+        elif r < 0.45:
+            s = rng.choice(sorted(live))
+            m.free(s)
+            abi.free(s)
+            live.discard(s)
+        else:
+            seqs = rng.sample(sorted(live), rng.randint(1, len(live)))
+            try:
+                exp = m.alloc_slots(seqs)
+            except OutOfBlocks:
+                with pytest.raises(pk.OutOfBlocks):
+                    abi.alloc_slots(seqs)
+            else:
+                got = abi.alloc_slots(seqs)
+                assert got[0] == exp[0]
+                assert [tuple(c) for c in got[1]] == exp[1]
+        _compare(abi, m, live)
+
+
+def test_abi_error_codes_and_no_partial_change():
+    d = pk.PoolDesc(3, 2, free_order=[0, 1, 2])
+    p = pk.pa_pool_create(d)
+    pk.pa_seq_add(p, 0, 2)
+    pk.pa_seq_add(p, 1, 2)
+    q0, r0 = pk.pa_pool_free_queue(p, 3).tolist(), pk.pa_pool_refcounts(p, 3).tolist()
+    with pytest.raises(pk.OutOfBlocks):
+        pk.pa_alloc_slots(p, [0, 1])
+    assert pk.pa_pool_free_queue(p, 3).tolist() == q0
+    assert pk.pa_pool_refcounts(p, 3).tolist() == r0
+    assert pk.pa_seq_info(p, 0) == (2, 1)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_alloc_slots(p, [0, 0])
+    assert e.value.code == pk.PA_ERR_INVALID_ARG
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_alloc_slots(p, [7])
+    assert e.value.code == pk.PA_ERR_NO_SEQ
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_seq_add(p, 0, 1)
+    assert e.value.code == pk.PA_ERR_NO_SEQ
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_seq_fork(p, 5, 6)
+    assert e.value.code == pk.PA_ERR_NO_SEQ
+    # copies_cap too small: copy-on-write needs one copy
+    pk.pa_seq_free(p, 1)
+    pk.pa_seq_add(p, 2, 1)
+    pk.pa_seq_fork(p, 2, 3)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_alloc_slots(p, [2], copies_cap=0)
+    assert e.value.code == pk.PA_ERR_INVALID_ARG
+    slots, copies = pk.pa_alloc_slots(p, [2], copies_cap=1)
+    assert copies.shape == (1, 2)
+    # table longer than max_blocks
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_get_block_tables(p, [0], 0)
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_pool_create(pk.PoolDesc(3, 2, free_order=[0, 0, 1]))
+    pk.pa_pool_destroy(p)
+
+
+def test_device_calls_reject_bad_geometry_before_any_cuda_work():
+    bad = pk.PoolDesc(4, 5, num_heads=2, head_dim=8)        # block size 5 unsupported
+    assert pk.pa_decode_workspace_bytes(2, 4, bad) == 0
+    for call in (
+        lambda: pk._lib.pa_write_kv(None, None, None, 1, None, None, bad.ref, None, None),
+        lambda: pk._lib.pa_decode_attention(None, None, None, None, None, None, 1, 4,
+                                            pk.ctypes.c_float(1.0), None, 0, None, bad.ref, None),
+        lambda: pk._lib.pa_copy_blocks(None, None, 1, None, 1, bad.ref, None, None),
+    ):
+        assert call() == pk.PA_ERR_INVALID_ARG
+        assert "block_size" in pk.pa_last_error_string()
+    d = pk.PoolDesc(4, 16, num_heads=40, head_dim=128)
+    # splitting at 512 tokens: 128 blocks -> 4 partitions, workspace (2 + D) floats per partition
+    ws = pk.pa_decode_workspace_bytes(3, 128, d)
+    rows = 3 * 40 * 4
+    assert ws >= rows * (128 + 2) * 4
+    assert pk.pa_decode_workspace_bytes(3, 32, d) == 0     # one partition: no workspace
+    # NULL pointers with a valid geometry are refused on the host
+    assert pk._lib.pa_write_kv(None, None, None, 1, None, None, d.ref, None, None) == \
+        pk.PA_ERR_INVALID_ARG

@@ -1,0 +1,185 @@
+"""End-to-end decode steps of the seeded workloads on the GPU, against the
+oracle run on the same seeded inputs.
+
+For every workload the block manager (C ABI) and the oracle's model must
+produce identical prompt slots, decode slots, copy-on-write pairs and block
+tables; the cache byte image after the prompt writes, the copies and the
+decode write must be identical; the attention outputs must be within 2e-3 of
+the fp64 oracle -- every output for the small workloads, every head of a
+sample of sequences (longest, shortest, around the 512-token partition
+boundary, random) for the full-size ones, which run in the launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_106_gb300 as pk
+from paged_kv_cache_106_gb300 import workloads as wl
+from paged_kv_cache_106_gb300.step import DecodeStepRunner
+from oracle import attention as oa
+from oracle import cache_ops as oc
+from oracle.alloc import BlockManager
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+class Both:
+    """The same workload driven through the library and through the oracle."""
+
+    def __init__(self, w: wl.DecodeWorkload, max_extra_steps: int = 1):
+        self.w = w
+        H, D, B, NB = w.num_heads, w.head_dim, w.block_size, w.num_blocks
+        self.m = BlockManager(NB, B, w.free_order)
+        self.desc = pk.PoolDesc(NB, B, num_layers=1, num_heads=H, head_dim=D,
+                                partition_tokens=w.split_tokens, free_order=w.free_order)
+        self.pool = pk.pa_pool_create(self.desc)
+        rng = wl.value_rng(w, 0)
+        ks, vs, slots = [], [], []
+        for i, n in enumerate(w.prompt_lens):
+            so = self.m.add(i, n)
+            sg = pk.pa_seq_add(self.pool, i, n)
+            assert sg.tolist() == so
+            slots.append(sg)
+            ks.append(wl.normal_f16(rng, (n, H, D)))
+            vs.append(wl.normal_f16(rng, (n, H, D)))
+        self.ids = list(range(len(w.prompt_lens)))
+        nxt = len(self.ids)
+        for root, extra in w.forks:
+            for _ in range(extra):
+                self.m.fork(root, nxt)
+                pk.pa_seq_fork(self.pool, root, nxt)
+                self.ids.append(nxt)
+                nxt += 1
+        K = np.concatenate(ks) if ks else np.zeros((0, H, D), np.float16)
+        V = np.concatenate(vs) if vs else np.zeros((0, H, D), np.float16)
+        S = np.concatenate(slots).astype(np.int64) if slots else np.zeros(0, np.int64)
+        # device cache, zero-filled, prompt written by the slot-write kernel
+        self.kc = torch.zeros((NB, H, B, D), dtype=torch.float16, device="cuda")
+        self.vc = torch.zeros_like(self.kc)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if len(S):
+            pk.pa_write_kv(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda(),
+                           torch.from_numpy(S).cuda(), self.kc, self.vc, self.desc,
+                           status=self.status)
+        # oracle cache image
+        self.okc = np.zeros((NB, H, B, D), np.float16)
+        self.ovc = np.zeros_like(self.okc)
+        oc.write_kv(self.okc, self.ovc, K, V, S)
+        del K, V
+        longest = max(m + max_extra_steps for m in w.prompt_lens)
+        self.max_blocks = -(-longest // B) + 1
+        self.runner = DecodeStepRunner(self.pool, self.desc, self.ids, self.max_blocks)
+        self.vrng = wl.value_rng(w, 1)
+
+    def check_cache(self):
+        torch.cuda.synchronize()
+        assert self.status.item() == 0
+        assert torch.equal(self.kc, torch.from_numpy(self.okc).cuda())
+        assert torch.equal(self.vc, torch.from_numpy(self.ovc).cuda())
+
+    def decode_step(self):
+        """One step on both sides; returns (gpu out [S,H,D] fp16 tensor, oracle inputs)."""
+        w = self.w
+        S, H, D = len(self.ids), w.num_heads, w.head_dim
+        q = wl.normal_f16(self.vrng, (S, H, D))
+        k = wl.normal_f16(self.vrng, (S, H, D))
+        v = wl.normal_f16(self.vrng, (S, H, D))
+        r = self.runner
+        r.prepare()
+        slots_o, copies_o = self.m.alloc_slots(self.ids)
+        _, _, tables_g, copies_g = r._views(r.host[(r.i - 1) & 1])
+        slots_g = r._views(r.host[(r.i - 1) & 1])[0]
+        assert slots_g.tolist() == slots_o
+        assert [tuple(c) for c in copies_g[: r.n_copies].tolist()] == copies_o
+        tables_o = np.array(self.m.padded_tables(self.ids, self.max_blocks), np.int32)
+        assert np.array_equal(tables_g, tables_o)
+        ctx_o = np.array([self.m.num_tokens(s) for s in self.ids], np.int32)
+        assert np.array_equal(r.ctx_host, ctx_o)
+        out = torch.empty((S, H, D), dtype=torch.float16, device="cuda")
+        r.copy_blocks([self.kc], [self.vc])
+        r.write_kv(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), self.kc, self.vc)
+        r.attention(out, torch.from_numpy(q).cuda(), self.kc, self.vc, w.scale)
+        oc.copy_blocks([self.okc], [self.ovc], copies_o)
+        oc.write_kv(self.okc, self.ovc, k, v, slots_o)
+        torch.cuda.synchronize()
+        assert r.status.item() == 0
+        return out, q, tables_o, ctx_o
+
+    def oracle_attention(self, q, tables, ctx, rows=None):
+        if rows is not None:
+            q, tables, ctx = q[rows], tables[rows], ctx[rows]
+        return oa.paged_attention(q, self.okc, self.ovc, tables, ctx, self.w.scale)
+
+
+def _err(gpu, ref):
+    return float(np.abs(gpu.astype(np.float64) - ref).max())
+
+
+def test_tiny_workload_everything_exact_and_attention_within_tolerance():
+    w = wl.tiny()
+    b = Both(w)
+    b.check_cache()
+    out, q, tables, ctx = b.decode_step()
+    assert ctx.tolist() == [9, 6]
+    b.check_cache()
+    ref = b.oracle_attention(q, tables, ctx)
+    assert _err(out.cpu().numpy(), ref) <= TOL
+
+
+def test_tiny_workload_with_the_tutorial_fixed_table():
+    """Same shapes, free order of the tutorial's Fig. 1-4: seq 0 ends on P5."""
+    w = wl.tiny()
+    w.free_order = np.array([3, 0, 1, 4, 5, 2], np.int32)
+    w.prompt_lens = [8, 5]
+    b = Both(w)
+    out, q, tables, ctx = b.decode_step()
+    assert tables[0].tolist()[:3] == [3, 0, 5]
+    ref = b.oracle_attention(q, tables, ctx)
+    assert _err(out.cpu().numpy(), ref) <= TOL
+
+
+def _sample_rows(ctx, rng, n_random=8):
+    order = np.argsort(ctx)
+    rows = {int(order[0]), int(order[-1])}
+    for edge in (512, 513, 1024, 1025):
+        near = int(np.argmin(np.abs(ctx - edge)))
+        rows.add(near)
+    rows.update(int(x) for x in rng.choice(len(ctx), size=min(n_random, len(ctx)), replace=False))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["opt13b_b64", "mixed_b256"])
+def test_full_size_workloads_sampled(name):
+    w = wl.CONFIGS[name]()
+    b = Both(w)
+    b.check_cache()
+    out, q, tables, ctx = b.decode_step()
+    b.check_cache()
+    rows = _sample_rows(ctx, np.random.default_rng(5))
+    ref = b.oracle_attention(q, tables, ctx, rows)
+    assert _err(out.cpu().numpy()[rows], ref) <= TOL
+    # a second step (contexts grow by one, some sequences take a new block)
+    out2, q2, tables2, ctx2 = b.decode_step()
+    assert np.array_equal(ctx2, ctx + 1)
+    rows2 = _sample_rows(ctx2, np.random.default_rng(6))
+    ref2 = b.oracle_attention(q2, tables2, ctx2, rows2)
+    assert _err(out2.cpu().numpy()[rows2], ref2) <= TOL
+
+
+def test_parallel_sampling_copy_on_write_64_steps():
+    w = wl.parallel_sampling()
+    b = Both(w, max_extra_steps=w.decode_steps)
+    b.check_cache()
+    total_copies = 0
+    for step in range(w.decode_steps):
+        out, q, tables, ctx = b.decode_step()
+        total_copies += b.runner.n_copies
+        if step in (0, 1, 15, 16, 17, w.decode_steps - 1):
+            b.check_cache()
+        ref = b.oracle_attention(q, tables, ctx)
+        assert _err(out.cpu().numpy(), ref) <= TOL, step
+    # every prompt whose last block is partial is copied for 3 of its 4 samples
+    partial = sum(1 for p in w.prompt_lens if p % w.block_size)
+    assert total_copies == 3 * partial
