@@ -138,21 +138,36 @@ def mixed_b256(seed: int = 109, batch: int = 256, growth_steps: int = 64,
                steady_state: bool = False) -> DecodeWorkload:
     """Mixed-length serving batch.
 
-    Each sequence sits at a uniformly drawn point 1..output of its
-    generation; its target (prompt + output, capped at 2048) is where it
-    finishes.  The pool leaves room for ``growth_steps`` more tokens per
-    sequence, or, with ``steady_state``, for every sequence at the cap (so a
-    continuous batch that replaces finished sequences never runs out).
+    Default (a snapshot): each sequence sits at a uniformly drawn point
+    1..output of its generation; its target (prompt + output, capped at
+    2048) is where it finishes; the pool leaves room for ``growth_steps``
+    more tokens per sequence.
+
+    ``steady_state``: the stationary state of a continuous batch that admits
+    (prompt, output) pairs from the same distributions -- a slot holds a
+    sequence with probability proportional to the steps it stays (target -
+    prompt), at a uniform point of its generation -- and a pool with room
+    for every sequence at the cap, so replacing finished sequences never
+    runs out of blocks.
     """
     rng = _rng(seed)
-    prompt = _lognormal_lengths(rng, batch, 200, 1536)
-    output = _lognormal_lengths(rng, batch, 250, 1 << 30)
-    done = np.array([rng.integers(1, o, endpoint=True) for o in output], dtype=np.int64)
-    ctx = np.minimum(prompt + done, CTX_CAP)
-    target = np.minimum(prompt + output, CTX_CAP)
     if steady_state:
+        cand = 64 * batch
+        prompt = _lognormal_lengths(rng, cand, 200, 1536)
+        target = np.minimum(prompt + _lognormal_lengths(rng, cand, 250, 1 << 30), CTX_CAP)
+        stay = (target - prompt).astype(np.float64)
+        pick = rng.choice(cand, size=batch, replace=True, p=stay / stay.sum())
+        prompt, target = prompt[pick], target[pick]
+        done = np.array([rng.integers(1, t - p, endpoint=True) for p, t in zip(prompt, target)],
+                        dtype=np.int64)
+        ctx = prompt + done
         nb = batch * _blocks(CTX_CAP, DEFAULT_BLOCK)
     else:
+        prompt = _lognormal_lengths(rng, batch, 200, 1536)
+        output = _lognormal_lengths(rng, batch, 250, 1 << 30)
+        done = np.array([rng.integers(1, o, endpoint=True) for o in output], dtype=np.int64)
+        ctx = np.minimum(prompt + done, CTX_CAP)
+        target = np.minimum(prompt + output, CTX_CAP)
         need = sum(_blocks(c + growth_steps, DEFAULT_BLOCK) for c in ctx)
         nb = int(math.ceil(1.25 * need))
     return DecodeWorkload(
