@@ -169,6 +169,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
 
     w = wl.mixed_b256(batch=args.batch, steady_state=True)
+    if args.partition:
+        w.split_tokens = args.partition
     H, D, B = w.num_heads, w.head_dim, w.block_size
     desc, pool = _pool_setup(pk, w)
     ids = np.arange(len(w.prompt_lens), dtype=np.int32)
@@ -425,6 +427,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)
+    ap.add_argument("--partition", type=int, default=0,
+                    help="split-context partition in tokens (default: the workload's 512)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -202,8 +202,9 @@ int pa_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_lay
                    int32_t *status, void *stream);
 
 /* Bytes of device workspace pa_decode_attention needs for a batch of n_seqs
- * sequences whose tables have max_blocks columns (0 when no context can be
- * longer than one partition). */
+ * sequences whose tables have max_blocks columns: 256 bytes of scheduling
+ * state, plus room for the partial results of split contexts when a context
+ * can be longer than one partition.  0 for an empty batch. */
 size_t pa_decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_pool_desc *desc);
 
 /* Single-query paged decode attention ([notes] §3.1 blockwise attention
@@ -213,7 +214,9 @@ size_t pa_decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_po
  * where k_p, v_p are read from physical block block_tables[s][p / B] at
  * offset p % B and ctx = ctx_lens[s] counts every stored token of the
  * sequence, the one written in this step included.  Slots past ctx are never
- * used.  ctx = 0 gives o = 0.  Contexts longer than partition_tokens are
+ * used.  ctx <= 0 gives o = 0; a ctx above max_blocks * B is reported as
+ * PA_ERR_BAD_BLOCK and its output left unwritten.  Contexts longer than
+ * partition_tokens are
  * split into partitions whose partial (max, sum, unnormalised output) go to
  * the workspace and are merged by a second kernel; results agree with the
  * unsplit sum to rounding.
@@ -223,7 +226,9 @@ size_t pa_decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_po
  *   ctx_lens      [n_seqs] int32, each <= max_blocks * B
  *   workspace     >= pa_decode_workspace_bytes(n_seqs, max_blocks, desc)
  *                 bytes, 256-byte aligned (may be NULL when that is 0); its
- *                 contents need no initialisation and are not preserved.
+ *                 contents need no initialisation and are not preserved (the
+ *                 call clears its scheduling word on the stream first).  Two
+ *                 calls must not use one workspace concurrently.
  * Errors: PA_ERR_INVALID_ARG, PA_ERR_CUDA. */
 int pa_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,

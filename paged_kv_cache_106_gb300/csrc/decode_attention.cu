@@ -10,35 +10,50 @@
 // llm-systems-engineering.pages.dev/posts/paged-kv-cache, Fig. 2, Fig. 4).
 // The review's §5.1 (2) describes the kernel the pages had: a fused block
 // read + attention adapted from FasterTransformer, one warp per block for
-// coalesced reads.  This design keeps "one warp owns whole blocks" but moves
-// the bytes with the Blackwell bulk-copy engine:
+// coalesced reads.  This design keeps "one warp owns whole blocks" and moves
+// the bytes with the Blackwell bulk-copy engine.
 //
-//  * grid = (partition, head, sequence); a partition is partition_tokens
-//    tokens of one sequence's context (contexts up to one partition need no
-//    merge);
-//  * each warp owns every WARPS-th block of its partition and runs its own
-//    ring of STAGES shared-memory stages; lane 0 issues two 1-D bulk copies
-//    per block (the (block, head) key rows and value rows are each one
-//    contiguous B*D*2-byte run in the cache layout) completing on that
-//    stage's mbarrier, so each warp keeps STAGES-1 blocks in flight with no
-//    CTA-wide synchronisation in the main loop;
-//  * q.k: lane (g, r) holds dims [8r, 8r+8) of token g of each pass (16-byte
-//    shared loads, conflict free); the NP partial dot products per lane are
-//    reduced across the row's lanes with a reduce-scatter butterfly, so one
-//    block costs NP-1+log2(TPR/NP) shuffles instead of NP*log2(TPR);
-//  * online softmax in base 2 (q is pre-scaled by scale*log2 e) with fp32
-//    running max / sum per warp; p.v accumulates in fp32 registers;
-//  * warps are combined through shared memory; a partition of a split
-//    context writes (max, sum, unnormalised output) to the workspace and the
-//    merge kernel combines partitions: m = max m_p, l = sum 2^(m_p-m) l_p,
-//    o = sum 2^(m_p-m) acc_p / l.  (The pages do not cover the split or the
-//    merge; this is the standard log-sum-exp combination of the same sum.)
+// Work unit = (sequence, head, partition); a partition is partition_tokens
+// tokens of one context (a context of at most one partition is one unit and
+// needs no merge).  Two kernels compute units:
+//
+//  * paged_decode_persistent (the main path): one CTA per SM slot, each a
+//    producer warp and C consumer warps.  CTAs take units from a global
+//    ticket counter.  The producer decodes the ticket (per-CTA prefix sums
+//    of partitions per sequence in shared memory), stages q, loads the
+//    unit's block-table entries (coalesced) and streams every block of the
+//    unit as two 1-D bulk copies (the (block, head) key rows and value rows
+//    are each one contiguous B*D*2-byte run in the cache layout) into a
+//    CTA-wide ring of STAGES shared-memory stages, across unit boundaries
+//    without draining.  Stage i goes to consumer i % C; full / empty
+//    mbarriers hand stages back and forth.  Each consumer keeps a running
+//    softmax state per unit; at its last block of a unit it leaves a partial
+//    (max, sum, output) in shared memory, and the last consumer to finish
+//    the unit combines them and writes the output (one partition) or the
+//    partition's partial to the workspace (split context).  CTA start-up
+//    cost is paid once per CTA instead of once per unit.
+//  * paged_decode_grid (fallback for batches too large for the per-CTA
+//    prefix sums): grid = (partition, head, sequence), every warp owns every
+//    WARPS-th block of its partition and runs its own bulk-copy ring.
+//
+// Per block (both kernels): lane (g, r) holds dims [8r, 8r+8) of token g of
+// each pass (16-byte shared loads, conflict free); q.k uses the f16 x f16 ->
+// f32 fused multiply-add (products exact, fp32 accumulation); the NP partial
+// dot products per lane are reduced across the row's lanes with a
+// reduce-scatter butterfly (NP-1+log2(TPR/NP) shuffles instead of
+// NP*log2(TPR)); online softmax in base 2 (scale * log2 e applied to the
+// reduced score) with fp32 running max / sum; p.v accumulates in fp32.
+// Partials of a split context are merged by paged_merge_kernel:
+// m = max m_p, l = sum 2^(m_p-m) l_p, o = sum 2^(m_p-m) acc_p / l.  (The
+// pages do not cover the split or the merge; this is the standard
+// log-sum-exp combination of the same sum.)
 //
 // Slots of the last block past ctx are neither copied (the bulk copy of a
 // partial block moves only its valid rows) nor used.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -51,6 +66,8 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxPersistentSeqs = 2048;   // per-CTA prefix sums live in shared memory
+constexpr size_t kCounterBytes = 256;      // workspace head: the unit ticket counter
 
 template <int D, int B>
 struct Geo {
@@ -64,26 +81,6 @@ struct Geo {
     static constexpr int STAGE = 2 * CHUNK;
 };
 
-#ifndef PA_ATTN_TARGET_STAGE_BYTES
-#define PA_ATTN_TARGET_STAGE_BYTES (96 * 1024)
-#endif
-
-template <int D, int B>
-struct DefaultCfg {
-    static constexpr int STAGE = Geo<D, B>::STAGE;
-    static constexpr int WARPS = (8 * STAGE > 200 * 1024) ? 2 : 4;
-    static constexpr int S0 = PA_ATTN_TARGET_STAGE_BYTES / (WARPS * STAGE);
-    static constexpr int STAGES = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);
-};
-
-template <int D, int B, int WARPS, int STAGES>
-struct Smem {
-    static constexpr int STAGE_BYTES = WARPS * STAGES * Geo<D, B>::STAGE;
-    static constexpr int BAR_OFF = STAGE_BYTES;
-    static constexpr int COMB_OFF = BAR_OFF + WARPS * STAGES * 8;
-    static constexpr int TOTAL = COMB_OFF + WARPS * (D + 2) * 4 + 128;   // +128: base alignment
-};
-
 struct DecodeParams {
     __half *out;
     const __half *q;
@@ -93,6 +90,7 @@ struct DecodeParams {
     const int32_t *ctx_lens;
     float *ws_ml;      // [S][H][max_parts][2]  (max, sum)
     float *ws_acc;     // [S][H][max_parts][D]  unnormalised output
+    int32_t *counter;  // unit tickets (persistent kernel), zeroed before each launch
     int32_t *status;
     int32_t n_seqs;
     int32_t num_heads;
@@ -102,6 +100,25 @@ struct DecodeParams {
     int32_t max_parts;
     float qscale;      // scale * log2(e)
 };
+
+// ---------------------------------------------------------------- block math
+
+// d += q . k over 8 halves (two 32-bit words hold four halves each), with
+// f16 x f16 -> f32 fused multiply-adds: every product is exact in fp32.
+__device__ __forceinline__ float dot8_f16(const uint4 &q, const uint4 &k, float d) {
+    const uint32_t qa[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t ka[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+            "mov.b32 {a0, a1}, %1;\n\t"
+            "mov.b32 {b0, b1}, %2;\n\t"
+            "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+            "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+            : "+f"(d)
+            : "r"(qa[i]), "r"(ka[i]));
+    return d;
+}
 
 // Sum NP partial values over the TPR lanes of a row group.  On return the
 // lane holds the full sum of value index idx(r) (see token_index_of).
@@ -134,12 +151,521 @@ __device__ __forceinline__ int token_index_of(int r) {
     return idx;
 }
 
-template <int D, int B, int WARPS, int STAGES>
-__global__ void __launch_bounds__(WARPS * 32)
-paged_decode_kernel(const DecodeParams p) {
+// Running softmax state of one warp over the blocks it has seen of a unit.
+template <int D, int B>
+struct WarpAttn {
     using G = Geo<D, B>;
-    using L = Smem<D, B, WARPS, STAGES>;
-    constexpr int TPR = G::TPR, TPP = G::TPP, NP = G::NP, DUP = G::DUP;
+    int r, g, my_tok;
+    uint4 qh;          // q halves, dims [8r, 8r+8)
+    float m, lsum, acc[8];
+
+    __device__ __forceinline__ void init_lane(int lane) {
+        r = lane % G::TPR;
+        g = lane / G::TPR;
+        my_tok = token_index_of<G::NP, G::TPR>(r) * G::TPP + g;
+    }
+    __device__ __forceinline__ void reset() {
+        m = -INFINITY;
+        lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+    }
+    // One block: keys at kst, values at vst (row t at t * D * 2 bytes), nv valid rows.
+    __device__ __forceinline__ void block(const uint8_t *kst, const uint8_t *vst, int nv,
+                                          float qscale) {
+        constexpr int TPR = G::TPR, TPP = G::TPP, NP = G::NP, DUP = G::DUP;
+        float part_dot[NP];
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+            const int t = ps * TPP + g;
+            float d = 0.f;
+            if (TPP * NP == B || t < B) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * (D * 2) + r * 16);
+                d = dot8_f16(qh, u, 0.f);
+            }
+            part_dot[ps] = d;
+        }
+        float sc = row_reduce_scatter<NP, TPR>(part_dot, r) * qscale;
+        if (my_tok >= nv) sc = -INFINITY;
+        float bm = sc;
+#pragma unroll
+        for (int off = DUP; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, off));
+        if (bm > m) {   // warp-uniform
+            const float a = exp2f(m - bm);
+            lsum *= a;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] *= a;
+            m = bm;
+        }
+        const float pr = exp2f(sc - m);
+        lsum += pr;
+#pragma unroll
+        for (int ps = 0; ps < NP; ++ps) {
+            const int t = ps * TPP + g;
+            const float pt = __shfl_sync(kFull, pr, g * TPR + ps * DUP);
+            if (t < nv) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(vst + t * (D * 2) + r * 16);
+                float vf[8];
+                half8_to_float8(u, vf);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[c] = fmaf(pt, vf[c], acc[c]);
+            }
+        }
+    }
+    // Totals over the warp: acc summed over token groups (lanes with g == 0
+    // hold dims [8r, 8r+8)), lsum over all lanes.
+    __device__ __forceinline__ void finalize() {
+#pragma unroll
+        for (int off = G::TPR; off < 32; off <<= 1)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] += __shfl_xor_sync(kFull, acc[c], off);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
+        lsum *= 1.0f / G::DUP;
+    }
+};
+
+// Write one unit's combined result: the fp16 output when the context is one
+// partition, else the partition's partial to the workspace.
+template <int D>
+__device__ __forceinline__ void store_unit(const DecodeParams &p, int s, int h, int part,
+                                           int n_parts, int d, float M, float L, float o) {
+    if (n_parts == 1) {
+        p.out[((size_t)s * p.num_heads + h) * D + d] = __float2half(o / L);
+    } else {
+        const size_t idx = ((size_t)s * p.num_heads + h) * p.max_parts + part;
+        if (d == 0) {
+            p.ws_ml[2 * idx] = M;
+            p.ws_ml[2 * idx + 1] = L;
+        }
+        p.ws_acc[idx * D + d] = o;
+    }
+}
+
+// ------------------------------------------------------- persistent kernel
+
+// A unit covers GH consecutive heads of one (sequence, partition): in the
+// cache layout the key rows of those heads in one physical block are one
+// contiguous GH * B * D * 2-byte run (same for values), so each block moves
+// as two long bulk copies -- scattered short runs cost the memory system far
+// more than their size.
+constexpr int align16(int x) { return (x + 15) & ~15; }
+
+template <int D, int B, int C, int SPC, int R, int GH>
+struct PLayout {
+    static constexpr int STAGES = C * SPC;
+    static constexpr int CHUNK = Geo<D, B>::CHUNK;
+    static constexpr int STAGE = 2 * GH * CHUNK;                     // K of GH heads, then V
+    static_assert(STAGE % 128 == 0 || STAGE % 16 == 0, "bulk-copy destinations need 16 B");
+    // every section starts on a 16-byte boundary (q rows are moved as uint4)
+    static constexpr int FULL_OFF = align16(STAGES * STAGE);
+    static constexpr int EMPTY_OFF = align16(FULL_OFF + STAGES * 8);
+    static constexpr int DESC_OFF = align16(EMPTY_OFF + STAGES * 8);    // int2 per stage
+    static constexpr int UNIT_OFF = align16(DESC_OFF + STAGES * 8);     // 16 int per unit slot
+    static constexpr int Q_OFF = align16(UNIT_OFF + R * 64);            // GH * D halves per slot
+    static constexpr int COMB_OFF = align16(Q_OFF + R * GH * D * 2);
+    static constexpr int SEQ_OFF = align16(COMB_OFF + R * C * GH * (D + 2) * 4);  // prefix[S+1]
+    static_assert(Q_OFF % 16 == 0 && FULL_OFF % 8 == 0 && DESC_OFF % 8 == 0, "alignment");
+    static constexpr int fixed_bytes() { return SEQ_OFF + 128; }     // +128: base alignment
+    static size_t bytes(int n_seqs) { return fixed_bytes() + (size_t)(2 * n_seqs + 2) * 4; }
+};
+
+// unit slot fields (int32)
+// U_DONE + g counts the groups that left their partial of head g; U_HDONE
+// counts the heads combined.
+enum { U_S = 0, U_H0, U_NH, U_PART, U_NPARTS, U_FIRSTC, U_NPARTIC, U_STATE, U_HDONE, U_DONE };
+// stage descriptor flags
+enum { F_FIRST = 1, F_LAST = 2, F_END = 4 };
+
+template <int D, int B, int C, int SPC, int R, int GH, int PF>
+__global__ void __launch_bounds__((C * GH + 1) * 32)
+paged_decode_persistent(const DecodeParams p) {
+    using G = Geo<D, B>;
+    using L = PLayout<D, B, C, SPC, R, GH>;
+    constexpr int STAGES = L::STAGES, STAGE = L::STAGE, CHUNK = G::CHUNK;
+    constexpr int QVEC = GH * D / 8;                  // 16-byte pieces of a unit's q rows
+    constexpr int QPL = (QVEC + 31) / 32;             // ... per producer lane
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::FULL_OFF);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L::EMPTY_OFF);
+    int2 *sdesc = reinterpret_cast<int2 *>(smem + L::DESC_OFF);
+    int32_t *units = reinterpret_cast<int32_t *>(smem + L::UNIT_OFF);
+    __half *qs = reinterpret_cast<__half *>(smem + L::Q_OFF);
+    float *comb = reinterpret_cast<float *>(smem + L::COMB_OFF);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + L::SEQ_OFF);   // partitions before s
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int S = p.n_seqs;
+    const int H = p.num_heads;
+    const int HG = (H + GH - 1) / GH;             // head groups
+
+    // ---- set-up: partitions per sequence (prefix sums), barriers
+    if (tid == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(smem_addr(&full[st]), 1);
+            mbar_init(smem_addr(&empty[st]), GH);   // every warp of the stage's group
+        }
+        fence_barrier_init();
+    }
+    for (int i = tid; i < R * 16; i += blockDim.x) units[i] = 0;
+    __syncthreads();
+    // A context of 0 is one unit (its output is zero); a context the table
+    // row cannot hold is reported and gets no unit.
+    auto parts_of = [&](int c) {
+        if (c > p.max_blocks * B) return 0;
+        return c <= 0 ? 1 : ((c + B - 1) / B + p.part_blocks - 1) / p.part_blocks;
+    };
+    for (int s = tid; s < S; s += blockDim.x) {
+        const int c = p.ctx_lens[s];
+        if (c > p.max_blocks * B && blockIdx.x == 0) report(p.status, PA_ERR_BAD_BLOCK);
+        prefix[s] = parts_of(c);   // counts first, turned into exclusive sums below
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive prefix sum of partitions per sequence
+        const int per = (S + 31) / 32;
+        const int lo = min(S, lane * per), hi = min(S, lo + per);
+        int sum = 0;
+        for (int s = lo; s < hi; ++s) sum += prefix[s];
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(kFull, incl, off);
+            if (lane >= off) incl += y;
+        }
+        int run = incl - sum;
+        for (int s = lo; s < hi; ++s) {
+            const int n = prefix[s];
+            prefix[s] = run;
+            run += n;
+        }
+        if (lane == 31) prefix[S] = incl;
+    }
+    __syncthreads();
+    const int n_units = prefix[S] * HG;
+
+    if (warp == C * GH) {
+        // ================================================ producer warp
+        // Software-pipelined: while unit k's blocks are issued, the ticket of
+        // unit k+2 and the q rows and first table entries of unit k+1 are in
+        // flight, so no global-memory latency sits between two units.
+        const uint64_t policy = l2_evict_first_policy();
+        const size_t blk_stride = (size_t)H * B * D;
+        int i_stage = 0;
+        int k_unit = 0;
+        bool ok = true;
+
+        struct Pending {
+            int ticket, s, h0, nh, part, ctx, n_parts, j0, nb, tbl;
+            uint4 q[QPL];
+        };
+        // Decode a ticket (shared memory only) and start the loads of its
+        // context length, q rows and first 32 table entries (lane t: entry
+        // j0 + t, padding included).  None of these loads is waited on until
+        // the unit becomes current, one unit later.
+        auto prepare = [&](int ticket) {
+            Pending u;
+            u.ticket = ticket;
+            u.s = u.h0 = u.nh = u.part = u.ctx = u.n_parts = u.j0 = u.nb = 0;
+            u.tbl = -1;
+#pragma unroll
+            for (int k = 0; k < QPL; ++k) u.q[k] = make_uint4(0, 0, 0, 0);
+            if (ticket >= n_units) return u;
+            const int gp = ticket / HG;
+            const int hg = ticket - gp * HG;
+            u.h0 = hg * GH;
+            u.nh = min(GH, H - u.h0);
+            int lo = 0, hi = S - 1;   // last sequence s with prefix[s] <= gp
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (prefix[mid] <= gp) lo = mid; else hi = mid - 1;
+            }
+            u.s = lo;
+            u.part = gp - prefix[lo];
+            u.n_parts = prefix[lo + 1] - prefix[lo];
+            u.j0 = u.part * p.part_blocks;
+            u.ctx = p.ctx_lens[lo];
+            if (u.j0 + lane < p.max_blocks)
+                u.tbl = p.block_tables[(size_t)lo * p.max_blocks + u.j0 + lane];
+            const uint4 *qsrc = reinterpret_cast<const uint4 *>(p.q + ((size_t)lo * H + u.h0) * D);
+#pragma unroll
+            for (int k = 0; k < QPL; ++k)
+                if (lane + 32 * k < u.nh * (D / 8)) u.q[k] = qsrc[lane + 32 * k];
+            return u;
+        };
+        // blocks of the unit in its partition (needs the context length)
+        auto blocks_of = [&](const Pending &u) {
+            if (u.ticket >= n_units || u.ctx <= 0) return 0;
+            return min(p.part_blocks, (u.ctx + B - 1) / B - u.j0);
+        };
+
+        // L2 prefetch runs PF blocks ahead of the shared-memory copies along
+        // the stream of blocks (into the next unit when the current one ends),
+        // so the number of bytes DRAM is working on is not bounded by the
+        // stages that fit in shared memory.  pf_cur / pf_nxt: blocks of the
+        // current / next unit already prefetched.
+        auto prefetch = [&](const Pending &u, int b, int phys) {
+            if (phys >= 0 && phys < p.num_blocks) {
+                const size_t off = (size_t)phys * blk_stride + (size_t)u.h0 * B * D;
+                prefetch_l2(p.k_cache + off, (uint32_t)u.nh * CHUNK);
+                prefetch_l2(p.v_cache + off, (uint32_t)u.nh * CHUNK);
+            }
+        };
+        int pf_cur = 0, pf_nxt = 0;
+
+        int t_next = 0;
+        if (lane == 0) t_next = atomicAdd(p.counter, 1);
+        Pending cur = prepare(__shfl_sync(kFull, t_next, 0));
+        if (lane == 0) t_next = atomicAdd(p.counter, 1);
+        while (ok && cur.ticket < n_units) {
+            cur.nb = blocks_of(cur);
+            const int tn = __shfl_sync(kFull, t_next, 0);
+            if (lane == 0) t_next = atomicAdd(p.counter, 1);
+            Pending nxt = prepare(tn);
+            if (PF > 0 && cur.ctx > 0) {
+                // the first PF blocks of this unit, one lane per block
+                const int upto = min(min(PF, cur.nb), 32);
+                if (lane >= pf_cur && lane < upto) prefetch(cur, lane, cur.tbl);
+                pf_cur = max(pf_cur, upto);
+            }
+            if (cur.ctx <= 0) {   // empty context (a negative length counts as 0): o = 0
+                __half *o = p.out + ((size_t)cur.s * H + cur.h0) * D;
+                for (int d = lane; d < cur.nh * D; d += 32) o[d] = __float2half(0.f);
+            } else {
+                const int slot = k_unit % R;
+                int32_t *u = units + slot * 16;
+                // wait until the slot's previous unit has been combined
+                if (lane == 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (*(volatile int32_t *)&u[U_STATE] != 0) {
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            report(p.status, PA_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                __threadfence_block();
+                // stage q and the unit's description
+#pragma unroll
+                for (int k = 0; k < QPL; ++k)
+                    if (lane + 32 * k < QVEC)
+                        reinterpret_cast<uint4 *>(qs + slot * GH * D)[lane + 32 * k] = cur.q[k];
+                if (lane == 0) {
+                    u[U_S] = cur.s;
+                    u[U_H0] = cur.h0;
+                    u[U_NH] = cur.nh;
+                    u[U_PART] = cur.part;
+                    u[U_NPARTS] = cur.n_parts;
+                    u[U_FIRSTC] = i_stage % C;
+                    u[U_NPARTIC] = min(C, cur.nb);
+                    u[U_HDONE] = 0;
+#pragma unroll
+                    for (int g = 0; g < GH; ++g) u[U_DONE + g] = 0;
+                    u[U_STATE] = 1;
+                }
+                __syncwarp();
+                __threadfence_block();
+                const int32_t *trow = p.block_tables + (size_t)cur.s * p.max_blocks + cur.j0;
+                const __half *kbase = p.k_cache + (size_t)cur.h0 * B * D;
+                const __half *vbase = p.v_cache + (size_t)cur.h0 * B * D;
+                int tbl = cur.tbl;
+                for (int b = 0; b < cur.nb; ++b) {
+                    if (b > 0 && (b & 31) == 0) tbl = b + lane < cur.nb ? trow[b + lane] : -1;
+                    const int phys = __shfl_sync(kFull, tbl, b & 31);
+                    if (PF > 0) {
+                        const int tgt = b + PF;
+                        const int pc = __shfl_sync(kFull, cur.tbl, tgt & 31);
+                        const int tn2 = tgt - cur.nb;
+                        const int pn = __shfl_sync(kFull, nxt.tbl, (tn2 < 0 ? 0 : tn2) & 31);
+                        const int nxt_nb = tn2 >= 0 ? blocks_of(nxt) : 0;
+                        if (lane == 0) {
+                            if (tgt < cur.nb) {
+                                if (tgt >= pf_cur && tgt < 32) prefetch(cur, tgt, pc);
+                            } else if (tn2 < nxt_nb && tn2 >= pf_nxt && tn2 < 32) {
+                                prefetch(nxt, tn2, pn);
+                            }
+                        }
+                        if (tgt < cur.nb) pf_cur = max(pf_cur, tgt + 1);
+                        else if (tn2 < nxt_nb) pf_nxt = max(pf_nxt, tn2 + 1);
+                    }
+                    const int st = i_stage % STAGES;
+                    const int use = i_stage / STAGES;
+                    if (lane == 0) {
+                        if (use > 0 && !mbar_wait_bounded(smem_addr(&empty[st]),
+                                                          (uint32_t)(use - 1) & 1u, p.status, true)) {
+                            report(p.status, PA_ERR_TIMEOUT);
+                            ok = false;
+                        } else {
+                            const int nv = min(B, cur.ctx - (cur.j0 + b) * B);
+                            const int flags =
+                                (b < C ? F_FIRST : 0) | (b >= cur.nb - C ? F_LAST : 0);
+                            sdesc[st] = make_int2(slot | (flags << 16), nv);
+                            const uint32_t fb = smem_addr(&full[st]);
+                            const uint32_t dk = smem_addr(smem + st * STAGE);
+                            const uint32_t dv = dk + GH * CHUNK;
+                            if (phys >= 0 && phys < p.num_blocks) {
+                                const __half *sk = kbase + (size_t)phys * blk_stride;
+                                const __half *sv = vbase + (size_t)phys * blk_stride;
+                                if (nv == B) {   // the heads' full rows: one run each
+                                    const uint32_t bytes = (uint32_t)cur.nh * CHUNK;
+                                    mbar_arrive_expect_tx(fb, 2 * bytes);
+                                    bulk_g2s(dk, sk, bytes, fb, policy);
+                                    bulk_g2s(dv, sv, bytes, fb, policy);
+                                } else {         // partial last block: valid rows per head
+                                    const uint32_t bytes = (uint32_t)nv * D * 2;
+                                    mbar_arrive_expect_tx(fb, 2 * bytes * cur.nh);
+                                    for (int g = 0; g < cur.nh; ++g) {
+                                        bulk_g2s(dk + g * CHUNK, sk + (size_t)g * B * D, bytes, fb,
+                                                 policy);
+                                        bulk_g2s(dv + g * CHUNK, sv + (size_t)g * B * D, bytes, fb,
+                                                 policy);
+                                    }
+                                }
+                            } else {
+                                report(p.status, PA_ERR_BAD_BLOCK);
+                                mbar_arrive(fb);
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    ++i_stage;
+                }
+                ++k_unit;
+            }
+            cur = nxt;
+            pf_cur = pf_nxt;
+            pf_nxt = 0;
+        }
+        // end of stream: one END stage per consumer
+        for (int c = 0; ok && c < C; ++c) {
+            const int st = i_stage % STAGES;
+            const int use = i_stage / STAGES;
+            if (lane == 0) {
+                if (use > 0 && !mbar_wait_bounded(smem_addr(&empty[st]), (uint32_t)(use - 1) & 1u,
+                                                  p.status, true)) {
+                    report(p.status, PA_ERR_TIMEOUT);
+                    ok = false;
+                } else {
+                    sdesc[st] = make_int2(F_END << 16, 0);
+                    mbar_arrive(smem_addr(&full[st]));
+                }
+            }
+            ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            ++i_stage;
+        }
+        if (!ok && lane == 0) {
+            // let every issued copy land before the CTA can exit
+            for (int k = max(0, i_stage - STAGES); k < i_stage; ++k)
+                mbar_wait_bounded(smem_addr(&full[k % STAGES]), (uint32_t)(k / STAGES) & 1u,
+                                  p.status, false);
+        }
+        return;
+    }
+
+    // ==================================================== consumer warps
+    // Warp (c, g): group c takes every C-th stage, member g its head g.
+    const int c = warp / GH;
+    const int g = warp - c * GH;
+    WarpAttn<D, B> wa;
+    wa.init_lane(lane);
+    wa.reset();
+    int nh = 0;
+    for (int i = c;; i += C) {
+        const int st = i % STAGES;
+        if (!mbar_wait_bounded(smem_addr(&full[st]), (uint32_t)(i / STAGES) & 1u, p.status, true)) {
+            report(p.status, PA_ERR_TIMEOUT);
+            return;
+        }
+        const int2 dsc = sdesc[st];
+        const int flags = dsc.x >> 16;
+        if (flags & F_END) return;
+        const int slot = dsc.x & 0xffff;
+        int32_t *u = units + slot * 16;
+        if (flags & F_FIRST) {
+            nh = u[U_NH];
+            wa.reset();
+            if (g < nh) wa.qh = reinterpret_cast<const uint4 *>(qs + (slot * GH + g) * D)[wa.r];
+        }
+        const uint8_t *kst = smem + st * STAGE;
+        if (g < nh) wa.block(kst + g * CHUNK, kst + (GH + g) * CHUNK, dsc.y, p.qscale);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
+        if ((flags & F_LAST) && g < nh) {
+            wa.finalize();
+            float *cw = comb + ((slot * C + c) * GH + g) * (D + 2);
+            if (wa.g == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) cw[wa.r * 8 + k] = wa.acc[k];
+            }
+            if (lane == 0) {
+                cw[D] = wa.m;
+                cw[D + 1] = wa.lsum;
+            }
+            __threadfence_block();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) last = atomicAdd(&u[U_DONE + g], 1) == u[U_NPARTIC] - 1;
+            last = __shfl_sync(kFull, last, 0);
+            if (last) {   // every group has left its partial of head g: combine
+                __threadfence_block();
+                const int first_c = u[U_FIRSTC], np = u[U_NPARTIC];
+                float M = -INFINITY;
+                for (int t = 0; t < np; ++t)
+                    M = fmaxf(M, comb[(((slot * C + (first_c + t) % C) * GH) + g) * (D + 2) + D]);
+                float Lt = 0.f;
+                for (int t = 0; t < np; ++t) {
+                    const float *pw = comb + (((slot * C + (first_c + t) % C) * GH) + g) * (D + 2);
+                    Lt = fmaf(exp2f(pw[D] - M), pw[D + 1], Lt);
+                }
+                const int s = u[U_S], h = u[U_H0] + g, part = u[U_PART], n_parts = u[U_NPARTS];
+                for (int d = lane; d < D; d += 32) {
+                    float o = 0.f;
+                    for (int t = 0; t < np; ++t) {
+                        const float *pw =
+                            comb + (((slot * C + (first_c + t) % C) * GH) + g) * (D + 2);
+                        o = fmaf(exp2f(pw[D] - M), pw[d], o);
+                    }
+                    store_unit<D>(p, s, h, part, n_parts, d, M, Lt, o);
+                }
+                __syncwarp();
+                __threadfence_block();
+                int free_it = 0;
+                if (lane == 0) free_it = atomicAdd(&u[U_HDONE], 1) == nh - 1;
+                free_it = __shfl_sync(kFull, free_it, 0);
+                if (free_it && lane == 0) atomicExch(&u[U_STATE], 0);
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------- grid kernel
+
+template <int D, int B>
+struct GridCfg {
+    static constexpr int STAGE = Geo<D, B>::STAGE;
+    static constexpr int WARPS = (8 * STAGE > 200 * 1024) ? 2 : 4;
+    static constexpr int S0 = (96 * 1024) / (WARPS * STAGE);
+    static constexpr int STAGES = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);
+    static constexpr int STAGE_BYTES = WARPS * STAGES * STAGE;
+    static constexpr int BAR_OFF = STAGE_BYTES;
+    static constexpr int COMB_OFF = BAR_OFF + WARPS * STAGES * 8;
+    static constexpr int TOTAL = COMB_OFF + WARPS * (D + 2) * 4 + 128;
+};
+
+template <int D, int B>
+__global__ void __launch_bounds__(GridCfg<D, B>::WARPS * 32)
+paged_decode_grid(const DecodeParams p) {
+    using G = Geo<D, B>;
+    using L = GridCfg<D, B>;
+    constexpr int WARPS = L::WARPS, STAGES = L::STAGES;
     constexpr int CHUNK = G::CHUNK, STAGE = G::STAGE;
 
     const int part = blockIdx.x;
@@ -151,13 +677,13 @@ paged_decode_kernel(const DecodeParams p) {
     const int H = p.num_heads;
 
     const int ctx = p.ctx_lens[s];
-    __half *out_row = p.out + ((size_t)s * H + h) * D;
-    if (ctx <= 0) {
+    if (ctx <= 0) {   // empty context (a negative length counts as 0): o = 0
         if (part == 0)
-            for (int i = tid; i < D; i += WARPS * 32) out_row[i] = __float2half(0.f);
+            for (int i = tid; i < D; i += WARPS * 32)
+                p.out[((size_t)s * H + h) * D + i] = __float2half(0.f);
         return;
     }
-    if (ctx > p.max_blocks * B) {   // the table row cannot hold this context
+    if (ctx > p.max_blocks * B) {
         if (part == 0 && tid == 0) report(p.status, PA_ERR_BAD_BLOCK);
         return;
     }
@@ -175,18 +701,10 @@ paged_decode_kernel(const DecodeParams p) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::BAR_OFF) + warp * STAGES;
     float *comb = reinterpret_cast<float *>(smem + L::COMB_OFF);
 
-    const int r = lane % TPR;
-    const int g = lane / TPR;
-
-    // q, dims [8r, 8r+8), pre-scaled into log2 units.
-    float qf[8];
-    {
-        const uint4 u =
-            *reinterpret_cast<const uint4 *>(p.q + ((size_t)s * H + h) * D + r * 8);
-        half8_to_float8(u, qf);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qf[i] *= p.qscale;
-    }
+    WarpAttn<D, B> wa;
+    wa.init_lane(lane);
+    wa.reset();
+    wa.qh = *reinterpret_cast<const uint4 *>(p.q + ((size_t)s * H + h) * D + wa.r * 8);
 
     const size_t blk_stride = (size_t)H * B * D;
     const __half *kbase = p.k_cache + (size_t)h * B * D;
@@ -233,15 +751,6 @@ paged_decode_kernel(const DecodeParams p) {
     const int pro = min(STAGES, n_w);
     for (int i = 0; i < pro; ++i) issue(i);
 
-    const int my_idx = token_index_of<NP, TPR>(r);
-    const int my_tok = my_idx * TPP + g;
-
-    float m = -INFINITY;
-    float lsum = 0.f;
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-
     for (int i = 0; i < n_w; ++i) {
         const int st = i % STAGES;
         const uint32_t parity = (uint32_t)(i / STAGES) & 1u;
@@ -255,74 +764,21 @@ paged_decode_kernel(const DecodeParams p) {
             break;
         }
         const int j = j0 + warp + WARPS * i;
-        const int nv = min(B, ctx - j * B);
         const uint8_t *kst = stages + st * STAGE;
-        const uint8_t *vst = kst + CHUNK;
-
-        // scores: partial q.k over this lane's 8 dims, one per pass
-        float part_dot[NP];
-#pragma unroll
-        for (int ps = 0; ps < NP; ++ps) {
-            const int t = ps * TPP + g;
-            float d = 0.f;
-            if (TPP * NP == B || t < B) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(kst + t * (D * 2) + r * 16);
-                float kf[8];
-                half8_to_float8(u, kf);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) d = fmaf(qf[c], kf[c], d);
-            }
-            part_dot[ps] = d;
-        }
-        float sc = row_reduce_scatter<NP, TPR>(part_dot, r);
-        if (my_tok >= nv) sc = -INFINITY;
-
-        float bm = sc;
-#pragma unroll
-        for (int off = DUP; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, off));
-        if (bm > m) {   // warp-uniform
-            const float a = exp2f(m - bm);
-            lsum *= a;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) acc[c] *= a;
-            m = bm;
-        }
-        const float pr = exp2f(sc - m);
-        lsum += pr;
-
-#pragma unroll
-        for (int ps = 0; ps < NP; ++ps) {
-            const int t = ps * TPP + g;
-            const float pt = __shfl_sync(kFull, pr, g * TPR + ps * DUP);
-            if (t < nv) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(vst + t * (D * 2) + r * 16);
-                float vf[8];
-                half8_to_float8(u, vf);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) acc[c] = fmaf(pt, vf[c], acc[c]);
-            }
-        }
+        wa.block(kst, kst + CHUNK, min(B, ctx - j * B), p.qscale);
         __syncwarp();
         if (i + STAGES < n_w) issue(i + STAGES);
     }
-
-    // warp totals: output over token groups, sum over all lanes
-#pragma unroll
-    for (int off = TPR; off < 32; off <<= 1)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) acc[c] += __shfl_xor_sync(kFull, acc[c], off);
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) lsum += __shfl_xor_sync(kFull, lsum, off);
-    lsum *= 1.0f / DUP;
+    wa.finalize();
 
     float *cw = comb + warp * (D + 2);
-    if (g == 0) {
+    if (wa.g == 0) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) cw[r * 8 + c] = acc[c];
+        for (int c = 0; c < 8; ++c) cw[wa.r * 8 + c] = wa.acc[c];
     }
     if (lane == 0) {
-        cw[D] = m;
-        cw[D + 1] = lsum;
+        cw[D] = wa.m;
+        cw[D + 1] = wa.lsum;
     }
     __syncthreads();
 
@@ -336,27 +792,11 @@ paged_decode_kernel(const DecodeParams p) {
         wgt[w] = exp2f(comb[w * (D + 2) + D] - M);
         Lt = fmaf(wgt[w], comb[w * (D + 2) + D + 1], Lt);
     }
-    if (n_parts == 1) {
-        const float inv = 1.0f / Lt;
-        for (int i = tid; i < D; i += WARPS * 32) {
-            float o = 0.f;
+    for (int i = tid; i < D; i += WARPS * 32) {
+        float o = 0.f;
 #pragma unroll
-            for (int w = 0; w < WARPS; ++w) o = fmaf(wgt[w], comb[w * (D + 2) + i], o);
-            out_row[i] = __float2half(o * inv);
-        }
-    } else {
-        const size_t idx = ((size_t)s * H + h) * p.max_parts + part;
-        if (tid == 0) {
-            p.ws_ml[2 * idx] = M;
-            p.ws_ml[2 * idx + 1] = Lt;
-        }
-        float *wacc = p.ws_acc + idx * D;
-        for (int i = tid; i < D; i += WARPS * 32) {
-            float o = 0.f;
-#pragma unroll
-            for (int w = 0; w < WARPS; ++w) o = fmaf(wgt[w], comb[w * (D + 2) + i], o);
-            wacc[i] = o;
-        }
+        for (int w = 0; w < WARPS; ++w) o = fmaf(wgt[w], comb[w * (D + 2) + i], o);
+        store_unit<D>(p, s, h, part, n_parts, i, M, Lt, o);
     }
 }
 
@@ -392,26 +832,134 @@ __global__ void __launch_bounds__(128) paged_merge_kernel(const DecodeParams p, 
     }
 }
 
-template <int D, int B, int WARPS, int STAGES>
-int launch_cfg(const DecodeParams &prm, int part_tokens, cudaStream_t stream) {
-    using L = Smem<D, B, WARPS, STAGES>;
-    auto kern = paged_decode_kernel<D, B, WARPS, STAGES>;
-    // Raising the dynamic shared-memory limit is per device; do it once each.
+// ------------------------------------------------------------- launching
+
+// Raise a kernel's dynamic shared-memory limit once per device.  Tag makes
+// the once-flags distinct per kernel instantiation (they share one type).
+template <typename Tag, typename K>
+cudaError_t set_smem_once(K kern, int bytes) {
     static std::once_flag once[64];
-    static cudaError_t attr_err[64];
+    static cudaError_t err[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [&] {
+        err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    });
+    return err[dev];
+}
+
+int sm_count() {
+    static std::once_flag once[64];
+    static int n[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::call_once(once[dev], [&] {
+        n[dev] = 148;
+        cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev);
+    });
+    return n[dev];
+}
+
+template <int D, int B>
+struct PersistCfg {
+    static constexpr int CHUNK = Geo<D, B>::CHUNK;
+#ifdef PA_TUNE_GH
+    static constexpr int GH = PA_TUNE_GH;
+#else
+    // heads per unit: at least 8 KB of contiguous key (and value) rows per copy
+    static constexpr int GH0 = 8192 / CHUNK;
+    static constexpr int GH = GH0 < 1 ? 1 : (GH0 > 4 ? 4 : GH0);
+#endif
+    static constexpr int STAGE = 2 * GH * CHUNK;
+#ifdef PA_TUNE_C
+    static constexpr int C = PA_TUNE_C;
+#else
+    static constexpr int C = STAGE <= 8192 ? 4 : (STAGE <= 16384 ? 3 : 2);   // consumer warps
+#endif
+#ifdef PA_TUNE_SPC
+    static constexpr int SPC = PA_TUNE_SPC;
+#else
+    static constexpr int SPC0 = (96 * 1024) / (C * STAGE);
+    static constexpr int SPC = SPC0 < 2 ? 2 : (SPC0 > 8 ? 8 : SPC0);
+#endif
+#ifdef PA_TUNE_R
+    static constexpr int R = PA_TUNE_R;
+#else
+    static constexpr int R = 3;       // unit slots (open units per CTA)
+#endif
+#ifdef PA_TUNE_PF
+    static constexpr int PF = PA_TUNE_PF;
+#else
+    static constexpr int PF = 0;      // L2 prefetch distance, blocks (0: none)
+#endif
+};
+
+template <int D, int B, bool Persistent>
+struct KernelTag {};
+
+template <int D, int B>
+int launch_db(const DecodeParams &prm_in, int part_tokens, cudaStream_t stream) {
+    DecodeParams prm = prm_in;
+    cudaError_t e;
+    using PC = PersistCfg<D, B>;
+    using L = PLayout<D, B, PC::C, PC::SPC, PC::R, PC::GH>;
+    auto pkern = paged_decode_persistent<D, B, PC::C, PC::SPC, PC::R, PC::GH, PC::PF>;
+    constexpr int threads = (PC::C * PC::GH + 1) * 32;
+    // The persistent kernel's shared memory grows with the batch (its prefix
+    // sums); it is used while that keeps the occupancy of a one-sequence
+    // batch, else the grid kernel runs.  Found once per device.
+    static std::once_flag once[64];
+    static int max_seqs[64], per_sm_full[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return fail(PA_ERR_CUDA, "pa_decode_attention: cudaGetDevice failed");
     std::call_once(once[dev], [&] {
-        attr_err[dev] =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+        max_seqs[dev] = 0;
+        per_sm_full[dev] = 0;
+        if (set_smem_once<KernelTag<D, B, true>>(pkern, (int)L::bytes(kMaxPersistentSeqs)) !=
+            cudaSuccess)
+            return;
+        int base = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&base, pkern, threads,
+                                                          (int)L::bytes(1)) != cudaSuccess ||
+            base < 1)
+            return;
+        int lo = 1, hi = kMaxPersistentSeqs;   // largest batch with the same occupancy
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            int n = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pkern, threads, (int)L::bytes(mid));
+            if (n >= base) lo = mid; else hi = mid - 1;
+        }
+        max_seqs[dev] = lo;
+        per_sm_full[dev] = base;
     });
-    if (attr_err[dev] != cudaSuccess)
-        return fail(PA_ERR_CUDA, "pa_decode_attention: cudaFuncSetAttribute: %s",
-                    cudaGetErrorString(attr_err[dev]));
-    dim3 grid(prm.max_parts, prm.num_heads, prm.n_seqs);
-    kern<<<grid, WARPS * 32, L::TOTAL, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
+#ifdef PA_TUNE_FORCE_GRID
+    if (false) {
+#else
+    if (prm.n_seqs <= max_seqs[dev]) {
+#endif
+        auto kern = pkern;
+        const int use_smem = (int)L::bytes(prm.n_seqs);
+        const int per_sm = per_sm_full[dev];
+        const int64_t max_units =
+            (int64_t)prm.n_seqs * ((prm.num_heads + PC::GH - 1) / PC::GH) * prm.max_parts;
+        const int grid = (int)std::min<int64_t>((int64_t)sm_count() * per_sm, max_units);
+        e = cudaMemsetAsync(prm.counter, 0, sizeof(int32_t), stream);
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "pa_decode_attention: memset: %s", cudaGetErrorString(e));
+        kern<<<grid, threads, use_smem, stream>>>(prm);
+    } else {
+        using L = GridCfg<D, B>;
+        auto kern = paged_decode_grid<D, B>;
+        e = set_smem_once<KernelTag<D, B, false>>(kern, L::TOTAL);
+        if (e != cudaSuccess)
+            return fail(PA_ERR_CUDA, "pa_decode_attention: cudaFuncSetAttribute: %s",
+                        cudaGetErrorString(e));
+        dim3 grid(prm.max_parts, prm.num_heads, prm.n_seqs);
+        kern<<<grid, L::WARPS * 32, L::TOTAL, stream>>>(prm);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "pa_decode_attention: launch: %s", cudaGetErrorString(e));
     if (prm.max_parts > 1) {
@@ -424,16 +972,6 @@ int launch_cfg(const DecodeParams &prm, int part_tokens, cudaStream_t stream) {
                         cudaGetErrorString(e));
     }
     return PA_OK;
-}
-
-template <int D, int B>
-int launch_db(const DecodeParams &prm, int part_tokens, cudaStream_t stream) {
-#if defined(PA_TUNE_WARPS) && defined(PA_TUNE_STAGES)
-    if (D == 128 && B == 16)
-        return launch_cfg<D, B, PA_TUNE_WARPS, PA_TUNE_STAGES>(prm, part_tokens, stream);
-#endif
-    return launch_cfg<D, B, DefaultCfg<D, B>::WARPS, DefaultCfg<D, B>::STAGES>(prm, part_tokens,
-                                                                             stream);
 }
 
 template <int D>
@@ -458,11 +996,13 @@ int max_parts_of(int32_t max_blocks, int part_blocks) {
 size_t decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_pool_desc *d) {
     std::string why;
     if (!d || n_seqs < 0 || max_blocks < 0 || !device_geometry_ok(d, &why)) return 0;
+    if (n_seqs == 0) return 0;
     const int part_blocks = partition_tokens_of(d) / d->block_size;
     const int mp = max_parts_of(max_blocks, part_blocks);
-    if (mp <= 1) return 0;
+    if (mp <= 1) return kCounterBytes;
     const size_t rows = (size_t)n_seqs * d->num_heads * mp;
-    return align256(rows * 2 * sizeof(float)) + align256(rows * d->head_dim * sizeof(float));
+    return kCounterBytes + align256(rows * 2 * sizeof(float)) +
+           align256(rows * d->head_dim * sizeof(float));
 }
 
 int launch_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -490,14 +1030,12 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
     const int part_blocks = part_tokens / d->block_size;
     const int mp = max_parts_of(max_blocks, part_blocks);
     const size_t need = decode_workspace_bytes(n_seqs, max_blocks, d);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need)
-            return fail(PA_ERR_INVALID_ARG,
-                        "pa_decode_attention: workspace of %zu bytes needed, %zu given", need,
-                        workspace ? workspace_bytes : (size_t)0);
-        if (reinterpret_cast<uintptr_t>(workspace) & 255)
-            return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: workspace must be 256-byte aligned");
-    }
+    if (!workspace || workspace_bytes < need)
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention: workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: workspace must be 256-byte aligned");
     DecodeParams prm{};
     prm.out = static_cast<__half *>(out);
     prm.q = static_cast<const __half *>(q);
@@ -505,11 +1043,13 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
     prm.v_cache = static_cast<const __half *>(v_cache);
     prm.block_tables = block_tables;
     prm.ctx_lens = ctx_lens;
+    char *ws = static_cast<char *>(workspace);
+    prm.counter = reinterpret_cast<int32_t *>(ws);
     const size_t rows = (size_t)n_seqs * d->num_heads * mp;
-    prm.ws_ml = need ? static_cast<float *>(workspace) : nullptr;
-    prm.ws_acc = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                                  align256(rows * 2 * sizeof(float)))
-                      : nullptr;
+    prm.ws_ml = mp > 1 ? reinterpret_cast<float *>(ws + kCounterBytes) : nullptr;
+    prm.ws_acc = mp > 1 ? reinterpret_cast<float *>(ws + kCounterBytes +
+                                                    align256(rows * 2 * sizeof(float)))
+                        : nullptr;
     prm.status = status;
     prm.n_seqs = n_seqs;
     prm.num_heads = d->num_heads;

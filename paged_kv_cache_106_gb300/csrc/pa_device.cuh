@@ -99,6 +99,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Start fetching global memory into L2 (no shared memory, no completion).
+// addr and bytes must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void half8_to_float8(const uint4 &u, float f[8]) {
     const __half2 *h = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll

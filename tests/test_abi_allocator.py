@@ -196,7 +196,8 @@ def test_device_calls_reject_bad_geometry_before_any_cuda_work():
     ws = pk.pa_decode_workspace_bytes(3, 128, d)
     rows = 3 * 40 * 4
     assert ws >= rows * (128 + 2) * 4
-    assert pk.pa_decode_workspace_bytes(3, 32, d) == 0     # one partition: no workspace
+    assert pk.pa_decode_workspace_bytes(3, 32, d) == 256   # one partition: scheduling word only
+    assert pk.pa_decode_workspace_bytes(0, 32, d) == 0
     # NULL pointers with a valid geometry are refused on the host
     assert pk._lib.pa_write_kv(None, None, None, 1, None, None, d.ref, None, None) == \
         pk.PA_ERR_INVALID_ARG

@@ -241,3 +241,42 @@ def test_context_longer_than_table_is_reported():
     st = _status()
     _gpu_attention(q, kc, vc, tables, ctxa, 0.1, 8, status=st)
     assert st.item() == pk.PA_ERR_BAD_BLOCK
+
+
+def test_attention_many_short_units_persistent_path():
+    """Hundreds of 1-3 block contexts: more units in flight than unit slots."""
+    rng = np.random.default_rng(23)
+    ctx = list(rng.integers(1, 41, size=500)) + [0, 1, 16, 17]
+    q, kc, vc, tables, ctxa = _random_paged_batch(rng, ctx, 3, 128, 16)
+    ref = oa.paged_attention(q, kc, vc, tables, ctxa, 0.088)
+    got = _gpu_attention(q, kc, vc, tables, ctxa, 0.088, 16)
+    assert np.abs(got.astype(np.float64) - ref).max() <= TOL
+
+
+def test_attention_large_batch_grid_fallback_path():
+    """More sequences than the persistent kernel plans in shared memory."""
+    rng = np.random.default_rng(25)
+    ctx = list(rng.integers(0, 120, size=2100))
+    q, kc, vc, tables, ctxa = _random_paged_batch(rng, ctx, 2, 64, 8)
+    ref = oa.paged_attention(q, kc, vc, tables, ctxa, 0.125)
+    for pt in (0, 32):
+        got = _gpu_attention(q, kc, vc, tables, ctxa, 0.125, 8, partition_tokens=pt)
+        assert np.abs(got.astype(np.float64) - ref).max() <= TOL
+
+
+def test_attention_repeated_calls_reuse_workspace():
+    """The scheduling word in the workspace is cleared by every call."""
+    rng = np.random.default_rng(27)
+    q, kc, vc, tables, ctxa = _random_paged_batch(rng, [600, 5, 1300, 64], 4, 128, 16)
+    desc = pk.PoolDesc(kc.shape[0], 16, num_heads=4, head_dim=128)
+    ws = torch.zeros(pk.pa_decode_workspace_bytes(4, tables.shape[1], desc), dtype=torch.uint8,
+                     device="cuda")
+    ref = oa.paged_attention(q, kc, vc, tables, ctxa, 0.1)
+    dq, dk, dv, dt, dc = _dev(q), _dev(kc), _dev(vc), _dev(tables), _dev(ctxa)
+    st = _status()
+    for _ in range(3):
+        out = torch.full((4, 4, 128), float("nan"), dtype=torch.float16, device="cuda")
+        pk.pa_decode_attention(out, dq, dk, dv, dt, dc, 0.1, desc, workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert np.abs(out.cpu().numpy().astype(np.float64) - ref).max() <= TOL
