@@ -235,6 +235,39 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
                         int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
                         int32_t *status, const pa_pool_desc *desc, void *stream);
 
+/* ---- decode attention without a caller-provided workspace ------------------
+ * No counterpart on the pages: this entry point exists for callers that
+ * cannot allocate device memory when they run attention -- for instance a
+ * runtime that reserves all device memory up front and gives its kernels no
+ * allocator, or a plugin host that forbids cudaMalloc (an allocation can
+ * fail or synchronise the device) once serving has started.
+ *
+ * Same arguments and result as pa_decode_attention, minus the workspace: the
+ * library uses a fixed scratch area of PA_NOALLOC_SCRATCH_BYTES compiled into
+ * it as a static device array.  Every GPU on which the library is loaded
+ * holds that array until the process exits.  The call allocates nothing
+ * (no cudaMalloc / cudaFree or allocating library routine); it clears the
+ * scratch's scheduling word on the stream itself.
+ *
+ *   - A batch whose pa_decode_workspace_bytes(n_seqs, max_blocks, desc)
+ *     exceeds PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_INVALID_ARG
+ *     before any device work.
+ *   - The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - All calls share the one scratch area, which keeps the last call's
+ *     contents: calls whose work overlaps on the GPU (different streams,
+ *     threads or processes sharing the context, without ordering between
+ *     them) race and give wrong results.  Order them, e.g. on one stream.
+ * Errors: as pa_decode_attention, plus PA_ERR_INVALID_ARG for a batch too
+ * large for the scratch and PA_ERR_CUDA if the scratch address lookup fails. */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+int pa_decode_attention_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables, const int32_t *ctx_lens,
+                                int32_t n_seqs, int32_t max_blocks, float scale,
+                                int32_t *status, const pa_pool_desc *desc, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

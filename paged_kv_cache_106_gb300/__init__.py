@@ -28,6 +28,7 @@ PA_ERR_TIMEOUT = 5
 PA_ERR_BAD_BLOCK = 6
 PA_DTYPE_F16 = 0
 PA_DEFAULT_PARTITION_TOKENS = 512
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _ERR_NAMES = {1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_OUT_OF_BLOCKS", 3: "PA_ERR_NO_SEQ",
               4: "PA_ERR_CUDA", 5: "PA_ERR_TIMEOUT", 6: "PA_ERR_BAD_BLOCK"}
@@ -84,6 +85,8 @@ def _load():
         "pa_decode_workspace_bytes": (sz, [i32, i32, P(pa_pool_desc)]),
         "pa_decode_attention": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, vp, sz,
                                       vp, P(pa_pool_desc), vp]),
+        "pa_decode_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float,
+                                              vp, P(pa_pool_desc), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -260,3 +263,18 @@ def pa_decode_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, scale:
                                     _dev(block_tables), _dev(ctx_lens), n, mb,
                                     ctypes.c_float(scale), _dev(workspace), ws_bytes,
                                     _dev(status), desc.ref, _stream(stream)))
+
+
+def pa_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, ctx_lens, scale: float,
+                                desc: PoolDesc, status=None, stream=None,
+                                n_seqs: int | None = None, max_blocks: int | None = None) -> None:
+    """pa_decode_attention without a workspace argument, for callers that cannot
+    allocate device memory when they run attention: the library's fixed
+    scratch (PA_NOALLOC_SCRATCH_BYTES, shared by all calls) stands in for it.
+    Calls that overlap on the GPU race on that scratch."""
+    n = int(q.shape[0]) if n_seqs is None else int(n_seqs)
+    mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
+    _check(_lib.pa_decode_attention_noalloc(_dev(out), _dev(q), _dev(k_cache), _dev(v_cache),
+                                            _dev(block_tables), _dev(ctx_lens), n, mb,
+                                            ctypes.c_float(scale), _dev(status), desc.ref,
+                                            _stream(stream)))

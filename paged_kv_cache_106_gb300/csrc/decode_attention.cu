@@ -1071,3 +1071,51 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
 }
 
 }  // namespace pagedkv
+
+// ------------------------------------------------ workspace-free entry point
+//
+// For callers that cannot allocate device memory at call time (a runtime that
+// owns all device memory, a plugin host that forbids cudaMalloc once serving
+// has started): the workspace of pa_decode_attention comes from this fixed
+// array instead.  Every device that loads the library holds it until exit.
+// Host code cannot use the array's name as an address (on the host it is only
+// a stand-in for the symbol): the device address is looked up with
+// cudaGetSymbolAddress, once per device, with that device current, on the
+// first call there.  All calls share the array; concurrent calls race.
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+std::once_flag g_noalloc_once[64];
+void *g_noalloc_ptr[64];
+cudaError_t g_noalloc_err[64];
+}  // namespace
+
+extern "C" int pa_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                           const void *v_cache, const int32_t *block_tables,
+                                           const int32_t *ctx_lens, int32_t n_seqs,
+                                           int32_t max_blocks, float scale, int32_t *status,
+                                           const pa_pool_desc *desc, void *stream) {
+    using namespace pagedkv;
+    if (!desc) return fail(PA_ERR_INVALID_ARG, "pa_decode_attention_noalloc: NULL desc");
+    const size_t need = decode_workspace_bytes(n_seqs, max_blocks, desc);
+    if (need > PA_NOALLOC_SCRATCH_BYTES)
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_noalloc: the batch needs %zu bytes of scratch, the "
+                    "fixed scratch holds %zu (use pa_decode_attention with a workspace)",
+                    need, (size_t)PA_NOALLOC_SCRATCH_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64)
+        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaGetDevice: %s",
+                    cudaGetErrorString(e));
+    std::call_once(g_noalloc_once[dev], [&] {
+        void *ptr = nullptr;
+        g_noalloc_err[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        g_noalloc_ptr[dev] = ptr;
+    });
+    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev])
+        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaGetSymbolAddress: %s",
+                    cudaGetErrorString(g_noalloc_err[dev]));
+    return launch_decode_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, n_seqs,
+                                   max_blocks, scale, g_noalloc_ptr[dev],
+                                   (size_t)PA_NOALLOC_SCRATCH_BYTES, status, desc, stream);
+}
