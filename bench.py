@@ -193,11 +193,18 @@ def run_ours(args):
     merge = pk.pa_decode_workspace_bytes(S, max_blocks, desc) > 0
     bytes_fixed = S * H * D * 2 * 2       # q read + o written
 
+    dump = [] if args.dump_steps else None
+
     def step(ev_pair=None, stats=None):
         batch.admit(ids)
         n_cp = runner.prepare()
         batch.appended()
         ctx = runner.ctx_host.astype(np.int64)
+        if dump is not None:
+            nblk_d = (ctx + B - 1) // B
+            dump.append({"tokens": int(ctx.sum()),
+                         "attn_bytes": int(ctx.sum()) * H * D * 4 + int(nblk_d.sum()) * 4
+                         + S * 4 + bytes_fixed})
         runner.copy_blocks([kc], [vc])
         runner.write_kv(k_new, v_new, kc, vc)
         if ev_pair is not None:
@@ -238,6 +245,9 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     clocks = sampler.stop()
+    if dump is not None and rank == 0:
+        with open(args.dump_steps, "w") as f:
+            json.dump({"warmup": args.warmup, "steps": dump}, f)
     elapsed = t0.elapsed_time(t1) / 1e3
     attn_ms = [a.elapsed_time(b) for a, b in evs]
     assert runner.status.item() == 0, f"device status {runner.status.item()}"
@@ -309,7 +319,7 @@ def run_ours(args):
             "gpu_launches": stats["launches"],
             "roofline": {
                 "bound": "hbm",
-                "kernel": "paged_decode_kernel + paged_merge_kernel (pa_decode_attention)",
+                "kernel": "paged_decode_persistent + paged_merge_kernel (pa_decode_attention)",
                 "achieved": achieved,
                 "peak": peak,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -318,6 +328,8 @@ def run_ours(args):
                 "frac": achieved / peak,
                 "frac_of_nominal_7900": achieved / 7900.0,
                 "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                "traffic_over_algorithmic": None if traffic is None
+                else traffic["traffic_over_algorithmic"],
                 "algorithmic_bytes_per_launch": stats["attn_bytes"] / args.steps,
                 "attn_ms_per_launch": attn_avg_s * 1e3,
                 "attn_share_of_step": attn_avg_s / (elapsed_max / args.steps),
@@ -427,6 +439,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)
+    ap.add_argument("--dump-steps", default="",
+                    help="write each warm-up and timed step's algorithmic attention bytes here")
     ap.add_argument("--partition", type=int, default=0,
                     help="split-context partition in tokens (default: the workload's 512)")
     args = ap.parse_args()
