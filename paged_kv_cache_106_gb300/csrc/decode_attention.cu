@@ -66,7 +66,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMaxPersistentSeqs = 2048;   // per-CTA prefix sums live in shared memory
+constexpr int kMaxPersistentSeqs = 2048;   // the per-CTA work plan lives in shared memory
 constexpr size_t kCounterBytes = 256;      // workspace head: the unit ticket counter
 
 template <int D, int B>
@@ -264,7 +264,7 @@ struct PLayout {
     static constexpr int UNIT_OFF = align16(DESC_OFF + STAGES * 8);     // 16 int per unit slot
     static constexpr int Q_OFF = align16(UNIT_OFF + R * 64);            // GH * D halves per slot
     static constexpr int COMB_OFF = align16(Q_OFF + R * GH * D * 2);
-    static constexpr int SEQ_OFF = align16(COMB_OFF + R * C * GH * (D + 2) * 4);  // prefix[S+1]
+    static constexpr int SEQ_OFF = align16(COMB_OFF + R * C * GH * (D + 2) * 4);  // plan, 2S+2 ints
     static_assert(Q_OFF % 16 == 0 && FULL_OFF % 8 == 0 && DESC_OFF % 8 == 0, "alignment");
     static constexpr int fixed_bytes() { return SEQ_OFF + 128; }     // +128: base alignment
     static size_t bytes(int n_seqs) { return fixed_bytes() + (size_t)(2 * n_seqs + 2) * 4; }
@@ -295,7 +295,15 @@ paged_decode_persistent(const DecodeParams p) {
     int32_t *units = reinterpret_cast<int32_t *>(smem + L::UNIT_OFF);
     __half *qs = reinterpret_cast<__half *>(smem + L::Q_OFF);
     float *comb = reinterpret_cast<float *>(smem + L::COMB_OFF);
-    int32_t *prefix = reinterpret_cast<int32_t *>(smem + L::SEQ_OFF);   // partitions before s
+    // Work plan (same in every CTA, so a ticket names the same unit everywhere):
+    //  fullpre[s]  full partitions (every partition but a context's last one)
+    //              of the sequences before s; fullpre[S] = F;
+    //  order[r]    the r-th last partition, (s | partition << 16), grouped by
+    //              size class, largest first, sequence order within a class.
+    // Tickets F*HG.. run through order[]: big units go first and the stream
+    // ends with the smallest ones, which keeps the CTAs' finishing times close.
+    int32_t *fullpre = reinterpret_cast<int32_t *>(smem + L::SEQ_OFF);
+    int32_t *order = fullpre + p.n_seqs + 1;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -316,37 +324,76 @@ paged_decode_persistent(const DecodeParams p) {
     __syncthreads();
     // A context of 0 is one unit (its output is zero); a context the table
     // row cannot hold is reported and gets no unit.
-    auto parts_of = [&](int c) {
-        if (c > p.max_blocks * B) return 0;
-        return c <= 0 ? 1 : ((c + B - 1) / B + p.part_blocks - 1) / p.part_blocks;
+    const int PB = p.part_blocks;
+    auto plan_of = [&](int c, int &n_parts, int &cls) {
+        if (c > p.max_blocks * B) {
+            n_parts = 0;
+            cls = 0;
+            return;
+        }
+        const int nblk = c <= 0 ? 0 : (c + B - 1) / B;
+        n_parts = c <= 0 ? 1 : (nblk + PB - 1) / PB;
+        const int last = nblk - (n_parts - 1) * PB;     // blocks of the last partition
+        cls = 4 * last >= 3 * PB ? 0 : (2 * last >= PB ? 1 : (4 * last >= PB ? 2 :
+              (8 * last >= PB ? 3 : 4)));
     };
-    for (int s = tid; s < S; s += blockDim.x) {
-        const int c = p.ctx_lens[s];
-        if (c > p.max_blocks * B && blockIdx.x == 0) report(p.status, PA_ERR_BAD_BLOCK);
-        prefix[s] = parts_of(c);   // counts first, turned into exclusive sums below
-    }
-    __syncthreads();
-    if (warp == 0) {   // exclusive prefix sum of partitions per sequence
+    constexpr int NCLS = 5;
+    if (warp == 0) {
         const int per = (S + 31) / 32;
         const int lo = min(S, lane * per), hi = min(S, lo + per);
-        int sum = 0;
-        for (int s = lo; s < hi; ++s) sum += prefix[s];
-        int incl = sum;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(kFull, incl, off);
-            if (lane >= off) incl += y;
-        }
-        int run = incl - sum;
+        int nfull = 0, ncls[NCLS] = {0, 0, 0, 0, 0};
         for (int s = lo; s < hi; ++s) {
-            const int n = prefix[s];
-            prefix[s] = run;
-            run += n;
+            const int c = p.ctx_lens[s];
+            if (c > p.max_blocks * B && blockIdx.x == 0) report(p.status, PA_ERR_BAD_BLOCK);
+            int np, cls;
+            plan_of(c, np, cls);
+            if (np > 0) {
+                nfull += np - 1;
+#pragma unroll
+                for (int k = 0; k < NCLS; ++k) ncls[k] += cls == k;
+            }
         }
-        if (lane == 31) prefix[S] = incl;
+        // exclusive scans over lanes: full partitions, and each class
+        auto scan = [&](int v, int &total) {
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, off);
+                if (lane >= off) incl += y;
+            }
+            total = __shfl_sync(kFull, incl, 31);
+            return incl - v;
+        };
+        int F;
+        int frun = scan(nfull, F);
+        int cbase[NCLS], start = 0;
+#pragma unroll
+        for (int k = 0; k < NCLS; ++k) {
+            int tot;
+            cbase[k] = start + scan(ncls[k], tot);
+            start += tot;
+        }
+        for (int s = lo; s < hi; ++s) {
+            int np, cls;
+            plan_of(p.ctx_lens[s], np, cls);
+            fullpre[s] = frun;
+            if (np > 0) {
+                frun += np - 1;
+                int r = 0;
+#pragma unroll
+                for (int k = 0; k < NCLS; ++k)
+                    if (cls == k) r = cbase[k]++;
+                order[r] = s | ((np - 1) << 16);
+            }
+        }
+        if (lane == 0) {
+            fullpre[S] = F;
+            order[S] = start;          // number of last partitions (scratch slot)
+        }
     }
     __syncthreads();
-    const int n_units = prefix[S] * HG;
+    const int n_full = fullpre[S];
+    const int n_units = (n_full + order[S]) * HG;
 
     if (warp == C * GH) {
         // ================================================ producer warp
@@ -379,14 +426,23 @@ paged_decode_persistent(const DecodeParams p) {
             const int hg = ticket - gp * HG;
             u.h0 = hg * GH;
             u.nh = min(GH, H - u.h0);
-            int lo = 0, hi = S - 1;   // last sequence s with prefix[s] <= gp
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (prefix[mid] <= gp) lo = mid; else hi = mid - 1;
+            int lo;
+            if (gp < n_full) {   // a full partition: last sequence s with fullpre[s] <= gp
+                lo = 0;
+                int hi = S - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (fullpre[mid] <= gp) lo = mid; else hi = mid - 1;
+                }
+                u.part = gp - fullpre[lo];
+                u.n_parts = 2;       // more than one partition: the unit leaves a partial
+            } else {             // a context's last partition
+                const int e = order[gp - n_full];
+                lo = e & 0xffff;
+                u.part = e >> 16;
+                u.n_parts = u.part + 1;
             }
             u.s = lo;
-            u.part = gp - prefix[lo];
-            u.n_parts = prefix[lo + 1] - prefix[lo];
             u.j0 = u.part * p.part_blocks;
             u.ctx = p.ctx_lens[lo];
             if (u.j0 + lane < p.max_blocks)
@@ -801,8 +857,12 @@ paged_decode_grid(const DecodeParams p) {
 }
 
 // One warp per (sequence, head) whose context spans more than one partition.
+// All loads of a pass are issued before any is used: lane q holds partition
+// q's (max, sum), every lane its D/32 output dims of up to 8 partitions.
 template <int D>
 __global__ void __launch_bounds__(128) paged_merge_kernel(const DecodeParams p, int part_tokens) {
+    constexpr int DL = D >= 32 ? D / 32 : 1;   // dims per lane
+    constexpr int QB = 8;                      // partitions per pass
     const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     const int H = p.num_heads;
@@ -813,22 +873,43 @@ __global__ void __launch_bounds__(128) paged_merge_kernel(const DecodeParams p, 
     const int n_parts = ctx > 0 ? (ctx + part_tokens - 1) / part_tokens : 0;
     if (n_parts <= 1 || n_parts > p.max_parts) return;
     const size_t base = ((size_t)s * H + h) * p.max_parts;
+    const float2 *ml = reinterpret_cast<const float2 *>(p.ws_ml) + base;
     float M = -INFINITY;
-    for (int q = lane; q < n_parts; q += 32) M = fmaxf(M, p.ws_ml[2 * (base + q)]);
+    for (int q = lane; q < n_parts; q += 32) M = fmaxf(M, ml[q].x);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    float Lt = 0.f;
-    for (int q = lane; q < n_parts; q += 32)
-        Lt += exp2f(p.ws_ml[2 * (base + q)] - M) * p.ws_ml[2 * (base + q) + 1];
+    float o[DL];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) Lt += __shfl_xor_sync(kFull, Lt, off);
+    for (int k = 0; k < DL; ++k) o[k] = 0.f;
+    float Lt = 0.f;
+    for (int q0 = 0; q0 < n_parts; q0 += QB) {
+        float a[QB][DL];
+#pragma unroll
+        for (int q = 0; q < QB; ++q)
+#pragma unroll
+            for (int k = 0; k < DL; ++k) {
+                const int d = lane + 32 * k;
+                a[q][k] = (q0 + q < n_parts && d < D) ? p.ws_acc[(base + q0 + q) * D + d] : 0.f;
+            }
+        const float2 mine = q0 + lane < n_parts && lane < QB ? ml[q0 + lane] : make_float2(-INFINITY, 0.f);
+        const float w = exp2f(mine.x - M);
+        float lw = w * mine.y;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) lw += __shfl_xor_sync(kFull, lw, off);
+        Lt += lw;
+#pragma unroll
+        for (int q = 0; q < QB; ++q) {
+            const float wq = __shfl_sync(kFull, w, q);
+#pragma unroll
+            for (int k = 0; k < DL; ++k) o[k] = fmaf(wq, a[q][k], o[k]);
+        }
+    }
     const float inv = 1.0f / Lt;
     __half *out_row = p.out + ((size_t)s * H + h) * D;
-    for (int d = lane; d < D; d += 32) {
-        float o = 0.f;
-        for (int q = 0; q < n_parts; ++q)
-            o = fmaf(exp2f(p.ws_ml[2 * (base + q)] - M), p.ws_acc[(base + q) * D + d], o);
-        out_row[d] = __float2half(o * inv);
+#pragma unroll
+    for (int k = 0; k < DL; ++k) {
+        const int d = lane + 32 * k;
+        if (d < D) out_row[d] = __float2half(o[k] * inv);
     }
 }
 
