@@ -119,6 +119,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_across_ranks(to_sum, to_max, device):
+    """Whole-job numbers: work summed over ranks, times maxed over ranks
+    (no-op without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+
+    tot = torch.tensor([float(x) for x in to_sum], dtype=torch.float64, device=device)
+    mx = torch.tensor([float(x) for x in to_max], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    return tot.tolist(), mx.tolist()
+
+
 def _pool_setup(pk, w):
     desc = pk.PoolDesc(w.num_blocks, w.block_size, num_layers=1, num_heads=w.num_heads,
                        head_dim=w.head_dim, partition_tokens=w.split_tokens,
@@ -195,9 +209,15 @@ def run_ours(args):
 
     dump = [] if args.dump_steps else None
 
+    host_s = []
+
     def step(ev_pair=None, stats=None):
+        h0 = time.perf_counter()
         batch.admit(ids)
+        h_admit = time.perf_counter() - h0
         n_cp = runner.prepare()
+        if stats is not None:
+            host_s.append(h_admit + runner.host_seconds)
         batch.appended()
         ctx = runner.ctx_host.astype(np.int64)
         if dump is not None:
@@ -206,6 +226,8 @@ def run_ours(args):
                          "attn_bytes": int(ctx.sum()) * H * D * 4 + int(nblk_d.sum()) * 4
                          + S * 4 + bytes_fixed})
         runner.copy_blocks([kc], [vc])
+        if ev_pair is not None:
+            ev_pair[2].record(stream)
         runner.write_kv(k_new, v_new, kc, vc)
         if ev_pair is not None:
             ev_pair[0].record(stream)
@@ -230,7 +252,7 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     stats = {"tokens": 0, "attn_bytes": 0, "launches": 0, "copies": 0}
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -249,7 +271,9 @@ def run_ours(args):
         with open(args.dump_steps, "w") as f:
             json.dump({"warmup": args.warmup, "steps": dump}, f)
     elapsed = t0.elapsed_time(t1) / 1e3
-    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    write_ms = [e[2].elapsed_time(e[0]) for e in evs]
+    copy_stats = time_copy_blocks(pk, pool, desc, w, kc, vc, stream) if rank == 0 else None
     assert runner.status.item() == 0, f"device status {runner.status.item()}"
 
     # ---- e2e: host buffers, H2D of q/k/v and D2H of o inside every step
@@ -278,13 +302,8 @@ def run_ours(args):
     e2e_time = time.perf_counter() - w0
 
     # ---- reduce over ranks: max time, summed work
-    tot = torch.tensor([stats["tokens"], e2e_tokens], dtype=torch.float64, device=dev)
-    mx = torch.tensor([elapsed, e2e_time], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-    tokens_all, e2e_tokens_all = tot.tolist()
-    elapsed_max, e2e_max = mx.tolist()
+    (tokens_all, e2e_tokens_all), (elapsed_max, e2e_max) = reduce_across_ranks(
+        [stats["tokens"], e2e_tokens], [elapsed, e2e_time], dev)
 
     if rank == 0:
         peak, peak_kind = _peaks()
@@ -335,6 +354,20 @@ def run_ours(args):
                 "attn_share_of_step": attn_avg_s / (elapsed_max / args.steps),
             },
             "decode_tokens_per_s": ws * S * args.steps / elapsed_max,
+            "kernels": {
+                "pa_write_kv": {
+                    "us_per_launch": 1e3 * sum(write_ms) / len(write_ms),
+                    "algorithmic_bytes": 2 * 2 * S * H * D * 2 + 8 * S,
+                    "GB/s": (2 * 2 * S * H * D * 2 + 8 * S) / (sum(write_ms) / len(write_ms) / 1e3) / 1e9,
+                    "note": "new K/V of the batch read and scattered to their slots (timed in the step loop)",
+                },
+                "pa_copy_blocks": copy_stats,
+                "host_block_manager": {
+                    "us_per_step": 1e6 * sum(host_s) / len(host_s),
+                    "note": "host wall clock per step: free/admit finished sequences, pa_alloc_slots "
+                            "and pa_get_block_tables for the batch (waits on the GPU excluded)",
+                },
+            },
             "e2e": {
                 "value": e2e_tokens_all / e2e_max,
                 "unit": UNIT,
@@ -351,6 +384,147 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
+    pk.pa_pool_destroy(pool)
+
+
+def time_copy_blocks(pk, pool, desc, w, kc, vc, stream, n_pairs=256, reps=50):
+    """Copy-on-write-sized batch of block copies (one layer, K and V): live
+    blocks into free ones, timed with CUDA events on the launching stream."""
+    import torch
+
+    free = pk.pa_pool_free_queue(pool, w.num_blocks)
+    refs = pk.pa_pool_refcounts(pool, w.num_blocks)
+    used = np.nonzero(refs > 0)[0]
+    n = int(min(n_pairs, len(free), len(used)))
+    if n == 0:
+        return None
+    rng = np.random.default_rng(5)
+    pairs = np.stack([rng.choice(used, n, replace=False), free[:n]], axis=1).astype(np.int32)
+    d_pairs = torch.from_numpy(pairs).to(kc.device)
+    status = torch.zeros(1, dtype=torch.int32, device=kc.device)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            pk.pa_copy_blocks([kc], [vc], d_pairs, desc, status=status, stream=stream)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            pk.pa_copy_blocks([kc], [vc], d_pairs, desc, status=status, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    us = a.elapsed_time(b) * 1e3 / reps
+    nbytes = n * 2 * w.num_heads * w.block_size * w.head_dim * 2 * 2 + n * 8
+    return {"pairs": n, "layers": 1, "us_per_launch": us, "algorithmic_bytes": nbytes,
+            "GB/s": nbytes / (us / 1e6) / 1e9,
+            "note": "blocks of live sequences copied into free blocks, K and V (read + write)"}
+
+
+def run_full40(args):
+    """The 40-layer decode step over a pool-filling cache (one GPU).
+
+    The K/V pool takes min(120 GB, half the free device memory); sequences
+    with context uniform in [512, 2048] fill it; with --beam, groups of 4 beams
+    share the first 55 % of their blocks.  One step = host block manager,
+    metadata upload, block copies (every layer) and, per layer, slot write and
+    decode attention.  Contexts grow by one token per step (warm-up + timed
+    steps must stay within the one spare block per sequence: <= 16).
+    """
+    import torch
+
+    import paged_kv_cache_106_gb300 as pk
+    from paged_kv_cache_106_gb300 import workloads as wl
+    from paged_kv_cache_106_gb300.step import DecodeStepRunner, admit_workload
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    free, _ = torch.cuda.mem_get_info(dev)
+    pool_bytes = int(min(120e9, 0.5 * free))
+    w = wl.full_40l(pool_bytes, beam=args.beam)
+    L, H, D, B = w.num_layers, w.num_heads, w.head_dim, w.block_size
+    if args.warmup + args.steps > 16:
+        raise SystemExit("full_40l: warm-up + steps must be <= 16 (one spare block per sequence)")
+    desc = pk.PoolDesc(w.num_blocks, B, num_layers=L, num_heads=H, head_dim=D,
+                       partition_tokens=w.split_tokens, free_order=w.free_order)
+    pool = pk.pa_pool_create(desc)
+    ids = np.array(admit_workload(pool, w), dtype=np.int32)
+    S = len(ids)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    kc_all = torch.empty((L, w.num_blocks, H, B, D), dtype=torch.float16, device=dev)
+    vc_all = torch.empty_like(kc_all)
+    kc_all.normal_(generator=gen)
+    vc_all.normal_(generator=gen)
+    kcs, vcs = list(kc_all.unbind(0)), list(vc_all.unbind(0))
+    q = torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+    k_new, v_new = torch.randn_like(q), torch.randn_like(q)
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    max_blocks = -(-(wl.CTX_CAP + 16) // B)
+    runner = DecodeStepRunner(pool, desc, ids, max_blocks, device=dev, stream=stream)
+    refs = pk.pa_pool_refcounts(pool, w.num_blocks)
+
+    def step(evs=None, stats=None):
+        runner.prepare()
+        ctx = runner.ctx_host.astype(np.int64)
+        runner.copy_blocks(kcs, vcs)
+        for l in range(L):
+            runner.write_kv(k_new, v_new, kcs[l], vcs[l])
+            if evs is not None:
+                evs[l][0].record(stream)
+            runner.attention(out, q, kcs[l], vcs[l], w.scale)
+            if evs is not None:
+                evs[l][1].record(stream)
+        if stats is not None:
+            nblk = (ctx + B - 1) // B
+            stats["tokens"] += int(ctx.sum()) * L
+            stats["attn_bytes"] += L * (int(ctx.sum()) * H * D * 4 + int(nblk.sum()) * 4 + S * 4
+                                        + S * H * D * 4)
+            stats["copies"] += runner.n_copies
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    stats = {"tokens": 0, "attn_bytes": 0, "copies": 0}
+    evs = [[tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(L)]
+           for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i], stats)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert runner.status.item() == 0, f"device status {runner.status.item()}"
+    elapsed = t0.elapsed_time(t1) / 1e3
+    attn_s = sum(a.elapsed_time(b) for layer in evs for a, b in layer) / 1e3
+    peak, peak_kind = _peaks()
+    achieved = stats["attn_bytes"] / attn_s / 1e9
+    print(json.dumps({
+        "metric": METRIC, "value": stats["tokens"] / elapsed, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": "full 40-layer OPT-13B-shaped decode step, pool-filling cache"
+                               + (", beam groups of 4 sharing 55 % of blocks" if args.beam else ""),
+                   "pool_bytes": pool_bytes, "pool_blocks": w.num_blocks, "sequences": S,
+                   "layers": L, "mean_ctx": stats["tokens"] / L / args.steps / S,
+                   "shared_blocks": int((refs > 1).sum()),
+                   "logical_over_unique_blocks": float((refs.sum()) / max(1, (refs > 0).sum())),
+                   "copies_per_step": stats["copies"] / args.steps},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes_per_step": stats["attn_bytes"] / args.steps,
+                     "attn_share_of_step": attn_s / elapsed,
+                     "note": "K/V counted once per referencing sequence (shared blocks once "
+                             "per beam): logical bytes"},
+        "clocks": clocks,
+    }), flush=True)
     pk.pa_pool_destroy(pool)
 
 
@@ -439,6 +613,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)
+    ap.add_argument("--workload", choices=["mixed_b256", "full_40l"], default="mixed_b256",
+                    help="mixed_b256: the headline workload; full_40l: 40-layer pool-filling step")
+    ap.add_argument("--beam", action="store_true", help="full_40l: beam groups sharing blocks")
     ap.add_argument("--dump-steps", default="",
                     help="write each warm-up and timed step's algorithmic attention bytes here")
     ap.add_argument("--partition", type=int, default=0,
@@ -448,6 +625,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "full_40l":
+        run_full40(args)
     else:
         run_ours(args)
 

@@ -17,6 +17,8 @@ calls and owns the staging buffers; the work runs in libpagedkv.so.
 """
 from __future__ import annotations
 
+import time
+
 import numpy as np
 import torch
 
@@ -57,6 +59,7 @@ class DecodeStepRunner:
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.n_copies = 0
         self.ctx_host = None
+        self.host_seconds = 0.0
         self.i = 0
 
     def _views(self, buf):
@@ -73,12 +76,14 @@ class DecodeStepRunner:
         self.i += 1
         if self.events[k] is not None:
             self.events[k].synchronize()     # staging buffer k no longer in flight
+        t0 = time.perf_counter()
         slots, ctx, tables, copies = self._views(self.host[k])
         _, cp = pa_alloc_slots(self.pool, self.ids, copies_cap=self.S, slot_out=slots,
                                copies_out=copies)
         self.n_copies = int(cp.shape[0])
         pa_get_block_tables(self.pool, self.ids, self.max_blocks, tables_out=tables, ctx_out=ctx)
         self.ctx_host = ctx
+        self.host_seconds = time.perf_counter() - t0   # block manager work of this step
         with torch.cuda.stream(self.stream):
             self.dev.copy_(self.host[k], non_blocking=True)
             ev = torch.cuda.Event()
@@ -106,3 +111,41 @@ class DecodeStepRunner:
         for l in range(len(k_caches)):
             self.write_kv(k_new[l], v_new[l], k_caches[l], v_caches[l])
             self.attention(out[l], q[l], k_caches[l], v_caches[l], scale)
+
+
+def admit_workload(pool, w) -> list:
+    """Admit a workload's sequences into a pool through the block manager.
+
+    A plain sequence is added with its prompt.  A beam group (root index in
+    ``w.forks`` with ``w.shared_prefix`` shared tokens) is added with the
+    shared prefix, forked into its beams, and every beam then appends its own
+    tokens one step at a time, so the beams share the prefix blocks through
+    reference counts.  Returns the sequence ids in batch order.
+    """
+    from . import pa_alloc_slots, pa_seq_add, pa_seq_fork
+
+    groups = {root: (extra, shared) for (root, extra), shared in
+              zip(w.forks, w.shared_prefix or [None] * len(w.forks))}
+    ids, next_id = [], len(w.prompt_lens)
+    growing = []          # (ids of a group, own tokens still to append)
+    for i, n in enumerate(w.prompt_lens):
+        if i not in groups:
+            pa_seq_add(pool, i, n, want_slots=False)
+            ids.append(i)
+            continue
+        extra, shared = groups[i]
+        shared = n if shared is None else shared
+        pa_seq_add(pool, i, shared, want_slots=False)
+        members = [i]
+        for _ in range(extra):
+            pa_seq_fork(pool, i, next_id)
+            members.append(next_id)
+            next_id += 1
+        ids.extend(members)
+        if n > shared:
+            growing.append((members, n - shared))
+    for t in range(max((g[1] for g in growing), default=0)):
+        batch = [s for members, own in growing if own > t for s in members]
+        if batch:
+            pa_alloc_slots(pool, batch)
+    return ids

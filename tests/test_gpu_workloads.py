@@ -183,3 +183,106 @@ def test_parallel_sampling_copy_on_write_64_steps():
     # every prompt whose last block is partial is copied for 3 of its 4 samples
     partial = sum(1 for p in w.prompt_lens if p % w.block_size)
     assert total_copies == 3 * partial
+
+
+def _oracle_admit(m: BlockManager, w):
+    """The workload's admission on the oracle's block manager (own loop)."""
+    groups = {root: (extra, shared) for (root, extra), shared in zip(w.forks, w.shared_prefix)}
+    ids, nxt, growing = [], len(w.prompt_lens), []
+    for i, n in enumerate(w.prompt_lens):
+        if i not in groups:
+            m.add(i, n)
+            ids.append(i)
+            continue
+        extra, shared = groups[i]
+        m.add(i, shared)
+        members = [i]
+        for _ in range(extra):
+            m.fork(i, nxt)
+            members.append(nxt)
+            nxt += 1
+        ids.extend(members)
+        growing.append((members, n - shared))
+    for t in range(max((g[1] for g in growing), default=0)):
+        batch = [s for members, own in growing if own > t for s in members]
+        if batch:
+            m.alloc_slots(batch)
+    return ids
+
+
+@pytest.mark.parametrize("beam", [False, True])
+def test_full_40_layer_pool_filling_step_sampled(beam):
+    """40 layers over a pool of min(120 GB, half the free memory), as the
+    benchmark's 40-layer mode runs it; layers 0 and 39 of a sample of
+    sequences (a whole beam group in the beam variant) checked."""
+    from paged_kv_cache_106_gb300.step import admit_workload
+
+    free = torch.cuda.mem_get_info()[0]
+    w = wl.full_40l(int(min(120e9, 0.5 * free)), beam=beam)
+    L, H, D, B, NB = w.num_layers, w.num_heads, w.head_dim, w.block_size, w.num_blocks
+    desc = pk.PoolDesc(NB, B, num_layers=L, num_heads=H, head_dim=D,
+                       partition_tokens=w.split_tokens, free_order=w.free_order)
+    pool = pk.pa_pool_create(desc)
+    ids = admit_workload(pool, w)
+    m = BlockManager(NB, B, w.free_order)
+    assert _oracle_admit(m, w) == ids
+    max_blocks = -(-(wl.CTX_CAP + 16) // B)
+    t_gpu, ctx_gpu = pk.pa_get_block_tables(pool, ids, max_blocks)
+    assert t_gpu.tolist() == m.padded_tables(ids, max_blocks)
+
+    rng = np.random.default_rng(77)
+    rows = sorted(set(rng.choice(len(ids), 6, replace=False).tolist()) | {int(np.argmax(ctx_gpu))})
+    if beam:
+        rows = sorted(set(rows) | set(range(4)))           # the first beam group
+    layers = [0, L - 1]
+    kc_all = torch.empty((L, NB, H, B, D), dtype=torch.float16, device="cuda")
+    vc_all = torch.empty_like(kc_all)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    kc_all.normal_(generator=g)
+    vc_all.normal_(generator=g)
+    vr = wl.value_rng(w, 3)
+    blocks = sorted({b for r in rows for b in m.block_table(ids[r])})
+    okc = {l: np.zeros((NB, H, B, D), np.float16) for l in layers}
+    ovc = {l: np.zeros((NB, H, B, D), np.float16) for l in layers}
+    bidx = torch.tensor(blocks, device="cuda")
+    for l in layers:
+        okc[l][blocks] = wl.normal_f16(vr, (len(blocks), H, B, D))
+        ovc[l][blocks] = wl.normal_f16(vr, (len(blocks), H, B, D))
+        kc_all[l][bidx] = torch.from_numpy(okc[l][blocks]).cuda()
+        vc_all[l][bidx] = torch.from_numpy(ovc[l][blocks]).cuda()
+    S = len(ids)
+    q = {l: wl.normal_f16(vr, (S, H, D)) for l in layers}
+    kn = {l: wl.normal_f16(vr, (S, H, D)) for l in layers}
+    vn = {l: wl.normal_f16(vr, (S, H, D)) for l in layers}
+
+    runner = DecodeStepRunner(pool, desc, ids, max_blocks)
+    runner.prepare()
+    slots_o, copies_o = m.alloc_slots(ids)
+    slots_g = runner._views(runner.host[0])[0]
+    assert slots_g.tolist() == slots_o
+    kcs, vcs = list(kc_all.unbind(0)), list(vc_all.unbind(0))
+    runner.copy_blocks(kcs, vcs)
+    assert [tuple(c) for c in runner._views(runner.host[0])[3][: runner.n_copies].tolist()] == copies_o
+    outs = {}
+    dev_rand = torch.randn((S, H, D), dtype=torch.float16, device="cuda", generator=g)
+    for l in range(L):
+        if l in layers:
+            qd, kd, vd = (torch.from_numpy(x[l]).cuda() for x in (q, kn, vn))
+        else:
+            qd = kd = vd = dev_rand
+        out = torch.empty((S, H, D), dtype=torch.float16, device="cuda")
+        runner.write_kv(kd, vd, kcs[l], vcs[l])
+        runner.attention(out, qd, kcs[l], vcs[l], w.scale)
+        if l in layers:
+            outs[l] = out
+    torch.cuda.synchronize()
+    assert runner.status.item() == 0
+    tables = np.array(m.padded_tables(ids, max_blocks), np.int32)
+    ctx = np.array([m.num_tokens(s) for s in ids], np.int32)
+    for l in layers:
+        oc.copy_blocks([okc[l]], [ovc[l]], copies_o)
+        oc.write_kv(okc[l], ovc[l], kn[l], vn[l], slots_o)
+        ref = oa.paged_attention(q[l][rows], okc[l], ovc[l], tables[rows], ctx[rows], w.scale)
+        assert _err(outs[l].cpu().numpy()[rows], ref) <= TOL, l
+    pk.pa_pool_destroy(pool)
