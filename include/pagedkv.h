@@ -76,6 +76,7 @@ extern "C" {
  *                     PA_DEFAULT_PARTITION_TOKENS; otherwise a positive
  *                     multiple of block_size (a value at least as long as
  *                     every context turns the split off)
+ *   flags             0 or PA_POOL_PREFIX_CACHING (host block manager only)
  *   free_order        (host, optional) initial order of the free-block queue,
  *                     a permutation of 0..num_blocks-1; NULL = 0,1,2,...
  *                     Read by pa_pool_create only.                          */
@@ -87,9 +88,12 @@ typedef struct pa_pool_desc {
     int32_t head_dim;
     int32_t dtype;
     int32_t partition_tokens;
-    int32_t reserved;
+    int32_t flags;
     const int32_t *free_order;
 } pa_pool_desc;
+
+/* pa_pool_desc.flags */
+#define PA_POOL_PREFIX_CACHING 1   /* keep full prompt blocks for reuse (pa_seq_add_tokens) */
 
 typedef struct pa_pool pa_pool;
 
@@ -119,6 +123,34 @@ int pa_pool_destroy(pa_pool *pool);
  * prompt token.  All-or-nothing.
  * Errors: PA_ERR_NO_SEQ (id in use), PA_ERR_OUT_OF_BLOCKS, PA_ERR_INVALID_ARG. */
 int pa_seq_add(pa_pool *pool, int32_t seq_id, int32_t n_tokens, int64_t *slots_out);
+
+/* Admit a sequence from its prompt's token ids, reusing cached blocks
+ * ([teardown] "PagedAttention" section, prefix sharing).  In a pool created
+ * with PA_POOL_PREFIX_CACHING every full block of a prompt is keyed by a hash
+ * chain over (its parent block's key, its B token ids, extra_key), so a key
+ * names the whole prefix up to that block.  The leading full blocks whose
+ * keys are cached (checked against the stored tokens, parent key and extra
+ * key) are touched instead of allocated: their reference count goes up and a
+ * cached block that was free leaves the free queue, no copy.  The scan stops
+ * at the first block that is not cached.  The remaining blocks come from the
+ * free queue, and the new full blocks are cached.  A cached block keeps its
+ * key while its count is 0 -- freed blocks join the tail of the free queue,
+ * so they are evicted (dropped from the cache) last, least recently freed
+ * first -- and loses it when the free queue hands it out again.  Blocks
+ * filled by later appends are not cached.
+ *   token_ids   (host) n_tokens int32 token ids
+ *   extra_key   mixed into every key (requests with different extra keys,
+ *               e.g. adapters, never share)
+ *   slots_out   (host, optional) slot of every prompt token
+ *   n_cached_out (host, optional) leading tokens whose K/V are already in
+ *               the cache (reused blocks x B): only the tokens after them need
+ *               their K/V written.
+ * Without PA_POOL_PREFIX_CACHING this is pa_seq_add (nothing is cached).
+ * All-or-nothing.  Errors: PA_ERR_NO_SEQ, PA_ERR_OUT_OF_BLOCKS,
+ * PA_ERR_INVALID_ARG.  pa_pool_cached_blocks: blocks currently cached. */
+int pa_seq_add_tokens(pa_pool *pool, int32_t seq_id, int32_t n_tokens, const int32_t *token_ids,
+                      int64_t extra_key, int64_t *slots_out, int32_t *n_cached_out);
+int pa_pool_cached_blocks(const pa_pool *pool, int32_t *n_cached);
 
 /* fork: the child gets a copy of the parent's block table and length, and
  * every block's reference count goes up by one ([notes] §4.2 fork;

@@ -38,6 +38,16 @@ Sources, in the order the steps are taken:
 * Failure: when the pool cannot cover a request, the allocation reports
   failure and changes nothing (teardown: allocate_slots returns None).
 
+* Prefix caching (vLLM teardown, "PagedAttention" section): every full
+  block of a prompt is identified by its whole prefix (the pages hash the
+  chain (parent hash, block tokens, extra keys)); a request whose leading full
+  blocks are cached touches them -- count + 1, no copy, a free cached block
+  leaves the free queue -- instead of allocating; the scan stops at the first
+  block that is not cached; freed cached blocks stay cached at the tail of
+  the free queue and are evicted (forgotten) only when the queue hands them
+  out again, least recently freed first.  Here the key is the exact token
+  prefix plus the extra key, so no hash is involved.
+
 Readings where the pages are silent (stated, not found on the pages): the
 queue is FIFO; a multi-sequence ``alloc_slots`` handles the sequences in the
 order given and is all-or-nothing as a whole; a sequence may appear only once
@@ -54,9 +64,13 @@ class OutOfBlocks(Exception):
 
 
 class BlockManager:
-    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+    def __init__(self, num_blocks: int, block_size: int, free_order=None,
+                 prefix_caching: bool = False):
         if num_blocks < 0 or block_size <= 0:
             raise ValueError("bad pool geometry")
+        self.prefix_caching = prefix_caching
+        self.cache = {}          # (extra_key, token prefix tuple) -> physical block
+        self.block_key = {}      # physical block -> its key while cached
         self.num_blocks = int(num_blocks)
         self.B = int(block_size)
         order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
@@ -95,6 +109,8 @@ class BlockManager:
         b = self.free_queue.popleft()
         assert self.ref[b] == 0
         self.ref[b] = 1
+        if b in self.block_key:               # evicted from the prefix cache
+            del self.cache[self.block_key.pop(b)]
         return b
 
     def _release_block(self, b: int) -> None:
@@ -119,6 +135,44 @@ class BlockManager:
             left -= self.B
         self.tables[seq_id] = table
         return [self.slot_of(seq_id, p) for p in range(n_tokens)]
+
+    def add_tokens(self, seq_id: int, tokens, extra_key: int = 0):
+        """Admit a sequence from its prompt tokens, reusing cached full blocks.
+
+        Returns (slots, n_cached_tokens)."""
+        if seq_id in self.tables:
+            raise ValueError("sequence exists")
+        tokens = [int(t) for t in tokens]
+        n, B = len(tokens), self.B
+        total, full = -(-n // B), n // B
+        hits = []
+        if self.prefix_caching:
+            for j in range(full):
+                b = self.cache.get((extra_key, tuple(tokens[:(j + 1) * B])))
+                if b is None:
+                    break
+                hits.append(b)
+        need = total - len(hits)
+        if need > len(self.free_queue) - sum(1 for b in hits if self.ref[b] == 0):
+            raise OutOfBlocks()
+        table = []
+        for b in hits:
+            if self.ref[b] == 0:
+                self.free_queue.remove(b)
+            self.ref[b] += 1
+            table.append([b, B])
+        left = n - len(hits) * B
+        for _ in range(need):
+            table.append([self._take_block(), min(B, left)])
+            left -= B
+        if self.prefix_caching:
+            for j in range(len(hits), full):
+                key = (extra_key, tuple(tokens[:(j + 1) * B]))
+                if key not in self.cache:
+                    self.cache[key] = table[j][0]
+                    self.block_key[table[j][0]] = key
+        self.tables[seq_id] = table
+        return [self.slot_of(seq_id, p) for p in range(n)], len(hits) * B
 
     def fork(self, parent: int, child: int) -> None:
         """Child shares every block of the parent; counts go up by one."""
@@ -170,7 +224,8 @@ class BlockManager:
         for s in seq_ids:
             if s not in self.tables:
                 raise KeyError(s)
-        saved = (copy.deepcopy(self.free_queue), list(self.ref), copy.deepcopy(self.tables))
+        saved = (copy.deepcopy(self.free_queue), list(self.ref), copy.deepcopy(self.tables),
+                 dict(self.cache), dict(self.block_key))
         slots, copies = [], []
         try:
             for s in seq_ids:
@@ -179,7 +234,7 @@ class BlockManager:
                 if cp is not None:
                     copies.append(cp)
         except OutOfBlocks:
-            self.free_queue, self.ref, self.tables = saved
+            self.free_queue, self.ref, self.tables, self.cache, self.block_key = saved
             raise
         return slots, copies
 
@@ -195,4 +250,5 @@ class BlockManager:
         return out
 
     def snapshot(self):
-        return copy.deepcopy((list(self.free_queue), list(self.ref), self.tables))
+        return copy.deepcopy((list(self.free_queue), list(self.ref), self.tables,
+                              sorted(self.block_key.items())))

@@ -27,6 +27,7 @@ PA_ERR_CUDA = 4
 PA_ERR_TIMEOUT = 5
 PA_ERR_BAD_BLOCK = 6
 PA_DTYPE_F16 = 0
+PA_POOL_PREFIX_CACHING = 1
 PA_DEFAULT_PARTITION_TOKENS = 512
 PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -53,7 +54,7 @@ class pa_pool_desc(ctypes.Structure):
         ("head_dim", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
         ("partition_tokens", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("flags", ctypes.c_int32),
         ("free_order", ctypes.POINTER(ctypes.c_int32)),
     ]
 
@@ -72,6 +73,8 @@ def _load():
         "pa_pool_create": (i32, [P(pa_pool_desc), P(vp)]),
         "pa_pool_destroy": (i32, [vp]),
         "pa_seq_add": (i32, [vp, i32, i32, vp]),
+        "pa_seq_add_tokens": (i32, [vp, i32, i32, vp, i64, vp, P(i32)]),
+        "pa_pool_cached_blocks": (i32, [vp, P(i32)]),
         "pa_seq_fork": (i32, [vp, i32, i32]),
         "pa_seq_free": (i32, [vp, i32]),
         "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
@@ -141,10 +144,10 @@ class PoolDesc:
     """Holds a pa_pool_desc (and keeps its free_order array alive)."""
 
     def __init__(self, num_blocks, block_size, num_layers=1, num_heads=1, head_dim=8,
-                 partition_tokens=0, free_order=None):
+                 partition_tokens=0, free_order=None, flags=0):
         self._free = None if free_order is None else _host_i32(free_order)
         self.c = pa_pool_desc(int(num_blocks), int(block_size), int(num_layers), int(num_heads),
-                              int(head_dim), PA_DTYPE_F16, int(partition_tokens), 0,
+                              int(head_dim), PA_DTYPE_F16, int(partition_tokens), int(flags),
                               None if self._free is None else
                               self._free.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)))
 
@@ -172,6 +175,24 @@ def pa_seq_add(pool, seq_id: int, n_tokens: int, want_slots: bool = True):
     _check(_lib.pa_seq_add(pool, int(seq_id), int(n_tokens),
                            None if slots is None else slots.ctypes.data))
     return slots
+
+
+def pa_seq_add_tokens(pool, seq_id: int, token_ids, extra_key: int = 0, want_slots: bool = True):
+    """Returns (slots int64[n] or None, n_cached_tokens)."""
+    toks = _host_i32(token_ids)
+    n = int(toks.shape[0])
+    slots = np.empty(n, np.int64) if want_slots else None
+    nc = ctypes.c_int32(0)
+    _check(_lib.pa_seq_add_tokens(pool, int(seq_id), n, toks.ctypes.data if n else None,
+                                  int(extra_key), None if slots is None else slots.ctypes.data,
+                                  ctypes.byref(nc)))
+    return slots, nc.value
+
+
+def pa_pool_cached_blocks(pool) -> int:
+    n = ctypes.c_int32()
+    _check(_lib.pa_pool_cached_blocks(pool, ctypes.byref(n)))
+    return n.value
 
 
 def pa_seq_fork(pool, parent: int, child: int) -> None:

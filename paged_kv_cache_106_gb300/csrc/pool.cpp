@@ -45,31 +45,82 @@ struct pa_pool {
     int32_t num_blocks = 0;
     int32_t block_size = 1;
     pa_pool_desc desc{};
-    // FIFO free queue as a ring over num_blocks entries.
-    std::vector<int32_t> ring;
-    int64_t head = 0;
+    bool caching = false;
+    // FIFO free queue as a doubly linked list over block ids (-1 = none), so
+    // that a cached free block can leave the middle of the queue when a new
+    // request reuses it.
+    std::vector<int32_t> nxt, prv;
+    std::vector<char> in_queue;
+    int32_t head = -1, tail = -1;
     int64_t count = 0;
     std::vector<int32_t> ref;
     std::unordered_map<int32_t, Seq> seqs;
+    // Prefix cache: full prompt blocks keyed by a hash chain over
+    // (parent key, the block's token ids, extra key).  Per block: its key,
+    // its parent's key, the extra key and its token ids, to verify a hit.
+    std::unordered_map<uint64_t, int32_t> cache;
+    std::vector<char> cached;
+    std::vector<uint64_t> key, parent_key;
+    std::vector<int64_t> extra;
+    std::vector<int32_t> tokens;   // [num_blocks][block_size]
 
-    int32_t pop_free() {
-        int32_t b = ring[(size_t)(head % num_blocks)];
-        head = (head + 1) % num_blocks;
-        --count;
-        ref[b] = 1;
-        return b;
-    }
-    void push_free(int32_t b) {
-        ring[(size_t)((head + count) % num_blocks)] = b;
+    void queue_push_tail(int32_t b) {
+        prv[(size_t)b] = tail;
+        nxt[(size_t)b] = -1;
+        if (tail >= 0) nxt[(size_t)tail] = b; else head = b;
+        tail = b;
+        in_queue[(size_t)b] = 1;
         ++count;
     }
+    void queue_remove(int32_t b) {
+        const int32_t p = prv[(size_t)b], n = nxt[(size_t)b];
+        if (p >= 0) nxt[(size_t)p] = n; else head = n;
+        if (n >= 0) prv[(size_t)n] = p; else tail = p;
+        in_queue[(size_t)b] = 0;
+        --count;
+    }
+    void uncache(int32_t b) {
+        if (!cached[(size_t)b]) return;
+        cache.erase(key[(size_t)b]);
+        cached[(size_t)b] = 0;
+    }
+    // Take the block at the head of the free queue; a cached block there is
+    // evicted from the prefix cache (it was the least recently freed).
+    int32_t pop_free() {
+        const int32_t b = head;
+        queue_remove(b);
+        uncache(b);
+        ref[(size_t)b] = 1;
+        return b;
+    }
     void release(int32_t b) {
-        if (--ref[b] == 0) push_free(b);
+        if (--ref[(size_t)b] == 0) queue_push_tail(b);
     }
     int32_t last_filled(const Seq &s) const {
         return s.num_tokens - (int32_t)(s.table.size() - 1) * block_size;
     }
 };
+
+namespace {
+
+// 64-bit mixing (splitmix64 finaliser) and the block key chain.
+uint64_t mix64(uint64_t x) {
+    x += 0x9e3779b97f4a7c15ull;
+    x = (x ^ (x >> 30)) * 0xbf58476d1ce4e5b9ull;
+    x = (x ^ (x >> 27)) * 0x94d049bb133111ebull;
+    return x ^ (x >> 31);
+}
+
+uint64_t block_key(uint64_t parent, const int32_t *tok, int32_t n, int64_t extra) {
+    uint64_t h = mix64(parent ^ 0x5bd1e995u);
+    h = mix64(h ^ (uint64_t)extra);
+    for (int32_t i = 0; i < n; ++i) h = mix64(h ^ (uint32_t)tok[i]);
+    return h;
+}
+
+constexpr uint64_t kRootKey = 0x243f6a8885a308d3ull;
+
+}  // namespace
 
 using pagedkv::fail;
 
@@ -79,22 +130,36 @@ int pa_pool_create(const pa_pool_desc *desc, pa_pool **out) {
     if (!desc || !out) return fail(PA_ERR_INVALID_ARG, "pa_pool_create: NULL argument");
     *out = nullptr;
     if (desc->num_blocks < 0 || desc->block_size < 1 || desc->num_layers < 1 ||
-        desc->num_heads < 1 || desc->head_dim < 1 || desc->dtype != PA_DTYPE_F16)
+        desc->num_heads < 1 || desc->head_dim < 1 || desc->dtype != PA_DTYPE_F16 ||
+        (desc->flags & ~PA_POOL_PREFIX_CACHING) != 0)
         return fail(PA_ERR_INVALID_ARG,
                     "pa_pool_create: bad geometry (num_blocks=%d block_size=%d num_layers=%d "
-                    "num_heads=%d head_dim=%d dtype=%d)",
+                    "num_heads=%d head_dim=%d dtype=%d flags=%d)",
                     desc->num_blocks, desc->block_size, desc->num_layers, desc->num_heads,
-                    desc->head_dim, desc->dtype);
+                    desc->head_dim, desc->dtype, desc->flags);
     pa_pool *p = new (std::nothrow) pa_pool();
     if (!p) return fail(PA_ERR_INVALID_ARG, "pa_pool_create: out of host memory");
     p->num_blocks = desc->num_blocks;
     p->block_size = desc->block_size;
     p->desc = *desc;
     p->desc.free_order = nullptr;
-    p->ring.resize((size_t)desc->num_blocks);
-    p->ref.assign((size_t)desc->num_blocks, 0);
+    const size_t nb = (size_t)desc->num_blocks;
+    p->nxt.assign(nb, -1);
+    p->prv.assign(nb, -1);
+    p->in_queue.assign(nb, 0);
+    p->ref.assign(nb, 0);
+    p->caching = (desc->flags & PA_POOL_PREFIX_CACHING) != 0;
+    if (p->caching) {
+        p->cached.assign(nb, 0);
+        p->key.assign(nb, 0);
+        p->parent_key.assign(nb, 0);
+        p->extra.assign(nb, 0);
+        p->tokens.assign(nb * (size_t)desc->block_size, 0);
+    } else {
+        p->cached.assign(nb, 0);
+    }
     if (desc->free_order) {
-        std::vector<char> seen((size_t)desc->num_blocks, 0);
+        std::vector<char> seen(nb, 0);
         for (int32_t i = 0; i < desc->num_blocks; ++i) {
             int32_t b = desc->free_order[i];
             if (b < 0 || b >= desc->num_blocks || seen[(size_t)b]) {
@@ -104,12 +169,11 @@ int pa_pool_create(const pa_pool_desc *desc, pa_pool **out) {
                             b);
             }
             seen[(size_t)b] = 1;
-            p->ring[(size_t)i] = b;
+            p->queue_push_tail(b);
         }
     } else {
-        for (int32_t i = 0; i < desc->num_blocks; ++i) p->ring[(size_t)i] = i;
+        for (int32_t i = 0; i < desc->num_blocks; ++i) p->queue_push_tail(i);
     }
-    p->count = desc->num_blocks;
     *out = p;
     return PA_OK;
 }
@@ -137,6 +201,81 @@ int pa_seq_add(pa_pool *pool, int32_t seq_id, int32_t n_tokens, int64_t *slots_o
         for (int32_t p = 0; p < n_tokens; ++p)
             slots_out[p] = (int64_t)s.table[(size_t)(p / B)] * B + p % B;
     pool->seqs.emplace(seq_id, std::move(s));
+    return PA_OK;
+}
+
+int pa_seq_add_tokens(pa_pool *pool, int32_t seq_id, int32_t n_tokens, const int32_t *token_ids,
+                      int64_t extra_key, int64_t *slots_out, int32_t *n_cached_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_add_tokens: NULL pool");
+    if (n_tokens < 0 || (n_tokens > 0 && !token_ids))
+        return fail(PA_ERR_INVALID_ARG, "pa_seq_add_tokens: bad arguments");
+    if (pool->seqs.count(seq_id))
+        return fail(PA_ERR_NO_SEQ, "pa_seq_add_tokens: sequence %d already exists", seq_id);
+    const int32_t B = pool->block_size;
+    const int32_t total = (int32_t)(((int64_t)n_tokens + B - 1) / B);
+    const int32_t full = n_tokens / B;
+    // 1. the longest run of leading full blocks already in the cache
+    std::vector<int32_t> hit;
+    std::vector<uint64_t> keys((size_t)full);
+    uint64_t parent = kRootKey;
+    bool chain = pool->caching;
+    for (int32_t j = 0; j < full; ++j) {
+        const int32_t *tok = token_ids + (int64_t)j * B;
+        keys[(size_t)j] = block_key(parent, tok, B, extra_key);
+        if (chain) {
+            auto it = pool->cache.find(keys[(size_t)j]);
+            const int32_t b = it == pool->cache.end() ? -1 : it->second;
+            if (b >= 0 && pool->cached[(size_t)b] && pool->parent_key[(size_t)b] == parent &&
+                pool->extra[(size_t)b] == extra_key &&
+                std::memcmp(&pool->tokens[(size_t)b * B], tok, sizeof(int32_t) * B) == 0)
+                hit.push_back(b);
+            else
+                chain = false;
+        }
+        parent = keys[(size_t)j];
+    }
+    // 2. room for the rest: hits that sit in the free queue leave it
+    int64_t hits_free = 0;
+    for (int32_t b : hit) hits_free += pool->ref[(size_t)b] == 0;
+    const int64_t need = total - (int64_t)hit.size();
+    if (need > pool->count - hits_free)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "pa_seq_add_tokens: need %lld new blocks, %lld free",
+                    (long long)need, (long long)(pool->count - hits_free));
+    // 3. touch the hits, take new blocks, register the new full blocks
+    Seq s;
+    s.table.reserve((size_t)total);
+    for (int32_t b : hit) {
+        if (pool->ref[(size_t)b] == 0) pool->queue_remove(b);
+        ++pool->ref[(size_t)b];
+        s.table.push_back(b);
+    }
+    for (int64_t i = 0; i < need; ++i) s.table.push_back(pool->pop_free());
+    if (pool->caching) {
+        for (int32_t j = (int32_t)hit.size(); j < full; ++j) {
+            const int32_t b = s.table[(size_t)j];
+            const uint64_t k = keys[(size_t)j];
+            if (pool->cache.count(k)) continue;   // a different block holds this key
+            pool->cache.emplace(k, b);
+            pool->cached[(size_t)b] = 1;
+            pool->key[(size_t)b] = k;
+            pool->parent_key[(size_t)b] = j ? keys[(size_t)j - 1] : kRootKey;
+            pool->extra[(size_t)b] = extra_key;
+            std::memcpy(&pool->tokens[(size_t)b * B], token_ids + (int64_t)j * B,
+                        sizeof(int32_t) * B);
+        }
+    }
+    s.num_tokens = n_tokens;
+    if (slots_out)
+        for (int32_t p = 0; p < n_tokens; ++p)
+            slots_out[p] = (int64_t)s.table[(size_t)(p / B)] * B + p % B;
+    if (n_cached_out) *n_cached_out = (int32_t)hit.size() * B;
+    pool->seqs.emplace(seq_id, std::move(s));
+    return PA_OK;
+}
+
+int pa_pool_cached_blocks(const pa_pool *pool, int32_t *n_cached) {
+    if (!pool || !n_cached) return fail(PA_ERR_INVALID_ARG, "pa_pool_cached_blocks: NULL argument");
+    *n_cached = (int32_t)pool->cache.size();
     return PA_OK;
 }
 
@@ -278,8 +417,8 @@ int pa_pool_free_queue(const pa_pool *pool, int32_t *out, int32_t cap, int32_t *
     if (pool->count > cap)
         return fail(PA_ERR_INVALID_ARG, "pa_pool_free_queue: cap %d < queue length %lld", cap,
                     (long long)pool->count);
-    for (int64_t i = 0; i < pool->count; ++i)
-        out[i] = pool->ring[(size_t)((pool->head + i) % pool->num_blocks)];
+    int64_t i = 0;
+    for (int32_t b = pool->head; b >= 0; b = pool->nxt[(size_t)b]) out[i++] = b;
     return PA_OK;
 }
 

@@ -286,3 +286,60 @@ def test_full_40_layer_pool_filling_step_sampled(beam):
         ref = oa.paged_attention(q[l][rows], okc[l], ovc[l], tables[rows], ctx[rows], w.scale)
         assert _err(outs[l].cpu().numpy()[rows], ref) <= TOL, l
     pk.pa_pool_destroy(pool)
+
+
+def test_prefix_cached_prompts_write_only_their_tails():
+    """Requests sharing system prompts through the prefix cache: each writes
+    the K/V of its uncached tail only, yet attends over its whole prompt."""
+    H, D, B, NB = 4, 128, 16, 96
+    rng = np.random.default_rng(41)
+    vocab = 50
+    systems = [list(rng.integers(0, vocab, n)) for n in (64, 40, 200)]
+    reqs = [(systems[i % 3] + list(rng.integers(0, vocab, int(rng.integers(1, 60)))), i % 2)
+            for i in range(9)]
+    desc = pk.PoolDesc(NB, B, num_heads=H, head_dim=D, flags=pk.PA_POOL_PREFIX_CACHING)
+    pool = pk.pa_pool_create(desc)
+    m = BlockManager(NB, B, prefix_caching=True)
+    kc = torch.zeros((NB, H, B, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    okc, ovc = np.zeros((NB, H, B, D), np.float16), np.zeros((NB, H, B, D), np.float16)
+    # the K/V of a token depend only on its prefix: derive them from a per-prefix seed
+    def kv_of(toks, extra):
+        r = np.random.default_rng(abs(hash((extra, tuple(toks)))) % (2**32))
+        return wl.normal_f16(r, (2, H, D))
+    written = 0
+    for s, (toks, extra) in enumerate(reqs):
+        slots_g, n_cached = pk.pa_seq_add_tokens(pool, s, toks, extra)
+        slots_o, n_cached_o = m.add_tokens(s, toks, extra)
+        assert slots_g.tolist() == slots_o and n_cached == n_cached_o
+        tail = range(n_cached, len(toks))
+        kv = np.stack([kv_of(toks[:p + 1], extra) for p in tail]) if len(tail) else \
+            np.zeros((0, 2, H, D), np.float16)
+        k, v = np.ascontiguousarray(kv[:, 0]), np.ascontiguousarray(kv[:, 1])
+        sl = np.array(slots_o[n_cached:], np.int64)
+        if len(sl):
+            pk.pa_write_kv(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                           torch.from_numpy(sl).cuda(), kc, vc, desc)
+            oc.write_kv(okc, ovc, k, v, sl)
+        written += len(sl)
+    assert written < sum(len(t) for t, _ in reqs)          # the cache saved writes
+    ids = list(range(len(reqs)))
+    mb = max(len(m.block_table(s)) for s in ids)
+    tables = np.array(m.padded_tables(ids, mb), np.int32)
+    ctx = np.array([len(t) for t, _ in reqs], np.int32)
+    q = wl.normal_f16(rng, (len(ids), H, D))
+    out = torch.empty((len(ids), H, D), dtype=torch.float16, device="cuda")
+    ws = torch.empty(pk.pa_decode_workspace_bytes(len(ids), mb, desc), dtype=torch.uint8,
+                     device="cuda")
+    pk.pa_decode_attention(out, torch.from_numpy(q).cuda(), kc, vc, torch.from_numpy(tables).cuda(),
+                           torch.from_numpy(ctx).cuda(), 0.088, desc, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(kc.cpu(), torch.from_numpy(okc))
+    # every request reads the K/V its own full prompt defines, shared blocks included
+    for s, (toks, extra) in enumerate(reqs):
+        for p in range(len(toks)):
+            kv = kv_of(toks[:p + 1], extra)
+            blk = m.block_table(s)[p // B]
+            assert np.array_equal(okc[blk, :, p % B], kv[0])
+    ref = oa.paged_attention(q, okc, ovc, tables, ctx, 0.088)
+    assert _err(out.cpu().numpy(), ref) <= TOL
