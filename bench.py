@@ -274,6 +274,7 @@ def run_ours(args):
     attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
     write_ms = [e[2].elapsed_time(e[0]) for e in evs]
     copy_stats = time_copy_blocks(pk, pool, desc, w, kc, vc, stream) if rank == 0 else None
+    swap_stats = time_swap_blocks(pk, desc, w, kc, vc, stream) if rank == 0 else None
     assert runner.status.item() == 0, f"device status {runner.status.item()}"
 
     # ---- e2e: host buffers, H2D of q/k/v and D2H of o inside every step
@@ -362,6 +363,7 @@ def run_ours(args):
                     "note": "new K/V of the batch read and scattered to their slots (timed in the step loop)",
                 },
                 "pa_copy_blocks": copy_stats,
+                "pa_swap_blocks": swap_stats,
                 "host_block_manager": {
                     "us_per_step": 1e6 * sum(host_s) / len(host_s),
                     "note": "host wall clock per step: free/admit finished sequences, pa_alloc_slots "
@@ -526,6 +528,40 @@ def run_full40(args):
         "clocks": clocks,
     }), flush=True)
     pk.pa_pool_destroy(pool)
+
+
+def time_swap_blocks(pk, desc, w, kc, vc, stream, n_pairs=256, reps=20):
+    """Swap-sized batches of block copies between the GPU cache and swap space
+    in pinned host memory (over NVLink-C2C), each direction, one launch each."""
+    import torch
+
+    hk = torch.empty((n_pairs, w.num_heads, w.block_size, w.head_dim), dtype=torch.float16,
+                     pin_memory=True)
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(6)
+    src = rng.choice(w.num_blocks, n_pairs, replace=False)
+    out_pairs = torch.from_numpy(np.stack([src, np.arange(n_pairs)], 1).astype(np.int32)).to(kc.device)
+    in_pairs = torch.from_numpy(np.stack([np.arange(n_pairs), src], 1).astype(np.int32)).to(kc.device)
+    status = torch.zeros(1, dtype=torch.int32, device=kc.device)
+    res = {}
+    for name, args in (("gpu_to_host", ([kc], [vc], w.num_blocks, [hk], [hv], n_pairs, out_pairs)),
+                       ("host_to_gpu", ([hk], [hv], n_pairs, [kc], [vc], w.num_blocks, in_pairs))):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                pk.pa_swap_blocks(*args, desc, status=status, stream=stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                pk.pa_swap_blocks(*args, desc, status=status, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / reps
+        moved = n_pairs * 2 * w.num_heads * w.block_size * w.head_dim * 2
+        res[name] = {"us_per_launch": us, "bytes_moved": moved, "GB/s": moved / (us / 1e6) / 1e9}
+    assert status.item() == 0
+    res["pairs"] = n_pairs
+    res["note"] = "pa_swap_blocks: K and V of 256 blocks, one layer, one launch per direction"
+    return res
 
 
 def _oracle_sample(n_seqs):

@@ -184,6 +184,26 @@ int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
                    int64_t *slot_mapping_out, int32_t *copies_out, int32_t copies_cap,
                    int32_t *n_copies_out);
 
+/* Swapping ([review] §4.5 (1) swapping; [notes] §3.5 Swapping, CPU block
+ * manager): a preempted group of sequences moves, all its blocks at once,
+ * from the GPU pool to a second pool that manages swap space in host memory,
+ * and later back (pa_swap_out from gpu to cpu, pa_swap_in from cpu to gpu;
+ * the two pools must have the same block size).  The group must hold every
+ * reference to its blocks ([review] §4.5 (2): sequences that share blocks
+ * are evicted together); each distinct block gets one block of the target
+ * pool (with the same reference count), the sequences' tables are rewritten
+ * to the new ids, and the source blocks return to their free queue, the
+ * last-used first.  pairs_out (host, pairs_cap x 2 int32) receives the
+ * (source block, target block) pairs in first-use order -- the copies that
+ * pa_swap_blocks must perform.  All-or-nothing.
+ * Errors: PA_ERR_NO_SEQ, PA_ERR_OUT_OF_BLOCKS (target pool full),
+ * PA_ERR_INVALID_ARG (a block shared outside the group, small pairs_cap,
+ * different block sizes). */
+int pa_swap_out(pa_pool *gpu, pa_pool *cpu, int32_t n_seqs, const int32_t *seq_ids,
+                int32_t *pairs_out, int32_t pairs_cap, int32_t *n_pairs_out);
+int pa_swap_in(pa_pool *cpu, pa_pool *gpu, int32_t n_seqs, const int32_t *seq_ids,
+               int32_t *pairs_out, int32_t pairs_cap, int32_t *n_pairs_out);
+
 /* Export block tables and context lengths for a batch, in the layout the
  * attention kernel reads: tables_out (host, n_seqs x max_blocks int32,
  * row-major) gets each sequence's physical block ids, padded with -1;
@@ -232,6 +252,20 @@ int pa_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32
 int pa_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_layers,
                    const int32_t *pairs, int32_t n_pairs, const pa_pool_desc *desc,
                    int32_t *status, void *stream);
+
+/* Block copies between two cache sets (swap out / swap in, [review] §5.1 (3)
+ * fused block copy): for every pair (a, b) in pairs (device-accessible,
+ * n_pairs x 2 int32) and every layer, block b of dst_k[l] / dst_v[l] becomes
+ * a copy of block a of src_k[l] / src_v[l], in one launch.  The caches are
+ * device memory or page-locked host memory mapped into the device's address
+ * space (e.g. swap space in Grace memory, reached over NVLink-C2C); src and
+ * dst hold src_num_blocks / dst_num_blocks blocks of the layout above.
+ * Pairs outside either pool are skipped and reported as PA_ERR_BAD_BLOCK.
+ * num_layers <= 128.  Errors: PA_ERR_INVALID_ARG, PA_ERR_CUDA. */
+int pa_swap_blocks(const void *const *src_k, const void *const *src_v, int32_t src_num_blocks,
+                   void *const *dst_k, void *const *dst_v, int32_t dst_num_blocks,
+                   int32_t num_layers, const int32_t *pairs, int32_t n_pairs,
+                   const pa_pool_desc *desc, int32_t *status, void *stream);
 
 /* Bytes of device workspace pa_decode_attention needs for a batch of n_seqs
  * sequences whose tables have max_blocks columns: 256 bytes of scheduling

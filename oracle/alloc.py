@@ -48,6 +48,13 @@ Sources, in the order the steps are taken:
   out again, least recently freed first.  Here the key is the exact token
   prefix plus the extra key, so no hash is involved.
 
+* Swapping (review §4.5 (1), notes §3.5): a preempted sequence group moves
+  all its blocks to a second pool standing for swap space in host memory, and
+  back later; sequences sharing blocks move together (review §4.5 (2)).
+  ``move_group`` below gives each distinct block of the group a block of the
+  target pool (same reference count), rewrites the tables and returns the
+  source blocks to their free queue, last-used first.
+
 Readings where the pages are silent (stated, not found on the pages): the
 queue is FIFO; a multi-sequence ``alloc_slots`` handles the sequences in the
 order given and is all-or-nothing as a whole; a sequence may appear only once
@@ -252,3 +259,43 @@ class BlockManager:
     def snapshot(self):
         return copy.deepcopy((list(self.free_queue), list(self.ref), self.tables,
                               sorted(self.block_key.items())))
+
+
+def move_group(src: BlockManager, dst: BlockManager, seq_ids):
+    """Swap a sequence group from ``src`` to ``dst``; returns the
+    (source block, target block) pairs to copy, in first-use order.
+
+    Raises KeyError (unknown sequence), ValueError (block shared outside
+    the group, sequence already in ``dst``, block sizes differ) or OutOfBlocks;
+    nothing changes on failure."""
+    seq_ids = [int(s) for s in seq_ids]
+    if src.B != dst.B or len(set(seq_ids)) != len(seq_ids):
+        raise ValueError("bad group")
+    uses, blocks = {}, []
+    for s in seq_ids:
+        if s not in src.tables:
+            raise KeyError(s)
+        if s in dst.tables:
+            raise ValueError("sequence already in the target pool")
+        for b in src.block_table(s):
+            if b not in uses:
+                uses[b] = 0
+                blocks.append(b)
+            uses[b] += 1
+    if any(src.ref[b] != uses[b] for b in blocks):
+        raise ValueError("a block is shared outside the group")
+    if len(blocks) > len(dst.free_queue):
+        raise OutOfBlocks()
+    moved, pairs = {}, []
+    for b in blocks:
+        nb = dst._take_block()
+        dst.ref[nb] = uses[b]
+        moved[b] = nb
+        pairs.append((b, nb))
+    for s in seq_ids:
+        dst.tables[s] = [[moved[b], f] for b, f in src.tables.pop(s)]
+    for b in reversed(blocks):
+        src.ref[b] = 0
+        src.free_queue.append(b)
+    return pairs
+

@@ -47,3 +47,11 @@ def copy_blocks(k_caches, v_caches, pairs) -> None:
         for cache in list(k_caches) + list(v_caches):
             cache[int(dst)] = cache[int(src)]
 
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, pairs) -> None:
+    """In-place: for each (a, b) and each layer, dst block b <- src block a
+    (swap out / swap in between two cache sets)."""
+    for a, b in pairs:
+        for s, d in list(zip(src_k, dst_k)) + list(zip(src_v, dst_v)):
+            d[int(b)] = s[int(a)]
+

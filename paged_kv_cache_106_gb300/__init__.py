@@ -75,6 +75,9 @@ def _load():
         "pa_seq_add": (i32, [vp, i32, i32, vp]),
         "pa_seq_add_tokens": (i32, [vp, i32, i32, vp, i64, vp, P(i32)]),
         "pa_pool_cached_blocks": (i32, [vp, P(i32)]),
+        "pa_swap_out": (i32, [vp, vp, i32, vp, vp, i32, P(i32)]),
+        "pa_swap_in": (i32, [vp, vp, i32, vp, vp, i32, P(i32)]),
+        "pa_swap_blocks": (i32, [vp, vp, i32, vp, vp, i32, i32, vp, i32, P(pa_pool_desc), vp, vp]),
         "pa_seq_fork": (i32, [vp, i32, i32]),
         "pa_seq_free": (i32, [vp, i32]),
         "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
@@ -128,6 +131,17 @@ def _dev(x):
         raise ValueError("expected a CUDA tensor")
     if not x.is_contiguous():
         raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def _addr(x):
+    """Device-reachable address of a CUDA tensor or of a pinned host tensor."""
+    if x is None or isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if not (x.is_cuda or x.is_pinned()):
+        raise ValueError("expected a CUDA tensor or a pinned host tensor")
     return x.data_ptr()
 
 
@@ -193,6 +207,39 @@ def pa_pool_cached_blocks(pool) -> int:
     n = ctypes.c_int32()
     _check(_lib.pa_pool_cached_blocks(pool, ctypes.byref(n)))
     return n.value
+
+
+def _group_move(fn, src_pool, dst_pool, seq_ids):
+    ids = _host_i32(seq_ids)
+    cap = 0
+    # room for every distinct block: at most the sum of the tables' lengths
+    for s in ids.tolist():
+        cap += pa_seq_info(src_pool, s)[1]
+    pairs = np.empty((max(cap, 1), 2), np.int32)
+    n = ctypes.c_int32(0)
+    _check(fn(src_pool, dst_pool, ids.shape[0], ids.ctypes.data, pairs.ctypes.data, cap,
+              ctypes.byref(n)))
+    return pairs[: n.value]
+
+
+def pa_swap_out(gpu_pool, cpu_pool, seq_ids):
+    """Move a sequence group to the CPU pool; returns the (gpu, cpu) block pairs."""
+    return _group_move(_lib.pa_swap_out, gpu_pool, cpu_pool, seq_ids)
+
+
+def pa_swap_in(cpu_pool, gpu_pool, seq_ids):
+    """Move a sequence group back to the GPU pool; returns the (cpu, gpu) block pairs."""
+    return _group_move(_lib.pa_swap_in, cpu_pool, gpu_pool, seq_ids)
+
+
+def pa_swap_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks, pairs,
+                   desc: PoolDesc, status=None, stream=None, n_pairs: int | None = None) -> None:
+    L = len(src_k)
+    arr = lambda xs: (ctypes.c_void_p * L)(*[_addr(x) for x in xs])
+    n = int(pairs.shape[0]) if n_pairs is None else int(n_pairs)
+    _check(_lib.pa_swap_blocks(arr(src_k), arr(src_v), int(src_num_blocks), arr(dst_k),
+                               arr(dst_v), int(dst_num_blocks), L, _addr(pairs), n, desc.ref,
+                               _dev(status), _stream(stream)))
 
 
 def pa_seq_fork(pool, parent: int, child: int) -> None:

@@ -79,6 +79,14 @@ int pa_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_lay
                               stream);
 }
 
+int pa_swap_blocks(const void *const *src_k, const void *const *src_v, int32_t src_num_blocks,
+                   void *const *dst_k, void *const *dst_v, int32_t dst_num_blocks,
+                   int32_t num_layers, const int32_t *pairs, int32_t n_pairs,
+                   const pa_pool_desc *desc, int32_t *status, void *stream) {
+    return launch_swap_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks,
+                              num_layers, pairs, n_pairs, desc, status, stream);
+}
+
 size_t pa_decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_pool_desc *desc) {
     return decode_workspace_bytes(n_seqs, max_blocks, desc);
 }

@@ -28,6 +28,10 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slot_mapping, i
 int launch_copy_blocks(void *const *k_caches, void *const *v_caches, int32_t num_layers,
                        const int32_t *pairs, int32_t n_pairs, const pa_pool_desc *d,
                        int32_t *status, void *stream);
+int launch_swap_blocks(const void *const *src_k, const void *const *src_v, int32_t src_blocks,
+                       void *const *dst_k, void *const *dst_v, int32_t dst_blocks,
+                       int32_t num_layers, const int32_t *pairs, int32_t n_pairs,
+                       const pa_pool_desc *d, int32_t *status, void *stream);
 size_t decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_pool_desc *d);
 int launch_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,

@@ -279,6 +279,75 @@ int pa_pool_cached_blocks(const pa_pool *pool, int32_t *n_cached) {
     return PA_OK;
 }
 
+// Move a group of sequences from pool `from` to pool `to` (swapping).
+static int move_group(const char *who, pa_pool *from, pa_pool *to, int32_t n_seqs,
+                      const int32_t *seq_ids, int32_t *pairs_out, int32_t pairs_cap,
+                      int32_t *n_pairs_out) {
+    if (!from || !to || from == to || n_seqs < 0 || (n_seqs > 0 && !seq_ids) || pairs_cap < 0 ||
+        (pairs_cap > 0 && !pairs_out))
+        return fail(PA_ERR_INVALID_ARG, "%s: bad arguments", who);
+    if (from->block_size != to->block_size)
+        return fail(PA_ERR_INVALID_ARG, "%s: the pools' block sizes differ", who);
+    // blocks of the group in first-use order, with their reference counts
+    std::unordered_set<int32_t> ids;
+    std::unordered_map<int32_t, int32_t> uses;   // block -> references from the group
+    std::vector<int32_t> blocks;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        auto it = from->seqs.find(seq_ids[i]);
+        if (it == from->seqs.end())
+            return fail(PA_ERR_NO_SEQ, "%s: no sequence %d", who, seq_ids[i]);
+        if (!ids.insert(seq_ids[i]).second)
+            return fail(PA_ERR_INVALID_ARG, "%s: sequence %d listed twice", who, seq_ids[i]);
+        if (to->seqs.count(seq_ids[i]))
+            return fail(PA_ERR_NO_SEQ, "%s: sequence %d already in the target pool", who,
+                        seq_ids[i]);
+        for (int32_t b : it->second.table)
+            if (uses[b]++ == 0) blocks.push_back(b);
+    }
+    for (int32_t b : blocks)
+        if (from->ref[(size_t)b] != uses[b])
+            return fail(PA_ERR_INVALID_ARG,
+                        "%s: block %d is shared with a sequence outside the group", who, b);
+    if ((int64_t)blocks.size() > to->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "%s: need %zu blocks, %lld free", who, blocks.size(),
+                    (long long)to->count);
+    if ((int64_t)blocks.size() > pairs_cap)
+        return fail(PA_ERR_INVALID_ARG, "%s: %zu copies, pairs_cap is %d", who, blocks.size(),
+                    pairs_cap);
+    std::unordered_map<int32_t, int32_t> moved;
+    for (size_t k = 0; k < blocks.size(); ++k) {
+        const int32_t b = blocks[k], nb = to->pop_free();
+        to->ref[(size_t)nb] = uses[b];
+        moved[b] = nb;
+        pairs_out[2 * k] = b;
+        pairs_out[2 * k + 1] = nb;
+    }
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        auto it = from->seqs.find(seq_ids[i]);
+        Seq s = std::move(it->second);
+        from->seqs.erase(it);
+        for (int32_t &b : s.table) b = moved[b];
+        to->seqs.emplace(seq_ids[i], std::move(s));
+    }
+    // the source blocks go back to their free queue, last-used first
+    for (size_t k = blocks.size(); k-- > 0;) {
+        from->ref[(size_t)blocks[k]] = 0;
+        from->queue_push_tail(blocks[k]);
+    }
+    if (n_pairs_out) *n_pairs_out = (int32_t)blocks.size();
+    return PA_OK;
+}
+
+int pa_swap_out(pa_pool *gpu, pa_pool *cpu, int32_t n_seqs, const int32_t *seq_ids,
+                int32_t *pairs_out, int32_t pairs_cap, int32_t *n_pairs_out) {
+    return move_group("pa_swap_out", gpu, cpu, n_seqs, seq_ids, pairs_out, pairs_cap, n_pairs_out);
+}
+
+int pa_swap_in(pa_pool *cpu, pa_pool *gpu, int32_t n_seqs, const int32_t *seq_ids,
+               int32_t *pairs_out, int32_t pairs_cap, int32_t *n_pairs_out) {
+    return move_group("pa_swap_in", cpu, gpu, n_seqs, seq_ids, pairs_out, pairs_cap, n_pairs_out);
+}
+
 int pa_seq_fork(pa_pool *pool, int32_t parent, int32_t child) {
     if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_fork: NULL pool");
     auto it = pool->seqs.find(parent);
