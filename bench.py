@@ -564,6 +564,98 @@ def time_swap_blocks(pk, desc, w, kc, vc, stream, n_pairs=256, reps=20):
     return res
 
 
+def run_beam_churn(args):
+    """Beam-search churn: 64 requests x 4 beams (OPT-13B layer shapes), every
+    step = prune (fork repeated survivors, free the rest), host block
+    manager, copy-on-write copies, slot write, decode attention."""
+    import torch
+
+    import paged_kv_cache_106_gb300 as pk
+    from paged_kv_cache_106_gb300 import workloads as wl
+    from paged_kv_cache_106_gb300.step import BeamGroups, DecodeStepRunner
+
+    _, _, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    churn = wl.beam_churn(groups=64, width=4)
+    H, D, B = wl.OPT13B_HEADS, wl.OPT13B_HEAD_DIM, wl.DEFAULT_BLOCK
+    total = args.warmup + args.steps
+    nb = sum(-(-n // B) for n in churn.prompt_lens) * churn.width \
+        + churn.groups * churn.width * (total // B + 4)
+    order = np.random.default_rng(churn.seed).permutation(nb)
+    desc = pk.PoolDesc(nb, B, num_heads=H, head_dim=D, free_order=order)
+    pool = pk.pa_pool_create(desc)
+    bg = BeamGroups(pool, churn)
+    S = len(bg.ids())
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(churn.seed)
+    kc = torch.empty((nb, H, B, D), dtype=torch.float16, device=dev).normal_(generator=gen)
+    vc = torch.empty_like(kc).normal_(generator=gen)
+    q = torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+    k_new, v_new, out = torch.randn_like(q), torch.randn_like(q), torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    mb = -(-(max(churn.prompt_lens) + total) // B) + 1
+    runner = DecodeStepRunner(pool, desc, bg.ids(), mb, device=dev, stream=stream)
+    rng = np.random.default_rng(churn.seed + 1)
+    # the seeded survivor draws are inputs: drawn before any timing
+    draws = iter([churn.survivors(rng) for _ in range(total)])
+    host, stats = [], {"copies": 0, "forks": 0, "frees": 0, "tokens": 0, "bytes": 0}
+
+    split = {"prepare_wait": 0.0, "block_manager": 0.0, "launches": 0.0, "prune": 0.0}
+
+    def step(record):
+        h0 = time.perf_counter()
+        runner.ids = np.array(bg.ids(), np.int32)
+        runner.prepare()
+        h1 = time.perf_counter()
+        ctx = runner.ctx_host.astype(np.int64)
+        runner.copy_blocks([kc], [vc])
+        runner.write_kv(k_new, v_new, kc, vc)
+        runner.attention(out, q, kc, vc, 1 / math.sqrt(D))
+        h2 = time.perf_counter()
+        f, fr = bg.prune(next(draws))
+        h3 = time.perf_counter()
+        if record:
+            host.append(h3 - h0 - (h1 - h0 - runner.host_seconds))
+            split["prepare_wait"] += h1 - h0 - runner.host_seconds
+            split["block_manager"] += runner.host_seconds
+            split["launches"] += h2 - h1
+            split["prune"] += h3 - h2
+            stats["copies"] += runner.n_copies
+            stats["forks"] += f
+            stats["frees"] += fr
+            stats["tokens"] += int(ctx.sum())
+            stats["bytes"] += int(ctx.sum()) * H * D * 4 + S * H * D * 4
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(False)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    assert runner.status.item() == 0
+    el = t0.elapsed_time(t1) / 1e3
+    print(json.dumps({
+        "metric": METRIC, "value": stats["tokens"] / el, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "data": "synthetic",
+        "config": {"workload": "beam-search churn, 64 requests x 4 beams, OPT-13B layer 40x128, "
+                               "block 16, prune + fork every step", "pool_blocks": nb},
+        "per_step": {k: stats[k] / args.steps for k in ("copies", "forks", "frees")},
+        "host_us_per_step": 1e6 * sum(host) / len(host),
+        "host_split_us_per_step": {k: 1e6 * v / args.steps for k, v in split.items()},
+        "logical_attention_GB/s": stats["bytes"] / el / 1e9,
+        "note": "logical bytes count shared blocks once per beam; host time = pruning + "
+                "block manager + Python launch path (the wait on the GPU excluded)",
+    }), flush=True)
+    pk.pa_pool_destroy(pool)
+
+
 def _oracle_sample(n_seqs):
     """Host data for the first n_seqs sequences of the same workload, laid
     out by the oracle's own block manager."""
@@ -649,8 +741,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)
-    ap.add_argument("--workload", choices=["mixed_b256", "full_40l"], default="mixed_b256",
-                    help="mixed_b256: the headline workload; full_40l: 40-layer pool-filling step")
+    ap.add_argument("--workload", choices=["mixed_b256", "full_40l", "beam_churn"],
+                    default="mixed_b256",
+                    help="mixed_b256: the headline workload; full_40l: 40-layer pool-filling "
+                         "step; beam_churn: beam search with pruning")
     ap.add_argument("--beam", action="store_true", help="full_40l: beam groups sharing blocks")
     ap.add_argument("--dump-steps", default="",
                     help="write each warm-up and timed step's algorithmic attention bytes here")
@@ -663,6 +757,8 @@ def main():
         run_reference(args)
     elif args.workload == "full_40l":
         run_full40(args)
+    elif args.workload == "beam_churn":
+        run_beam_churn(args)
     else:
         run_ours(args)
 

@@ -164,6 +164,15 @@ int pa_seq_fork(pa_pool *pool, int32_t parent, int32_t child);
  * Errors: PA_ERR_NO_SEQ. */
 int pa_seq_free(pa_pool *pool, int32_t seq_id);
 
+/* Batched fork and free for beam search ([notes] §3.4.2: beams fork at
+ * every step and pruned beams release their blocks): the same operations as
+ * pa_seq_fork / pa_seq_free, applied in order; pa_seq_fork_batch's parents
+ * may be children created earlier in the same call.  Every argument is
+ * checked before anything changes.  Errors: PA_ERR_NO_SEQ,
+ * PA_ERR_INVALID_ARG. */
+int pa_seq_fork_batch(pa_pool *pool, int32_t n, const int32_t *parents, const int32_t *children);
+int pa_seq_free_batch(pa_pool *pool, int32_t n, const int32_t *seq_ids);
+
 /* append, for a batch: one new token for each of seq_ids[0..n_seqs), handled
  * in the order given ([review] §4.3 steps 1-2; [tutorial] Fig. 3, Fig. 6):
  *   - no block yet, or the last block is full (shared or not): take a new

@@ -79,6 +79,8 @@ def _load():
         "pa_swap_in": (i32, [vp, vp, i32, vp, vp, i32, P(i32)]),
         "pa_swap_blocks": (i32, [vp, vp, i32, vp, vp, i32, i32, vp, i32, P(pa_pool_desc), vp, vp]),
         "pa_seq_fork": (i32, [vp, i32, i32]),
+        "pa_seq_fork_batch": (i32, [vp, i32, vp, vp]),
+        "pa_seq_free_batch": (i32, [vp, i32, vp]),
         "pa_seq_free": (i32, [vp, i32]),
         "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
         "pa_get_block_tables": (i32, [vp, i32, vp, i32, vp, vp]),
@@ -244,6 +246,18 @@ def pa_swap_blocks(src_k, src_v, src_num_blocks, dst_k, dst_v, dst_num_blocks, p
 
 def pa_seq_fork(pool, parent: int, child: int) -> None:
     _check(_lib.pa_seq_fork(pool, int(parent), int(child)))
+
+
+def pa_seq_fork_batch(pool, parents, children) -> None:
+    p, c = _host_i32(parents), _host_i32(children)
+    if p.shape != c.shape:
+        raise ValueError("parents and children differ in length")
+    _check(_lib.pa_seq_fork_batch(pool, p.shape[0], p.ctypes.data, c.ctypes.data))
+
+
+def pa_seq_free_batch(pool, seq_ids) -> None:
+    ids = _host_i32(seq_ids)
+    _check(_lib.pa_seq_free_batch(pool, ids.shape[0], ids.ctypes.data))
 
 
 def pa_seq_free(pool, seq_id: int) -> None:

@@ -360,6 +360,36 @@ int pa_seq_fork(pa_pool *pool, int32_t parent, int32_t child) {
     return PA_OK;
 }
 
+int pa_seq_fork_batch(pa_pool *pool, int32_t n, const int32_t *parents, const int32_t *children) {
+    if (!pool || n < 0 || (n > 0 && (!parents || !children)))
+        return fail(PA_ERR_INVALID_ARG, "pa_seq_fork_batch: bad arguments");
+    std::unordered_set<int32_t> born;
+    for (int32_t i = 0; i < n; ++i) {
+        if (!pool->seqs.count(parents[i]) && !born.count(parents[i]))
+            return fail(PA_ERR_NO_SEQ, "pa_seq_fork_batch: no sequence %d", parents[i]);
+        if (pool->seqs.count(children[i]) || !born.insert(children[i]).second)
+            return fail(PA_ERR_NO_SEQ, "pa_seq_fork_batch: sequence %d already exists",
+                        children[i]);
+    }
+    for (int32_t i = 0; i < n; ++i) pa_seq_fork(pool, parents[i], children[i]);
+    return PA_OK;
+}
+
+int pa_seq_free_batch(pa_pool *pool, int32_t n, const int32_t *seq_ids) {
+    if (!pool || n < 0 || (n > 0 && !seq_ids))
+        return fail(PA_ERR_INVALID_ARG, "pa_seq_free_batch: bad arguments");
+    std::unordered_set<int32_t> seen;
+    for (int32_t i = 0; i < n; ++i) {
+        if (!pool->seqs.count(seq_ids[i]))
+            return fail(PA_ERR_NO_SEQ, "pa_seq_free_batch: no sequence %d", seq_ids[i]);
+        if (!seen.insert(seq_ids[i]).second)
+            return fail(PA_ERR_INVALID_ARG, "pa_seq_free_batch: sequence %d listed twice",
+                        seq_ids[i]);
+    }
+    for (int32_t i = 0; i < n; ++i) pa_seq_free(pool, seq_ids[i]);
+    return PA_OK;
+}
+
 int pa_seq_free(pa_pool *pool, int32_t seq_id) {
     if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_seq_free: NULL pool");
     auto it = pool->seqs.find(seq_id);

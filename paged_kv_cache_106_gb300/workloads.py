@@ -237,3 +237,34 @@ CONFIGS = {
 def value_rng(workload: DecodeWorkload, stream: int = 0) -> np.random.Generator:
     """Generator for the workload's tensor values (independent of its structure draws)."""
     return _rng(workload.seed * 1000 + 17 + stream)
+
+
+@dataclass
+class BeamChurn:
+    """Seeded beam-search churn: ``groups`` requests decode with ``width``
+    beams each; after every step each group keeps ``width`` survivors drawn
+    (with replacement) from its beams, so a beam drawn m times is kept and
+    forked m-1 times and a beam not drawn is freed (PagedAttention notes,
+    unpurerationalist.github.io, §3.4.2: beams share ancestor blocks, a
+    pruned beam drops its references; vLLM paper review,
+    mz-moonzoo.tistory.com/116, §4.4 (2)).  The draws are this generator's;
+    applying them to a block manager is the caller's."""
+
+    groups: int
+    width: int
+    prompt_lens: list
+    seed: int
+
+    def survivors(self, rng: np.random.Generator):
+        """Per group, the beam indices (0..width-1) kept, with repeats."""
+        # beam 0 is likelier: beams of a request tend to collapse onto a few
+        p = np.array([2.0] + [1.0] * (self.width - 1))
+        return [sorted(rng.choice(self.width, size=self.width, p=p / p.sum()).tolist())
+                for _ in range(self.groups)]
+
+
+def beam_churn(groups: int = 32, width: int = 4, seed: int = 111) -> BeamChurn:
+    rng = _rng(seed)
+    return BeamChurn(groups=groups, width=width,
+                     prompt_lens=[int(x) for x in _lognormal_lengths(rng, groups, 160, 1024)],
+                     seed=seed)

@@ -343,3 +343,62 @@ def test_prefix_cached_prompts_write_only_their_tails():
             assert np.array_equal(okc[blk, :, p % B], kv[0])
     ref = oa.paged_attention(q, okc, ovc, tables, ctx, 0.088)
     assert _err(out.cpu().numpy(), ref) <= TOL
+
+
+def test_beam_search_churn_on_the_gpu():
+    """Beam groups decode 24 steps with pruning between steps: copy-on-write
+    copies, slot writes and attention of every beam against the oracle."""
+    from paged_kv_cache_106_gb300.step import BeamGroups
+    from tests.test_beam_churn import _oracle_groups, _oracle_prune
+
+    H, D, B = 8, 128, 16
+    churn = wl.beam_churn(groups=6, width=4, seed=321)
+    nb = sum(-(-n // B) for n in churn.prompt_lens) * churn.width + 6 * 4 * 6
+    order = np.random.default_rng(9).permutation(nb)
+    desc = pk.PoolDesc(nb, B, num_heads=H, head_dim=D, free_order=order)
+    pool = pk.pa_pool_create(desc)
+    m = BlockManager(nb, B, order)
+    # prompts written once by the root, shared by its beams
+    rng = wl.value_rng(wl.mixed_b256(), 9)
+    kc = torch.zeros((nb, H, B, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    okc, ovc = np.zeros((nb, H, B, D), np.float16), np.zeros((nb, H, B, D), np.float16)
+    bg = BeamGroups(pool, churn)
+    beams, nxt = _oracle_groups(m, churn)
+    for g, n in enumerate(churn.prompt_lens):
+        root = beams[g][0]
+        slots = np.array([m.slot_of(root, p) for p in range(n)], np.int64)
+        k, v = wl.normal_f16(rng, (n, H, D)), wl.normal_f16(rng, (n, H, D))
+        pk.pa_write_kv(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                       torch.from_numpy(slots).cuda(), kc, vc, desc)
+        oc.write_kv(okc, ovc, k, v, slots)
+    S = len(bg.ids())
+    mb = -(-max(churn.prompt_lens) // B) + 3
+    runner = DecodeStepRunner(pool, desc, bg.ids(), mb)
+    rg, ro = np.random.default_rng(2), np.random.default_rng(2)
+    copies = 0
+    for step in range(24):
+        runner.ids = np.array(bg.ids(), np.int32)
+        q, k, v = (wl.normal_f16(rng, (S, H, D)) for _ in range(3))
+        runner.prepare()
+        so, co = m.alloc_slots(list(runner.ids))
+        assert runner._views(runner.host[(runner.i - 1) & 1])[0].tolist() == so
+        copies += len(co)
+        out = torch.empty((S, H, D), dtype=torch.float16, device="cuda")
+        runner.copy_blocks([kc], [vc])
+        runner.write_kv(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), kc, vc)
+        runner.attention(out, torch.from_numpy(q).cuda(), kc, vc, 0.088)
+        oc.copy_blocks([okc], [ovc], co)
+        oc.write_kv(okc, ovc, k, v, so)
+        torch.cuda.synchronize()
+        assert runner.status.item() == 0
+        ids = list(runner.ids)
+        tables = np.array(m.padded_tables(ids, mb), np.int32)
+        ctx = np.array([m.num_tokens(s) for s in ids], np.int32)
+        ref = oa.paged_attention(q, okc, ovc, tables, ctx, 0.088)
+        assert _err(out.cpu().numpy(), ref) <= TOL, step
+        if step % 8 == 7:
+            assert torch.equal(kc.cpu(), torch.from_numpy(okc))
+        bg.prune(churn.survivors(rg))
+        nxt = _oracle_prune(m, beams, nxt, churn.survivors(ro))
+    assert copies > 0
