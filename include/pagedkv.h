@@ -213,6 +213,17 @@ int pa_swap_out(pa_pool *gpu, pa_pool *cpu, int32_t n_seqs, const int32_t *seq_i
 int pa_swap_in(pa_pool *cpu, pa_pool *gpu, int32_t n_seqs, const int32_t *seq_ids,
                int32_t *pairs_out, int32_t pairs_cap, int32_t *n_pairs_out);
 
+/* append, several tokens per sequence (chunked prefill, [review] §4.3 "all
+ * tokens of the step are concatenated"; [teardown] chunked prefill): like
+ * pa_alloc_slots with counts[i] >= 0 new tokens for seq_ids[i] -- the first
+ * may copy a shared, partly filled last block (copy-on-write), the tokens
+ * fill the last block's free slots and then take new blocks in queue order.
+ * slot_mapping_out (host, sum(counts) int64) gets the slots sequence by
+ * sequence, in the order given.  All-or-nothing.  Errors: as pa_alloc_slots. */
+int pa_alloc_slots_n(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                     const int32_t *counts, int64_t *slot_mapping_out, int32_t *copies_out,
+                     int32_t copies_cap, int32_t *n_copies_out);
+
 /* Export block tables and context lengths for a batch, in the layout the
  * attention kernel reads: tables_out (host, n_seqs x max_blocks int32,
  * row-major) gets each sequence's physical block ids, padded with -1;

@@ -245,6 +245,31 @@ class BlockManager:
             raise
         return slots, copies
 
+    def alloc_slots_n(self, seq_ids, counts):
+        """counts[i] new tokens for seq_ids[i]: repeated appends, sequence by
+        sequence in the order given (a chunk of tokens is appended one after
+        the other).  All-or-nothing; returns (slot_mapping, copies)."""
+        seq_ids = [int(s) for s in seq_ids]
+        if len(set(seq_ids)) != len(seq_ids) or any(int(c) < 0 for c in counts):
+            raise ValueError("bad batch")
+        for s in seq_ids:
+            if s not in self.tables:
+                raise KeyError(s)
+        saved = (copy.deepcopy(self.free_queue), list(self.ref), copy.deepcopy(self.tables),
+                 dict(self.cache), dict(self.block_key))
+        slots, copies = [], []
+        try:
+            for s, n in zip(seq_ids, counts):
+                for _ in range(int(n)):
+                    slot, cp = self.append(s)
+                    slots.append(slot)
+                    if cp is not None:
+                        copies.append(cp)
+        except OutOfBlocks:
+            self.free_queue, self.ref, self.tables, self.cache, self.block_key = saved
+            raise
+        return slots, copies
+
     # -- whole-state views (for comparisons) ---------------------------------
     def padded_tables(self, seq_ids, max_blocks: int, pad: int = -1):
         """[len(seq_ids)][max_blocks] physical ids, padded with ``pad``."""

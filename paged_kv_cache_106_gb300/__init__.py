@@ -83,6 +83,7 @@ def _load():
         "pa_seq_free_batch": (i32, [vp, i32, vp]),
         "pa_seq_free": (i32, [vp, i32]),
         "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
+        "pa_alloc_slots_n": (i32, [vp, i32, vp, vp, vp, vp, i32, P(i32)]),
         "pa_get_block_tables": (i32, [vp, i32, vp, i32, vp, vp]),
         "pa_seq_info": (i32, [vp, i32, P(i32), P(i32)]),
         "pa_pool_num_free": (i32, [vp, P(i32)]),
@@ -275,6 +276,21 @@ def pa_alloc_slots(pool, seq_ids, copies_cap: int | None = None, slot_out=None, 
     _check(_lib.pa_alloc_slots(pool, n, ids.ctypes.data, slots.ctypes.data, copies.ctypes.data,
                                cap, ctypes.byref(nc)))
     return slots, copies[: nc.value]
+
+
+def pa_alloc_slots_n(pool, seq_ids, counts, copies_cap: int | None = None):
+    """counts[i] new tokens for seq_ids[i]; returns (slot_mapping int64[sum], copies)."""
+    ids, cnt = _host_i32(seq_ids), _host_i32(counts)
+    if ids.shape != cnt.shape:
+        raise ValueError("seq_ids and counts differ in length")
+    n = ids.shape[0]
+    cap = n if copies_cap is None else int(copies_cap)
+    slots = np.empty(max(int(cnt.sum()), 1), np.int64)
+    copies = np.empty((max(cap, 1), 2), np.int32)
+    nc = ctypes.c_int32(0)
+    _check(_lib.pa_alloc_slots_n(pool, n, ids.ctypes.data, cnt.ctypes.data, slots.ctypes.data,
+                                 copies.ctypes.data, cap, ctypes.byref(nc)))
+    return slots[: int(cnt.sum())], copies[: nc.value]
 
 
 def pa_get_block_tables(pool, seq_ids, max_blocks: int, tables_out=None, ctx_out=None):

@@ -470,6 +470,79 @@ int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
     return PA_OK;
 }
 
+int pa_alloc_slots_n(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                     const int32_t *counts, int64_t *slot_mapping_out, int32_t *copies_out,
+                     int32_t copies_cap, int32_t *n_copies_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots_n: NULL pool");
+    if (n_seqs < 0 || (n_seqs > 0 && (!seq_ids || !counts)) || copies_cap < 0 ||
+        (copies_cap > 0 && !copies_out))
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots_n: bad arguments");
+    const int32_t B = pool->block_size;
+    // Dry run, as in pa_alloc_slots: only a shared, partly filled last block
+    // (its count decremented by earlier copies in this call) needs a copy.
+    std::vector<Seq *> seq(static_cast<size_t>(n_seqs));
+    std::unordered_set<int32_t> ids;
+    std::unordered_map<int32_t, int32_t> dec;
+    int64_t need = 0, total = 0;
+    int32_t n_copies = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        auto it = pool->seqs.find(seq_ids[i]);
+        if (it == pool->seqs.end())
+            return fail(PA_ERR_NO_SEQ, "pa_alloc_slots_n: no sequence %d", seq_ids[i]);
+        if (!ids.insert(seq_ids[i]).second)
+            return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots_n: sequence %d listed twice",
+                        seq_ids[i]);
+        if (counts[i] < 0) return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots_n: negative count");
+        Seq &s = it->second;
+        seq[(size_t)i] = &s;
+        total += counts[i];
+        if (counts[i] == 0) continue;
+        int64_t room = 0;   // free slots in the last block usable in place
+        if (!s.table.empty() && pool->last_filled(s) < B) {
+            const int32_t last = s.table.back();
+            int32_t &d = dec[last];
+            if (pool->ref[(size_t)last] - d > 1) {
+                ++need;       // copy-on-write block, then filled
+                ++n_copies;
+                ++d;
+            }
+            room = B - pool->last_filled(s);
+        }
+        if (counts[i] > room) need += (counts[i] - room + B - 1) / B;
+    }
+    if (need > pool->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "pa_alloc_slots_n: need %lld blocks, %lld free",
+                    (long long)need, (long long)pool->count);
+    if (n_copies > copies_cap)
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots_n: %d copies needed, copies_cap is %d",
+                    n_copies, copies_cap);
+    if (total > 0 && !slot_mapping_out)
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots_n: NULL slot_mapping_out");
+    int32_t c = 0;
+    int64_t o = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        Seq &s = *seq[(size_t)i];
+        for (int32_t t = 0; t < counts[i]; ++t) {
+            if (s.table.empty() || pool->last_filled(s) == B) {
+                s.table.push_back(pool->pop_free());
+            } else if (t == 0 && pool->ref[(size_t)s.table.back()] > 1) {
+                const int32_t last = s.table.back();
+                const int32_t nb = pool->pop_free();
+                copies_out[2 * c] = last;
+                copies_out[2 * c + 1] = nb;
+                ++c;
+                --pool->ref[(size_t)last];
+                s.table.back() = nb;
+            }
+            const int32_t off = s.num_tokens - (int32_t)(s.table.size() - 1) * B;
+            slot_mapping_out[o++] = (int64_t)s.table.back() * B + off;
+            ++s.num_tokens;
+        }
+    }
+    if (n_copies_out) *n_copies_out = c;
+    return PA_OK;
+}
+
 int pa_get_block_tables(const pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
                         int32_t max_blocks, int32_t *tables_out, int32_t *ctx_lens_out) {
     if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_get_block_tables: NULL pool");

@@ -201,3 +201,53 @@ def test_device_calls_reject_bad_geometry_before_any_cuda_work():
     # NULL pointers with a valid geometry are refused on the host
     assert pk._lib.pa_write_kv(None, None, None, 1, None, None, d.ref, None, None) == \
         pk.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_multi_token_append_lockstep(seed):
+    """pa_alloc_slots_n against repeated single appends in the oracle."""
+    rng = random.Random(7000 + seed)
+    B = rng.choice([1, 2, 4, 16])
+    nb = rng.randint(0, 48)
+    order = list(range(nb))
+    rng.shuffle(order)
+    abi = AbiAdapter({"num_blocks": nb, "block_size": B, "free_order": order})
+    m = BlockManager(nb, B, order)
+    live, nxt = set(), 0
+    for _ in range(200):
+        r = rng.random()
+        if r < 0.2 or not live:
+            n = rng.randint(0, 3 * B)
+            try:
+                exp = m.add(nxt, n)
+            except OutOfBlocks:
+                with pytest.raises(pk.OutOfBlocks):
+                    abi.add(nxt, n)
+            else:
+                assert abi.add(nxt, n) == exp
+                live.add(nxt)
+            nxt += 1
+        elif r < 0.35:
+            p = rng.choice(sorted(live))
+            m.fork(p, nxt)
+            abi.fork(p, nxt)
+            live.add(nxt)
+            nxt += 1
+        elif r < 0.45:
+            s = rng.choice(sorted(live))
+            m.free(s)
+            abi.free(s)
+            live.discard(s)
+        else:
+            seqs = rng.sample(sorted(live), rng.randint(1, len(live)))
+            counts = [rng.randint(0, 2 * B + 1) for _ in seqs]
+            try:
+                exp = m.alloc_slots_n(seqs, counts)
+            except OutOfBlocks:
+                with pytest.raises(pk.OutOfBlocks):
+                    pk.pa_alloc_slots_n(abi.p, seqs, counts)
+            else:
+                slots, copies = pk.pa_alloc_slots_n(abi.p, seqs, counts)
+                assert slots.tolist() == exp[0]
+                assert [tuple(c) for c in copies.tolist()] == exp[1]
+        _compare(abi, m, live)
