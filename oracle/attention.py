@@ -49,6 +49,13 @@ def _load():
                 ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                 ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int32,
             ]
+            lib.oracle_paged_prefill.restype = ctypes.c_int32
+            lib.oracle_paged_prefill.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_double, ctypes.c_int32,
+            ]
             lib.oracle_half_to_double.restype = ctypes.c_double
             lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -97,3 +104,32 @@ def paged_attention(q, k_cache, v_cache, block_tables, ctx_lens, scale: float,
     if rc != 0:
         raise ValueError(f"oracle_paged_attention rejected its arguments ({rc})")
     return out
+
+
+def paged_prefill(q, k_cache, v_cache, block_tables, ctx_lens, q_starts, scale: float,
+                  num_threads: int = 0) -> np.ndarray:
+    """fp64 causal paged prefill: q float16 [T, H, D] (rows of sequence s are
+    q_starts[s]..q_starts[s+1]-1, the last positions of its context);
+    returns float64 [T, H, D]."""
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    k_cache = np.ascontiguousarray(k_cache, dtype=np.float16)
+    v_cache = np.ascontiguousarray(v_cache, dtype=np.float16)
+    block_tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    q_starts = np.ascontiguousarray(q_starts, dtype=np.int32)
+    T, H, D = q.shape
+    NB, H2, B, D2 = k_cache.shape
+    S = ctx_lens.shape[0]
+    if (H2, D2) != (H, D) or q_starts.shape != (S + 1,) or int(q_starts[-1]) != T:
+        raise ValueError("shape mismatch")
+    out = np.empty((T, H, D), dtype=np.float64)
+    rc = _load().oracle_paged_prefill(
+        out.ctypes.data, q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
+        block_tables.ctypes.data, ctx_lens.ctypes.data, q_starts.ctypes.data,
+        S, H, D, B, NB, block_tables.shape[1], float(scale), int(num_threads))
+    if rc == -2:
+        raise IndexError("block table entry outside the pool")
+    if rc != 0:
+        raise ValueError(f"oracle_paged_prefill rejected its arguments ({rc})")
+    return out
+

@@ -146,6 +146,85 @@ int oracle_paged_attention(double *out,                  /* [S][H][D]           
     return 0;
 }
 
+/* Paged prefill (many queries per sequence, causal): the queries of
+ * sequence s are rows q_starts[s] .. q_starts[s+1]-1 of q and are the last
+ * q_len = q_starts[s+1] - q_starts[s] positions of its context of ctx_lens[s]
+ * tokens; the query at position p attends to positions 0..p (the paper
+ * review's §4.3 prompt phase: every prompt token attends to the tokens
+ * before it and itself).  Same blockwise softmax as the decode oracle.
+ * out: [T][H][D] fp64, T = q_starts[S].  Returns 0, -1 on a bad argument,
+ * -2 on a table entry outside the pool. */
+int oracle_paged_prefill(double *out, const uint16_t *q, const uint16_t *k_cache,
+                         const uint16_t *v_cache, const int32_t *block_tables,
+                         const int32_t *ctx_lens, const int32_t *q_starts, int32_t S, int32_t H,
+                         int32_t D, int32_t B, int32_t num_blocks, int32_t max_blocks,
+                         double scale, int32_t num_threads)
+{
+    if (S < 0 || H <= 0 || D <= 0 || B <= 0 || max_blocks < 0) return -1;
+    if (S > 0 && q_starts[0] != 0) return -1;
+    for (int32_t s = 0; s < S; ++s) {
+        int32_t n = ctx_lens[s], ql = q_starts[s + 1] - q_starts[s];
+        if (n < 0 || ql < 0 || ql > n || (int64_t)n > (int64_t)max_blocks * B) return -1;
+        for (int32_t j = 0; j < (n + B - 1) / B; ++j) {
+            int32_t blk = block_tables[(int64_t)s * max_blocks + j];
+            if (blk < 0 || blk >= num_blocks) return -2;
+        }
+    }
+    build_half_table();
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+    int64_t T = S > 0 ? q_starts[S] : 0;
+#pragma omp parallel
+    {
+        double *x = NULL;
+        int32_t x_cap = 0;
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t item = 0; item < T * H; ++item) {
+            int64_t row = item / H;
+            int32_t h = (int32_t)(item % H);
+            int32_t s = 0;                          /* sequence owning this row */
+            while (q_starts[s + 1] <= row) ++s;
+            int32_t n = ctx_lens[s];
+            int32_t ql = q_starts[s + 1] - q_starts[s];
+            int32_t pos = n - ql + (int32_t)(row - q_starts[s]);
+            int32_t m_tok = pos + 1;                /* causal: positions 0..pos */
+            double *o = out + item * D;
+            for (int32_t d = 0; d < D; ++d) o[d] = 0.0;
+            if (m_tok > x_cap) {
+                free(x);
+                x_cap = m_tok;
+                x = (double *)malloc(sizeof(double) * (size_t)m_tok);
+            }
+            const uint16_t *qv = q + item * D;
+            double mx = -INFINITY;
+            for (int32_t p = 0; p < m_tok; ++p) {
+                int32_t blk = block_tables[(int64_t)s * max_blocks + p / B];
+                const uint16_t *kv = k_cache + (((int64_t)blk * H + h) * B + p % B) * D;
+                double dot = 0.0;
+                for (int32_t d = 0; d < D; ++d) dot += g_half_table[qv[d]] * g_half_table[kv[d]];
+                x[p] = dot * scale;
+                if (x[p] > mx) mx = x[p];
+            }
+            double denom = 0.0;
+            for (int32_t p = 0; p < m_tok; ++p) {
+                x[p] = exp(x[p] - mx);
+                denom += x[p];
+            }
+            for (int32_t p = 0; p < m_tok; ++p) {
+                int32_t blk = block_tables[(int64_t)s * max_blocks + p / B];
+                const uint16_t *vv = v_cache + (((int64_t)blk * H + h) * B + p % B) * D;
+                double a = x[p] / denom;
+                for (int32_t d = 0; d < D; ++d) o[d] += a * g_half_table[vv[d]];
+            }
+        }
+        free(x);
+    }
+    return 0;
+}
+
 /* Threads an OpenMP parallel region would use (for reporting the CPU
  * baseline's core count). */
 int oracle_max_threads(void)

@@ -206,3 +206,70 @@ def test_zero_context_gives_zero_and_bad_table_is_rejected():
     assert np.array_equal(out, np.zeros_like(out))
     with pytest.raises(IndexError):
         oa.paged_attention(q, kc, kc, np.array([[0], [5]], np.int32), np.array([1, 1], np.int32), 1.0)
+
+
+# ---- causal paged prefill --------------------------------------------------
+
+def _prefill_batch(rng, ctx, qlen, H, D, B):
+    nblk = [-(-c // B) for c in ctx]
+    NB = sum(nblk) + 2
+    perm = rng.permutation(NB)
+    MB = max(nblk)
+    tables = np.full((len(ctx), MB), -1, np.int32)
+    pos = 0
+    for i, n in enumerate(nblk):
+        tables[i, :n] = perm[pos:pos + n]
+        pos += n
+    kc = rng.standard_normal((NB, H, B, D)).astype(np.float16)
+    vc = rng.standard_normal((NB, H, B, D)).astype(np.float16)
+    qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    q = rng.standard_normal((int(qs[-1]), H, D)).astype(np.float16)
+    return q, kc, vc, tables, np.array(ctx, np.int32), qs
+
+
+def test_prefill_matches_sdpa_with_an_explicit_causal_mask():
+    rng = _rng(101)
+    H, D, B = 3, 32, 4
+    ctx, qlen = [13, 7, 20], [13, 3, 6]          # whole prompt, a chunk, a chunk
+    q, kc, vc, tables, ctxa, qs = _prefill_batch(rng, ctx, qlen, H, D, B)
+    out = oa.paged_prefill(q, kc, vc, tables, ctxa, qs, 0.2)
+    for s, (n, ql) in enumerate(zip(ctx, qlen)):
+        # contiguous K/V of the sequence, gathered with numpy indexing only
+        t = tables[s, : -(-n // B)]
+        K = kc[t].transpose(1, 0, 2, 3).reshape(H, -1, D)[:, :n].astype(np.float64)
+        V = vc[t].transpose(1, 0, 2, 3).reshape(H, -1, D)[:, :n].astype(np.float64)
+        Q = q[qs[s]:qs[s + 1]].transpose(1, 0, 2).astype(np.float64)       # [H, ql, D]
+        mask = np.arange(n)[None, :] <= (n - ql + np.arange(ql))[:, None]   # bottom-right causal
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(Q), torch.from_numpy(K), torch.from_numpy(V),
+            attn_mask=torch.from_numpy(mask), scale=0.2).numpy()
+        np.testing.assert_allclose(out[qs[s]:qs[s + 1]].transpose(1, 0, 2), ref, atol=1e-12)
+
+
+def test_prefill_first_token_and_decode_special_case():
+    rng = _rng(103)
+    H, D, B = 2, 16, 4
+    q, kc, vc, tables, ctxa, qs = _prefill_batch(rng, [9, 5], [9, 1], H, D, B)
+    out = oa.paged_prefill(q, kc, vc, tables, ctxa, qs, 0.3)
+    # the first prompt token attends only to itself: o = v_0 exactly
+    assert np.array_equal(out[0], vc[tables[0, 0], :, 0, :].astype(np.float64))
+    # one query at the end of its context is a decode query
+    dec = oa.paged_attention(q[qs[1]:qs[2]], kc, vc, tables[1:2], ctxa[1:2], 0.3)
+    assert np.array_equal(out[qs[1]:qs[2]], dec)
+
+
+def test_prefill_never_reads_future_or_unwritten_positions():
+    rng = _rng(105)
+    H, D, B = 2, 8, 4
+    q, kc, vc, tables, ctxa, qs = _prefill_batch(rng, [10], [4], H, D, B)
+    ref = oa.paged_prefill(q, kc, vc, tables, ctxa, qs, 0.5)
+    kc2, vc2 = kc.copy(), vc.copy()
+    last = tables[0, 2]
+    kc2[last, :, 2:, :] = np.nan                 # slots past ctx 10
+    vc2[last, :, 2:, :] = np.nan
+    out = oa.paged_prefill(q, kc2, vc2, tables, ctxa, qs, 0.5)
+    assert np.array_equal(out, ref)
+    # changing position 9 (the last query's own token) leaves the earlier queries alone
+    kc2[last, :, 1, :] += np.float16(1.0)
+    out2 = oa.paged_prefill(q, kc2, vc2, tables, ctxa, qs, 0.5)
+    assert np.array_equal(out2[:3], ref[:3]) and not np.array_equal(out2[3], ref[3])
