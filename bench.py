@@ -656,6 +656,178 @@ def run_beam_churn(args):
     pk.pa_pool_destroy(pool)
 
 
+PREFILL_METRIC = "paged prefill-attn prompt-tokens/s (1 GB300) + achieved TFLOP/s"
+PREFILL_UNIT = "prompt-tokens/s"
+
+
+def prefill_flops(lens_ctx, lens_q, num_heads, head_dim):
+    """Algorithmic flops of causal prefill: the query at position p takes
+    p + 1 dot products of length D for the scores and as many scaled value
+    rows: 4 * D * (p + 1) flops per head."""
+    tot = 0
+    for c, n in zip(lens_ctx, lens_q):
+        first = c - n                       # positions first .. c-1 are queries
+        tot += (c * (c + 1) - first * (first + 1)) // 2
+    return 4 * head_dim * num_heads * tot
+
+
+def _prefill_cpu_baseline(seconds: float):
+    """The oracle on a bounded sample of the prefill batch: its first 8 prompts."""
+    from oracle import attention as oa
+    from paged_kv_cache_106_gb300 import workloads as wl
+    from oracle.alloc import BlockManager
+
+    w = wl.prefill_b256()
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    lens = w.prompt_lens[:8]
+    m = BlockManager(w.num_blocks, B, w.free_order)
+    for i, n in enumerate(lens):
+        m.add(i, n)
+    used = sorted({b for i in range(len(lens)) for b in m.block_table(i)})
+    rng = wl.value_rng(w, 3)
+    kc = np.zeros((w.num_blocks, H, B, D), np.float16)
+    vc = np.zeros_like(kc)
+    for b in used:
+        kc[b] = wl.normal_f16(rng, (H, B, D))
+        vc[b] = wl.normal_f16(rng, (H, B, D))
+    mb = -(-max(lens) // B)
+    tables = np.array(m.padded_tables(list(range(len(lens))), mb), np.int32)
+    ctx = np.array(lens, np.int32)
+    qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = wl.normal_f16(rng, (int(qs[-1]), H, D))
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oa.paged_prefill(q, kc, vc, tables, ctx, qs, w.scale)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": passes * int(qs[-1]) / dt, "unit": PREFILL_UNIT, "cores": oa.max_threads(),
+            "kind": "oracle",
+            "sample": f"first 8 of the 256 prompts ({int(qs[-1])} tokens), {passes} passes in "
+                      f"{dt:.1f} s, fp64 C + OpenMP"}
+
+
+def run_prefill(args):
+    """Prompt phase of the mixed batch: every step writes the K/V of all 256
+    prompts into the pool (pa_write_kv, one slot per prompt token) and runs
+    causal paged prefill attention over them (one OPT-13B layer)."""
+    import torch
+
+    import paged_kv_cache_106_gb300 as pk
+    from paged_kv_cache_106_gb300 import workloads as wl
+
+    ws, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.prefill_b256(seed=112 + rank)
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    lens = np.array(w.prompt_lens, np.int64)
+    desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
+    pool = pk.pa_pool_create(desc)
+    slots = np.concatenate([pk.pa_seq_add(pool, i, int(n)) for i, n in enumerate(lens)])
+    mb = -(-int(lens.max()) // B)
+    tables, ctx = pk.pa_get_block_tables(pool, list(range(len(lens))), mb)
+    T = int(lens.sum())
+    qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    kc = torch.empty((w.num_blocks, H, B, D), dtype=torch.float16, device=dev).normal_(generator=gen)
+    vc = torch.empty_like(kc).normal_(generator=gen)
+    q = torch.randn((T, H, D), dtype=torch.float16, device=dev, generator=gen)
+    k_new, v_new = torch.randn_like(q), torch.randn_like(q)
+    out = torch.empty_like(q)
+    d_slots = torch.from_numpy(slots).to(dev)
+    d_tables, d_ctx, d_qs = (torch.from_numpy(x).to(dev) for x in (tables, ctx, qs))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    mql = int(lens.max())
+    flops = prefill_flops(ctx.tolist(), lens.tolist(), H, D)
+
+    def step(ev=None):
+        pk.pa_write_kv(k_new, v_new, d_slots, kc, vc, desc, status=status, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pk.pa_prefill_attention(out, q, kc, vc, d_tables, d_ctx, d_qs, w.scale, desc,
+                                max_q_len=mql, status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert status.item() == 0, status.item()
+    el = t0.elapsed_time(t1) / 1e3
+    attn_s = sum(a.elapsed_time(b) for a, b in evs) / len(evs) / 1e3
+    # end to end through the same calls: the step's new K/V and queries come
+    # from pinned host memory, the output goes back to it
+    h_k, h_v, h_q = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
+    h_o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    for h in (h_k, h_v, h_q):
+        h.normal_()
+    e2e_steps = max(1, min(args.e2e_steps, 20))
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            k_new.copy_(h_k, non_blocking=True)
+            v_new.copy_(h_v, non_blocking=True)
+            q.copy_(h_q, non_blocking=True)
+            step()
+            h_o.copy_(out, non_blocking=True)
+            stream.synchronize()
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    (tok_all, e2e_tok), (el_max, e2e_max) = reduce_across_ranks(
+        [T * args.steps, T * e2e_steps], [el, e2e_s * e2e_steps], dev)
+    if rank == 0:
+        peak = None
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                peak, kind = float(json.load(f)["bf16_tflops"]), "measured bf16 burst (fp16 nominal rate = bf16)"
+        except Exception:
+            peak, kind = 1900.0, "fallback"
+        achieved = flops / attn_s / 1e12
+        line = {
+            "metric": PREFILL_METRIC, "value": tok_all / el_max, "unit": PREFILL_UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": "prompt phase of the mixed batch: 256 whole prompts, lognormal "
+                                   "(median 200, cap 1536), OPT-13B layer 40x128, block 16",
+                       "prompt_tokens": T, "pool_blocks": w.num_blocks,
+                       "l2": "K/V written and read back per step ~1.7 GB >> 129 MB L2, no flush"},
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill_mma<128> (pa_prefill_attention)",
+                         "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "algorithmic_flops_per_launch": flops,
+                         "attn_ms_per_launch": attn_s * 1e3},
+            "kernels": {"pa_write_kv": {"us_per_launch": (el / args.steps - attn_s) * 1e6,
+                                        "tokens": T, "algorithmic_bytes": T * H * D * 2 * 4}},
+            "e2e": {"value": e2e_tok / e2e_max, "unit": PREFILL_UNIT,
+                    "h2d_bytes_per_step": 3 * T * H * D * 2, "d2h_bytes_per_step": T * H * D * 2,
+                    "steps": e2e_steps, "timing": "wall clock, stream synchronised every step"},
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = _prefill_cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    pk.pa_pool_destroy(pool)
+
+
 def _oracle_sample(n_seqs):
     """Host data for the first n_seqs sequences of the same workload, laid
     out by the oracle's own block manager."""
@@ -741,10 +913,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)
-    ap.add_argument("--workload", choices=["mixed_b256", "full_40l", "beam_churn"],
+    ap.add_argument("--workload", choices=["mixed_b256", "full_40l", "beam_churn", "prefill"],
                     default="mixed_b256",
                     help="mixed_b256: the headline workload; full_40l: 40-layer pool-filling "
-                         "step; beam_churn: beam search with pruning")
+                         "step; beam_churn: beam search with pruning; prefill: causal "
+                         "prefill of the mixed batch's prompts")
     ap.add_argument("--beam", action="store_true", help="full_40l: beam groups sharing blocks")
     ap.add_argument("--dump-steps", default="",
                     help="write each warm-up and timed step's algorithmic attention bytes here")
@@ -759,6 +932,8 @@ def main():
         run_full40(args)
     elif args.workload == "beam_churn":
         run_beam_churn(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 

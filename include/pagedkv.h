@@ -321,6 +321,41 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
                         int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
                         int32_t *status, const pa_pool_desc *desc, void *stream);
 
+/* Causal paged prefill attention ([review] §4.3, the prompt phase: the
+ * prompt's tokens are processed together, each attending to the tokens
+ * before it and itself; [notes] §3.1 blockwise attention equation, applied
+ * to each of those queries).  Sequence s < n_seqs has
+ * q_len = q_starts[s+1] - q_starts[s] queries, rows q_starts[s] .. of q, and
+ * a context of ctx = ctx_lens[s] stored tokens that includes the queries' own
+ * tokens (written beforehand with pa_write_kv).  Row q_starts[s] + i is the
+ * query at position p = ctx - q_len + i and, for every head h,
+ *     out[row][h] = sum_{j <= p} softmax_j(scale * q[row][h] . k_j) v_j,
+ * with k_j, v_j read through block_tables[s] as in pa_decode_attention.
+ * q_len == ctx is a whole prompt; q_len < ctx continues a sequence whose
+ * first ctx - q_len tokens are already cached (a later chunk of a long
+ * prompt, or a prompt whose leading blocks came from the prefix cache).
+ * q_len == 1 is a decode query.
+ *   out, q        [T][num_heads][head_dim] fp16, T >= q_starts[n_seqs];
+ *                 out, q and the caches 16-byte aligned
+ *   block_tables  [n_seqs][max_blocks] int32 (entries past ceil(ctx/B) unread)
+ *   ctx_lens      [n_seqs] int32
+ *   q_starts      [n_seqs + 1] int32, non-decreasing
+ *   max_q_len     host bound on every q_len (sizes the launch)
+ * head_dim 64 or 128, block_size 4..32.  Tensor cores: fp16 products, fp32
+ * accumulation; the probabilities enter the second product as the sum of two
+ * fp16 terms, so the fp16 rounding of the output dominates the error.
+ * Device-side problems go to *status and leave that sequence's rows
+ * unwritten: PA_ERR_INVALID_ARG for q_len < 0, q_len > ctx or
+ * q_len > max_q_len; PA_ERR_BAD_BLOCK for ctx > max_blocks * B or a table
+ * entry outside the pool (that key / value is then read as zeros).
+ * Errors: PA_ERR_INVALID_ARG (geometry, sizes, NULL or misaligned
+ * pointers), PA_ERR_CUDA. */
+int pa_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, const int32_t *ctx_lens,
+                         const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,
+                         int32_t max_q_len, float scale, int32_t *status,
+                         const pa_pool_desc *desc, void *stream);
+
 /* ---- decode attention without a caller-provided workspace ------------------
  * No counterpart on the pages: this entry point exists for callers that
  * cannot allocate device memory when they run attention -- for instance a

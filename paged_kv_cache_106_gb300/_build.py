@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libpagedkv.so")
 OBJ = os.path.join(PKG, "_build")
 HEADERS = [os.path.join(ROOT, "include", "pagedkv.h")]
-SOURCES = ["pool.cpp", "api.cpp", "write_kv.cu", "copy_blocks.cu", "decode_attention.cu"]
+SOURCES = ["pool.cpp", "api.cpp", "write_kv.cu", "copy_blocks.cu", "decode_attention.cu",
+           "prefill_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

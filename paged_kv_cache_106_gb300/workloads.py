@@ -21,7 +21,9 @@ notes, unpurerationalist.github.io, §2 "Large KV cache"; default block size
                        context capped at 2048;
 * ``full_40l``         40 layers over a pool-filling cache, context uniform
                        in [512, 2048], optional beam groups of 4 sharing 55 %
-                       of their blocks.
+                       of their blocks;
+* ``prefill_b256``     the prompt phase of the mixed batch: 256 prompts,
+                       lognormal (median 200, cap 1536), each prefilled whole.
 
 Readings where the workload text is silent: lognormal sigma = 1.0 with
 mu = ln(median), lengths clipped to [1, cap]; a context length counts the
@@ -232,6 +234,18 @@ CONFIGS = {
     "parallel_sampling": parallel_sampling,
     "mixed_b256": mixed_b256,
 }
+
+
+def prefill_b256(seed: int = 112, batch: int = 256) -> DecodeWorkload:
+    """256 whole prompts drawn like the mixed batch's prompts; the pool holds
+    them with 25 % spare blocks and a shuffled free queue."""
+    rng = _rng(seed)
+    plen = _lognormal_lengths(rng, batch, 200, 1536)
+    nb = int(math.ceil(1.25 * sum(_blocks(n, DEFAULT_BLOCK) for n in plen)))
+    return DecodeWorkload(name="prefill_b256", seed=seed, num_heads=OPT13B_HEADS,
+                          head_dim=OPT13B_HEAD_DIM, block_size=DEFAULT_BLOCK, num_layers=1,
+                          num_blocks=nb, free_order=_free_order(rng, nb),
+                          prompt_lens=[int(x) for x in plen], decode_steps=0)
 
 
 def value_rng(workload: DecodeWorkload, stream: int = 0) -> np.random.Generator:

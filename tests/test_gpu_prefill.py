@@ -1,0 +1,304 @@
+"""GPU parity of causal paged prefill attention (pa_prefill_attention) and of
+the prefill step it belongs to (pa_seq_add / pa_alloc_slots_n -> pa_write_kv
+with many tokens per sequence -> pa_prefill_attention), against the fp64
+oracle.
+
+* max |gpu - oracle| <= 2e-3 (fp16 output, fp32 accumulation), over both
+  supported head dimensions, every block size, whole prompts and chunks
+  continuing a cached prefix, query counts that fill several 64-query tiles
+  and leave a ragged tail, one-query sequences and empty ones;
+* the output is bitwise independent of where the blocks sit in the pool;
+* a one-query sequence agrees with pa_decode_attention on the same context;
+* kernel-side checks: q_len > ctx and table entries outside the pool are
+  reported through the status word; unsupported geometry is refused on the
+  host.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_106_gb300 as pk
+from oracle import attention as oa
+from oracle import cache_ops as oc
+from paged_kv_cache_106_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _f16(rng, shape):
+    return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _batch(rng, ctx, qlen, H, D, B, extra_blocks=3):
+    nblk = [-(-c // B) for c in ctx]
+    NB = sum(nblk) + extra_blocks
+    perm = rng.permutation(NB).astype(np.int32)
+    MB = max(1, max(nblk))
+    tables = np.full((len(ctx), MB), -1, np.int32)
+    pos = 0
+    for i, n in enumerate(nblk):
+        tables[i, :n] = perm[pos:pos + n]
+        pos += n
+    kc = _f16(rng, (NB, H, B, D))
+    vc = _f16(rng, (NB, H, B, D))
+    qs = np.concatenate([[0], np.cumsum(qlen)]).astype(np.int32)
+    q = _f16(rng, (int(qs[-1]), H, D))
+    return q, kc, vc, tables, np.array(ctx, np.int32), qs
+
+
+def _gpu_prefill(q, kc, vc, tables, ctx, qs, scale, B, status=None, max_q_len=None):
+    T, H, D = q.shape
+    desc = pk.PoolDesc(kc.shape[0], B, num_heads=H, head_dim=D)
+    out = torch.full((max(T, 1), H, D), float("nan"), dtype=torch.float16, device="cuda")
+    st = _status() if status is None else status
+    mql = int(np.max(np.diff(qs))) if max_q_len is None and len(ctx) else (max_q_len or 0)
+    pk.pa_prefill_attention(out, _dev(q) if T else out, _dev(kc), _dev(vc), _dev(tables),
+                            _dev(ctx), _dev(qs), scale, desc, max_q_len=mql, status=st)
+    torch.cuda.synchronize()
+    if status is None:
+        assert st.item() == 0, pk.pa_last_error_string()
+    return out[:T].cpu().numpy()
+
+
+def _check(got, ref):
+    assert np.all(np.isfinite(got))
+    err = np.abs(got.astype(np.float64) - ref).max() if got.size else 0.0
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B", [4, 8, 16, 32])
+def test_prefill_matches_oracle(D, B):
+    rng = np.random.default_rng(1000 + D + B)
+    H = 3
+    # (ctx, q_len): whole prompts of 1, 63, 64, 65, 200 tokens; chunks after
+    # a cached prefix (q_len < ctx), one-query sequences, an empty query set
+    pairs = [(1, 1), (63, 63), (64, 64), (65, 65), (200, 200), (150, 37), (300, 129),
+             (77, 1), (5, 0), (129, 128), (2 * B + 1, 2)]
+    ctx = [c for c, _ in pairs]
+    ql = [x for _, x in pairs]
+    q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ql, H, D, B)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    got = _gpu_prefill(q, kc, vc, tables, ctxa, qs, scale, B)
+    ref = oa.paged_prefill(q, kc, vc, tables, ctxa, qs, scale)
+    _check(got, ref)
+
+
+def test_prefill_block_placement_is_bitwise_irrelevant():
+    rng = np.random.default_rng(7)
+    H, D, B = 2, 128, 16
+    ctx, ql = [300, 90, 17], [300, 50, 17]
+    q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ql, H, D, B, extra_blocks=0)
+    scale = 1 / math.sqrt(D)
+    a = _gpu_prefill(q, kc, vc, tables, ctxa, qs, scale, B)
+    # move every block to a new physical id, carrying its contents along
+    NB = kc.shape[0]
+    new = rng.permutation(NB).astype(np.int32)
+    kc2 = np.empty_like(kc)
+    vc2 = np.empty_like(vc)
+    kc2[new] = kc
+    vc2[new] = vc
+    t2 = np.where(tables >= 0, new[np.maximum(tables, 0)], -1).astype(np.int32)
+    b = _gpu_prefill(q, kc2, vc2, t2, ctxa, qs, scale, B)
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+def test_one_query_prefill_agrees_with_decode():
+    rng = np.random.default_rng(9)
+    H, D, B = 4, 128, 16
+    ctx = [1, 17, 300, 511]
+    q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, [1] * len(ctx), H, D, B)
+    scale = 1 / math.sqrt(D)
+    pre = _gpu_prefill(q, kc, vc, tables, ctxa, qs, scale, B)
+    desc = pk.PoolDesc(kc.shape[0], B, num_heads=H, head_dim=D)
+    out = torch.empty((len(ctx), H, D), dtype=torch.float16, device="cuda")
+    ws_bytes = pk.pa_decode_workspace_bytes(len(ctx), tables.shape[1], desc)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    st = _status()
+    pk.pa_decode_attention(out, _dev(q), _dev(kc), _dev(vc), _dev(tables), _dev(ctxa), scale,
+                           desc, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    dec = out.cpu().numpy().astype(np.float64)
+    ref = oa.paged_attention(q, kc, vc, tables, ctxa, scale)
+    _check(pre, ref)
+    assert np.abs(dec - pre.astype(np.float64)).max() <= 2 * TOL
+
+
+def _prefill_step(pool, desc, kc, vc, seq_ids, chunks, rng, H, D, MB, known):
+    """One prefill step through the pool: allocate slots for each sequence's
+    chunk (pa_alloc_slots_n for known sequences, pa_seq_add for new ones),
+    write the chunk's K/V, run prefill attention; returns what the oracle
+    needs."""
+    slots = []
+    for sid, n in zip(seq_ids, chunks):
+        if sid not in known:
+            slots.append(pk.pa_seq_add(pool, sid, n))
+            known.add(sid)
+        else:
+            s, copies = pk.pa_alloc_slots_n(pool, [sid], [n])
+            assert len(copies) == 0
+            slots.append(s)
+    slot_mapping = np.concatenate(slots).astype(np.int64)
+    T = slot_mapping.shape[0]
+    k_new, v_new, q = _f16(rng, (T, H, D)), _f16(rng, (T, H, D)), _f16(rng, (T, H, D))
+    st = _status()
+    pk.pa_write_kv(_dev(k_new), _dev(v_new), _dev(slot_mapping), kc, vc, desc, status=st)
+    tables, ctx = pk.pa_get_block_tables(pool, seq_ids, MB)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    out = torch.empty((T, H, D), dtype=torch.float16, device="cuda")
+    pk.pa_prefill_attention(out, _dev(q), kc, vc, _dev(tables), _dev(ctx), _dev(qs),
+                            1 / math.sqrt(D), desc, max_q_len=int(max(chunks)), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return q, tables, ctx, qs, out.cpu().numpy()
+
+
+def test_prefill_step_through_the_pool_whole_prompts_then_chunks():
+    rng = np.random.default_rng(11)
+    H, D, B, NB, MB = 2, 64, 16, 256, 64
+    order = rng.permutation(NB).astype(np.int32)
+    desc = pk.PoolDesc(NB, B, num_heads=H, head_dim=D, free_order=order)
+    pool = pk.pa_pool_create(desc)
+    try:
+        kc = torch.zeros((NB, H, B, D), dtype=torch.float16, device="cuda")
+        vc = torch.zeros_like(kc)
+        ids, known = [3, 8, 21, 40], set()
+        for chunks in ([70, 16, 1, 130], [64, 9, 33, 1], [1, 100, 15, 64]):
+            q, tables, ctx, qs, got = _prefill_step(pool, desc, kc, vc, ids, chunks, rng, H, D, MB, known)
+            ref = oa.paged_prefill(q, kc.cpu().numpy(), vc.cpu().numpy(), tables, ctx, qs,
+                                   1 / math.sqrt(D))
+            _check(got, ref)
+        assert list(ctx) == [135, 125, 49, 195]
+    finally:
+        pk.pa_pool_destroy(pool)
+
+
+def test_prefill_writes_land_where_the_oracle_byte_model_puts_them():
+    """The K1 write with N >> S tokens (a whole prompt per sequence) gives the
+    oracle's byte image, and prefill then reads exactly those bytes."""
+    rng = np.random.default_rng(12)
+    H, D, B, NB = 2, 128, 8, 96
+    desc = pk.PoolDesc(NB, B, num_heads=H, head_dim=D, free_order=rng.permutation(NB).astype(np.int32))
+    pool = pk.pa_pool_create(desc)
+    try:
+        lens = [200, 3, 97, 64]
+        slots = np.concatenate([pk.pa_seq_add(pool, i, n) for i, n in enumerate(lens)])
+        T = slots.shape[0]
+        k_new, v_new = _f16(rng, (T, H, D)), _f16(rng, (T, H, D))
+        kc0, vc0 = _f16(rng, (NB, H, B, D)), _f16(rng, (NB, H, B, D))
+        kc, vc = _dev(kc0), _dev(vc0)
+        st = _status()
+        pk.pa_write_kv(_dev(k_new), _dev(v_new), _dev(slots), kc, vc, desc, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        ek, ev = kc0.copy(), vc0.copy()
+        oc.write_kv(ek, ev, k_new, v_new, slots)
+        assert np.array_equal(kc.cpu().numpy().view(np.uint16), ek.view(np.uint16))
+        assert np.array_equal(vc.cpu().numpy().view(np.uint16), ev.view(np.uint16))
+        tables, ctx = pk.pa_get_block_tables(pool, list(range(len(lens))), 32)
+        qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        q = _f16(rng, (T, H, D))
+        got = _gpu_prefill(q, ek, ev, tables, ctx, qs, 0.08, B)
+        _check(got, oa.paged_prefill(q, ek, ev, tables, ctx, qs, 0.08))
+    finally:
+        pk.pa_pool_destroy(pool)
+
+
+def test_prefill_full_size_batch_sampled():
+    """The bench's prefill batch (256 prompts, 40 heads x 128, block 16) in the
+    launch configuration the bench times; the oracle checks a sample of
+    sequences (the longest, the shortest and random ones)."""
+    w = wl.prefill_b256()
+    rng = wl.value_rng(w)
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    lens = np.array(w.prompt_lens)
+    desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
+    pool = pk.pa_pool_create(desc)
+    try:
+        slots = np.concatenate([pk.pa_seq_add(pool, i, int(n)) for i, n in enumerate(lens)])
+        MB = -(-int(lens.max()) // B)
+        tables, ctx = pk.pa_get_block_tables(pool, list(range(len(lens))), MB)
+    finally:
+        pk.pa_pool_destroy(pool)
+    T = int(lens.sum())
+    g = torch.Generator(device="cuda").manual_seed(5)
+    kc = torch.randn((w.num_blocks, H, B, D), generator=g, device="cuda", dtype=torch.float16)
+    vc = torch.randn((w.num_blocks, H, B, D), generator=g, device="cuda", dtype=torch.float16)
+    q = torch.randn((T, H, D), generator=g, device="cuda", dtype=torch.float16)
+    qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    out = torch.empty_like(q)
+    st = _status()
+    pk.pa_prefill_attention(out, q, kc, vc, _dev(tables), _dev(ctx), _dev(qs), w.scale, desc,
+                            max_q_len=int(lens.max()), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    sample = sorted({int(lens.argmax()), int(lens.argmin())} |
+                    set(rng.choice(len(lens), 6, replace=False).tolist()))
+    used = np.unique(tables[sample][tables[sample] >= 0])
+    remap = np.full(w.num_blocks, -1, np.int32)
+    remap[used] = np.arange(used.size, dtype=np.int32)
+    kcs = kc[torch.from_numpy(used).cuda()].cpu().numpy()
+    vcs = vc[torch.from_numpy(used).cuda()].cpu().numpy()
+    ts = np.where(tables[sample] >= 0, remap[np.maximum(tables[sample], 0)], -1).astype(np.int32)
+    rows = np.concatenate([np.arange(qs[i], qs[i + 1]) for i in sample])
+    qsub = q[torch.from_numpy(rows).cuda()].cpu().numpy()
+    qss = np.concatenate([[0], np.cumsum(lens[sample])]).astype(np.int32)
+    ref = oa.paged_prefill(qsub, kcs, vcs, ts, ctx[sample], qss, w.scale)
+    got = out[torch.from_numpy(rows).cuda()].cpu().numpy()
+    _check(got, ref)
+
+
+def test_prefill_status_reports_bad_lengths_and_blocks():
+    rng = np.random.default_rng(13)
+    H, D, B = 2, 64, 4
+    q, kc, vc, tables, ctxa, qs = _batch(rng, [10, 10], [10, 4], H, D, B)
+    # q_len > ctx for sequence 1: its rows stay unwritten, the status says why
+    bad_ctx = ctxa.copy()
+    bad_ctx[1] = 3
+    st = _status()
+    got = _gpu_prefill(q, kc, vc, tables, bad_ctx, qs, 0.1, B, status=st)
+    assert st.item() == pk.PA_ERR_INVALID_ARG
+    assert np.all(np.isnan(got[qs[1]:qs[2]].astype(np.float32)))
+    _check(got[:qs[1]], oa.paged_prefill(q[:qs[1]], kc, vc, tables[:1], ctxa[:1], qs[:2], 0.1))
+    # a table entry outside the pool is skipped and reported
+    t2 = tables.copy()
+    t2[0, 1] = kc.shape[0] + 5
+    st = _status()
+    _gpu_prefill(q, kc, vc, t2, ctxa, qs, 0.1, B, status=st)
+    assert st.item() == pk.PA_ERR_BAD_BLOCK
+    # a context longer than the table
+    st = _status()
+    c3 = ctxa.copy()
+    c3[0] = tables.shape[1] * B + 1
+    _gpu_prefill(q, kc, vc, tables, c3, qs, 0.1, B, status=st)
+    assert st.item() == pk.PA_ERR_BAD_BLOCK
+
+
+def test_prefill_host_side_refusals():
+    rng = np.random.default_rng(14)
+    q, kc, vc, tables, ctxa, qs = _batch(rng, [8], [8], 2, 32, 4)
+    desc = pk.PoolDesc(kc.shape[0], 4, num_heads=2, head_dim=32)
+    out = torch.empty((8, 2, 32), dtype=torch.float16, device="cuda")
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_prefill_attention(out, _dev(q), _dev(kc), _dev(vc), _dev(tables), _dev(ctxa),
+                                _dev(qs), 0.1, desc, max_q_len=8)
+    # misaligned q
+    q2, kc2, vc2, t2, c2, qs2 = _batch(rng, [8], [8], 2, 64, 4)
+    desc2 = pk.PoolDesc(kc2.shape[0], 4, num_heads=2, head_dim=64)
+    qbuf = torch.empty(8 * 2 * 64 + 1, dtype=torch.float16, device="cuda")
+    out2 = torch.empty((8, 2, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(pk.PagedKVError):
+        pk.pa_prefill_attention(out2, qbuf[1:].view(8, 2, 64), _dev(kc2), _dev(vc2), _dev(t2),
+                                _dev(c2), _dev(qs2), 0.1, desc2, max_q_len=8)
