@@ -721,6 +721,8 @@ def run_prefill(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.prefill_b256(seed=112 + rank)
+    if args.prompts:
+        w.prompt_lens = w.prompt_lens[:args.prompts]
     H, D, B = w.num_heads, w.head_dim, w.block_size
     lens = np.array(w.prompt_lens, np.int64)
     desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
@@ -805,8 +807,8 @@ def run_prefill(args):
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": "prompt phase of the mixed batch: 256 whole prompts, lognormal "
-                                   "(median 200, cap 1536), OPT-13B layer 40x128, block 16",
+            "config": {"workload": f"prompt phase of the mixed batch: {len(lens)} whole prompts, "
+                                   "lognormal (median 200, cap 1536), OPT-13B layer 40x128, block 16",
                        "prompt_tokens": T, "pool_blocks": w.num_blocks,
                        "l2": "K/V written and read back per step ~1.7 GB >> 129 MB L2, no flush"},
             "gpu_launches": 2 * args.steps,
@@ -919,6 +921,8 @@ def main():
                          "step; beam_churn: beam search with pruning; prefill: causal "
                          "prefill of the mixed batch's prompts")
     ap.add_argument("--beam", action="store_true", help="full_40l: beam groups sharing blocks")
+    ap.add_argument("--prompts", type=int, default=0,
+                    help="prefill: use only the first N prompts of the batch (small profiling case)")
     ap.add_argument("--dump-steps", default="",
                     help="write each warm-up and timed step's algorithmic attention bytes here")
     ap.add_argument("--partition", type=int, default=0,

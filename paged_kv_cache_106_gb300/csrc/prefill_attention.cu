@@ -7,36 +7,53 @@
 // tokens before it and itself, with the blockwise attention equation of the
 // PagedAttention notes (§3.1) evaluated for each of those queries.
 //
-// Kernel design (sm_103a, tensor cores through mma.sync m16n8k16):
-//   - one CTA = (sequence, head, tile of 64 consecutive queries); 4 warps,
-//     16 query rows each.  Later query tiles (more keys) are launched first.
-//   - keys and values stream through shared memory in tiles of 64 positions,
-//     double-buffered with 16-byte cp.async copies.  A row's physical address
-//     comes from the block table (block j / B, offset j % B); in the cache
-//     layout [block][head][B][D] each (block, head) run is B*D*2 contiguous
-//     bytes, so a tile is a handful of contiguous runs.  Rows are stored
-//     with the 16-byte chunks XOR-swizzled by (row % 8), so ldmatrix reads
-//     hit eight different bank groups.
-//   - S = Q K^T accumulates in fp32; the online softmax runs in base 2 on the
-//     accumulator fragments; P V uses P as the sum of two fp16 terms
-//     (hi = fp16(p), lo = fp16(p - hi)), which keeps the probabilities to
-//     about 22 bits so the fp16 output is limited by its own rounding.
+// Kernel design (sm_103a, 5th-generation tensor cores through tcgen05):
+//   - one CTA = (sequence, head, tile of 128 consecutive queries); later
+//     query tiles (more keys) are launched first.  Warp roles:
+//       warps 0-3  softmax: thread i owns query row i, i.e. tensor-memory
+//                  lane i, so row maxima and sums need no shuffles;
+//       warp 4     one thread issues every tcgen05.mma and commit;
+//       warps 5-6  gather K tiles, warps 7-8 the Q tile and V tiles.
+//   - keys and values stream through two 3-stage shared-memory rings in
+//     tiles of 128 positions.  Position j lives in block table[j / B] at
+//     offset j % B; in the cache layout [block][head][B][D] each (block,
+//     head) run is B*D*2 contiguous bytes.  For B >= 8 a lane per block
+//     issues one 2-D TMA copy per 64-column panel of the run (a tensor map
+//     over the cache's rows), which lands already in the 128-byte-swizzled
+//     layout the tensor cores read; for B = 4 the loader threads gather the
+//     same layout with 16-byte cp.async.  The same bytes are the K-major B
+//     operand of S = Q K^T and the MN-major B operand of O = P V.  Rows past
+//     the context in the last V tile are zeroed before the product.
+//   - tensor memory (512 columns): three 128-column S buffers, so Q K^T for
+//     tile t+2 runs while tile t is in softmax, and the fp32 output
+//     accumulator O (D columns).  Softmax overwrites its S buffer with P as
+//     fp16 pairs, which the P V product reads as its A operand straight from
+//     tensor memory.
+//   - the softmax is online, in base 2 (ex2.approx), with a lazy rescale: a row's
+//     reference maximum moves only when a tile raises it by more than 2^8,
+//     so O is rescaled in tensor memory rarely; P <= 2^8 stays exact enough
+//     in fp16.  P enters P V as hi + lo fp16 terms (hi = fp16(p),
+//     lo = fp16(p - hi)), keeping about 22 bits of each probability, so the
+//     fp16 rounding of the output dominates the error.
 //   - positions past the causal end of the tile are zero-filled, and scores
 //     of keys after a row's own position are masked to -inf.
+//   - every mbarrier wait is bounded; a wait that runs out reports
+//     PA_ERR_TIMEOUT, and the CTA drains its MMAs (bounded) and frees its
+//     tensor memory before it returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "tc_device.cuh"
 
 namespace pagedkv {
 namespace {
-
-constexpr int kBM = 64;        // queries per CTA
-constexpr int kBN = 64;        // key positions per tile
-constexpr int kThreads = 128;  // 4 warps x 16 query rows
 
 struct PrefillParams {
     __half *out;
@@ -51,12 +68,6 @@ struct PrefillParams {
     int32_t *status;
 };
 
-// Byte offset of 16-byte chunk c of row r in a swizzled [rows][D] fp16 tile.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return (uint32_t)(r * (D * 2) + ((c ^ (r & 7)) << 4));
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                  "r"(valid ? 16 : 0)
@@ -70,27 +81,36 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
+// 2^x by the PTX approximation instruction (relative error about 2^-22;
+// -inf gives +0).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// c += a (16x16, row) * b (16x8, col); fp16 operands, fp32 accumulators.
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
+// Barrier among `count` threads of the CTA (ids 1.. are free; 0 is
+// __syncthreads) that also returns whether `v` held for all of them.
+__device__ __forceinline__ bool group_all(int id, int count, bool v) {
+    uint32_t r;
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// 2-D tensor copy global -> shared (box of the tensor map at element
+// coordinates x, y); completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 // Two probabilities as fp16 pairs hi + lo (lower column in the low half).
@@ -101,22 +121,50 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uin
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-template <int D>
-constexpr int prefill_smem_bytes() {
-    return kBM * D * 2 + 4 * kBN * D * 2;  // Q tile + two K and two V tiles
-}
+constexpr int TBM = 128;          // queries per CTA (= tensor-memory lanes)
+constexpr int TBN = 128;          // key positions per tile
+constexpr int NST = 3;            // K / V ring stages and S buffers
+constexpr int kMmaWarp = 4, kKWarp0 = 5, kVWarp0 = 7;
+constexpr int kTcThreads = 288;   // 9 warps
+constexpr uint32_t kPanel = TBM * 128;   // bytes of one 64-column panel of a 128-row tile
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = NST * 128;    // output accumulator after the S buffers
+constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) paged_prefill_mma(const PrefillParams p) {
-    constexpr int CPR = D / 8;                 // 16-byte chunks per row
-    constexpr int RPP = kThreads / CPR;        // rows covered by one pass of the CTA
-    constexpr int NLD = kBN * CPR / kThreads;  // chunks per thread per tile
-    constexpr int TILE = kBN * D * 2;
-    static_assert(kBM == kBN && CPR >= 8 && kThreads % CPR == 0, "tile geometry");
-    extern __shared__ __align__(128) unsigned char smem[];
-    const uint32_t sQ = smem_addr(smem);
-    const uint32_t sK = sQ + kBM * D * 2;
-    const uint32_t sV = sK + 2 * TILE;
+struct TcLayout {
+    static constexpr uint32_t TILE = (D / 64) * kPanel;
+    static constexpr uint32_t Q = 0, K = TILE, V = K + NST * TILE, END = V + NST * TILE;
+    // at least 116 KB so that one CTA holds an SM (its 512 tensor-memory
+    // columns are the whole SM's), plus 1 KB to align the tiles to 1024 bytes
+    static constexpr uint32_t BYTES = (END > 116u * 1024u ? END : 116u * 1024u) + 1024u;
+};
+
+struct TcBars {
+    uint64_t q_full;
+    uint64_t k_full[NST], k_empty[NST], v_full[NST], v_empty[NST];
+    uint64_t s_full[NST], p_full[NST], pv_done[NST];
+    uint64_t done, v_raw;
+    uint32_t tmem;
+    int32_t tab[2][2][TBN / 4];   // per loader group, double-buffered block ids of a tile
+};
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+// TMA: K / V tiles arrive by 2-D tensor copies of whole (block, head) runs
+// (block sizes 8..32, whose runs start on 1024-byte boundaries of the
+// swizzle pattern); otherwise (block size 4) by 16-byte cp.async.
+template <int D, bool TMA>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_prefill_tc(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv) {
+    using L = TcLayout<D>;
+    constexpr int CPR = D / 8;        // 16-byte chunks per row
+    constexpr int RPP = 64 / CPR;     // rows one pass of a 64-thread loader group covers
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ TcBars bars;
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sQ = base + L::Q, sK = base + L::K, sV = base + L::V;
 
     const int s = blockIdx.z, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -130,220 +178,417 @@ __global__ void __launch_bounds__(kThreads, 2) paged_prefill_mma(const PrefillPa
             report(p.status, bad_len ? PA_ERR_INVALID_ARG : PA_ERR_BAD_BLOCK);
         return;
     }
-    const int q0 = (p.q_tiles - 1 - (int)blockIdx.x) * kBM;  // later tiles first
+    const int q0 = (p.q_tiles - 1 - (int)blockIdx.x) * TBM;  // later tiles first
     if (q0 >= ql) return;
+    const int pos0 = ctx - ql;                 // position of query 0 of the sequence
+    const int rows = min(TBM, ql - q0);
+    const int n_end = pos0 + q0 + rows;        // this tile needs keys [0, n_end)
+    const int n_tiles = (n_end + TBN - 1) / TBN;
 
-    const int pos0 = ctx - ql;                   // position of query 0 of the sequence
-    const int rows = min(kBM, ql - q0);
-    const int n_end = pos0 + q0 + rows;          // this tile needs keys [0, n_end)
-    const int n_tiles = (n_end + kBN - 1) / kBN;
-    const int B = 1 << p.bshift;
-    const int c = tid % CPR, r0 = tid / CPR;
-    const int32_t *table = p.tables + (size_t)s * p.max_blocks;
-
-    // Q tile: rows past the sequence's last query are zero-filled.
-    for (int i = 0; i < NLD; ++i) {
-        const int r = r0 + i * RPP;
-        const bool v = r < rows;
-        const __half *src = p.q + ((size_t)(q_beg + q0 + (v ? r : 0)) * p.num_heads + h) * D + c * 8;
-        cp_async16(sQ + swz<D>(r, c), src, v);
-    }
-    auto load_kv = [&](int t, int buf) {
-        const int n0 = t * kBN;
-        for (int i = 0; i < NLD; ++i) {
-            const int r = r0 + i * RPP;
-            const int j = n0 + r;
-            bool v = j < n_end;
-            size_t off = 0;
-            if (v) {
-                const int phys = __ldg(table + (j >> p.bshift));
-                if (phys < 0 || phys >= p.num_blocks) {
-                    report(p.status, PA_ERR_BAD_BLOCK);
-                    v = false;
-                } else {
-                    off = (((size_t)phys * p.num_heads + h) * B + (j & (B - 1))) * D + c * 8;
-                }
-            }
-            cp_async16(sK + buf * TILE + swz<D>(r, c), p.k_cache + off, v);
-            cp_async16(sV + buf * TILE + swz<D>(r, c), p.v_cache + off, v);
+    const uint32_t b_q = smem_addr(&bars.q_full), b_done = smem_addr(&bars.done);
+    auto bar = [](uint64_t *arr, int i) { return smem_addr(arr + i); };
+    if (tid == 0) {
+        mbar_init(b_q, 64);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(bar(bars.k_full, i), TMA ? 1 : 64);
+            mbar_init(bar(bars.v_full, i), TMA ? 1 : 64);
+            mbar_init(bar(bars.k_empty, i), 1);
+            mbar_init(bar(bars.v_empty, i), 1);
+            mbar_init(bar(bars.s_full, i), 1);
+            mbar_init(bar(bars.p_full, i), 128);
+            mbar_init(bar(bars.pv_done, i), 1);
         }
-        cp_async_commit();
-    };
-    load_kv(0, 0);  // one group: Q and the first key/value tile
-    cp_async_wait<0>();
+        mbar_init(b_done, 1);
+        mbar_init(smem_addr(&bars.v_raw), 1);
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) tc::alloc(smem_addr(&bars.tmem), kTmemCols);
+    tc::fence_before();
     __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = bars.tmem;
 
-    const int mi = lane >> 3;                   // ldmatrix: which 8x8 matrix this lane addresses
-    uint32_t qf[D / 16][4];
-    {
-        const int r = warp * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            ldsm_x4(sQ + swz<D>(r, 2 * kk + (mi >> 1)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-    }
-
-    const int g = lane >> 2, tq = lane & 3;
-    const int wq = q0 + warp * 16;               // first query of this warp
-    const bool active = wq < ql;
-    const int pos_r[2] = {pos0 + min(wq + g, ql - 1), pos0 + min(wq + g + 8, ql - 1)};
-    const int wpos_min = pos0 + min(wq, ql - 1);
-    const int wpos_max = pos0 + min(wq + 15, ql - 1);
-
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-
-    for (int t = 0; t < n_tiles; ++t) {
-        const int buf = t & 1;
-        if (t + 1 < n_tiles) {
-            load_kv(t + 1, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
+    if (warp >= kKWarp0) {
+        // ---- loaders: 64 threads gather K tiles, 64 gather the Q tile and V tiles
+        const bool is_k = warp < kVWarp0;
+        const int g = is_k ? 0 : 1;
+        const int lt = tid - (is_k ? kKWarp0 : kVWarp0) * 32;
+        const int c = lt % CPR, r0 = lt / CPR;
+        const int B = 1 << p.bshift;
+        const int32_t *table = p.tables + (size_t)s * p.max_blocks;
+        if (!is_k) {
+#pragma unroll 4
+            for (int r = r0; r < TBM; r += RPP) {
+                const bool v = r < rows;
+                const __half *src =
+                    p.q + ((size_t)(q_beg + q0 + (v ? r : 0)) * p.num_heads + h) * D + c * 8;
+                cp_async16(sQ + tc::sw128(TBM, r, c), src, v);
+            }
+            cp_async_commit();
             cp_async_wait<0>();
+            fence_proxy_async_smem();
+            mbar_arrive(b_q);
         }
-        __syncthreads();
-        const int n0 = t * kBN;
-        if (active && n0 <= wpos_max) {
-            // S = Q K^T for this warp's 16 rows and the tile's 64 keys
-            float sc[kBN / 8][4];
+        const uint32_t ring = is_k ? sK : sV;
+        uint64_t *full = is_k ? bars.k_full : bars.v_full;
+        uint64_t *empty = is_k ? bars.k_empty : bars.v_empty;
+        const int nb = TBN >> p.bshift;   // blocks per tile (tiles start on a block)
+        if constexpr (TMA) {
+            // One warp per group issues the tensor copies, lane i for block i
+            // of the tile; the V group's second warp helps zero the rows past
+            // the context in the last V tile.
+            const CUtensorMap *map = is_k ? &tmk : &tmv;
+            const uint32_t run_bytes = (uint32_t)B * 128u * (D / 64);
+            const uint32_t b_raw = smem_addr(&bars.v_raw);
+            bool dead = false;   // a wait ran out: issue nothing more, but still meet the group
+            for (int t = 0; t < n_tiles; ++t) {
+                const int st = t % NST;
+                const int n0 = t * TBN;
+                // rows past the context must read as zeros in V (0 * garbage
+                // could be NaN); only the last tile has such rows
+                const bool fix = !is_k && t == n_tiles - 1 && n_end - n0 < TBN;
+                if (lt < 32 && !dead) {
+                    const bool ok = warp_all(t < NST || mbar_wait_bounded(bar(empty, st),
+                                                                          ((t / NST) - 1) & 1,
+                                                                          p.status, true));
+                    if (!ok) report(p.status, PA_ERR_TIMEOUT);
+                    dead = !ok;
+                }
+                if (lt < 32 && !dead) {
+                    const int j = n0 + (lt << p.bshift);
+                    const bool valid = lt < nb && j < n_end;
+                    const int phys = valid ? __ldg(table + (j >> p.bshift)) : -1;
+                    const bool in_pool = valid && phys >= 0 && phys < p.num_blocks;
+                    if (valid && !in_pool) report(p.status, PA_ERR_BAD_BLOCK);
+                    const uint32_t n_runs = __popc(__ballot_sync(0xffffffffu, in_pool));
+                    const uint32_t tgt = fix ? b_raw : bar(full, st);
+                    if (lt == 0) mbar_arrive_expect_tx(tgt, n_runs * run_bytes);
+                    __syncwarp();
+                    if (in_pool) {
+                        const uint32_t dst = ring + st * L::TILE + (uint32_t)(lt << p.bshift) * 128u;
+                        const int y = (phys * p.num_heads + h) << p.bshift;
 #pragma unroll
-            for (int j = 0; j < kBN / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-            const uint32_t kb = sK + buf * TILE;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-                for (int jp = 0; jp < kBN / 16; ++jp) {
-                    const int r = jp * 16 + (mi >> 1) * 8 + (lane & 7);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kb + swz<D>(r, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-                    mma16816(sc[2 * jp], qf[kk], b0, b1);
-                    mma16816(sc[2 * jp + 1], qf[kk], b2, b3);
+                        for (int pn = 0; pn < D / 64; ++pn)
+                            tma_load_2d(dst + pn * kPanel, map, pn * 64, y, tgt);
+                    }
+                }
+                if (fix) {
+                    // both V warps: wait for the copies, zero rows [n_end - n0, TBN)
+                    const bool ok = mbar_wait_bounded(b_raw, 0, p.status, true);
+                    if (ok) {
+                        const int first = n_end - n0;
+                        const uint32_t span = (uint32_t)(TBN - first) * 128u;
+                        for (int pn = 0; pn < D / 64; ++pn) {
+                            const uint32_t z = ring + st * L::TILE + pn * kPanel + first * 128u;
+                            for (uint32_t o = (uint32_t)lt * 16u; o < span; o += 64u * 16u)
+                                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(z + o),
+                                             "r"(0)
+                                             : "memory");
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    if (group_all(2, 64, ok)) {
+                        if (lt == 0) mbar_arrive(bar(full, st));
+                    } else {
+                        report(p.status, PA_ERR_TIMEOUT);
+                    }
                 }
             }
-            // online softmax, base 2
-            const bool mask = n0 + kBN - 1 > wpos_min;
-            float mt[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int j = 0; j < kBN / 8; ++j) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float x = sc[j][e] * p.qscale;
-                    if (mask && n0 + 8 * j + 2 * tq + (e & 1) > pos_r[e >> 1]) x = -INFINITY;
-                    sc[j][e] = x;
-                    mt[e >> 1] = fmaxf(mt[e >> 1], x);
+        } else {
+            const __half *cache = is_k ? p.k_cache : p.v_cache;
+            // Tile t is issued before tile t-1 is waited for, so two tiles of
+            // copies are in flight per thread.
+            int t = 0;
+            for (; t < n_tiles; ++t) {
+                const int st = t % NST;
+                const int n0 = t * TBN;
+                int32_t *tab = bars.tab[g][t & 1];
+                if (lt < nb) {   // the tile's physical block ids, read once by the group
+                    const int j = n0 + (lt << p.bshift);
+                    tab[lt] = j < n_end ? __ldg(table + (j >> p.bshift)) : -1;
+                }
+                const bool free_ok =
+                    t < NST || mbar_wait_bounded(bar(empty, st), ((t / NST) - 1) & 1, p.status, true);
+                // one decision for the whole group, and the block ids visible to it
+                if (!group_all(1 + g, 64, free_ok)) {
+                    report(p.status, PA_ERR_TIMEOUT);
+                    break;
+                }
+                const uint32_t dst = ring + st * L::TILE;
+#pragma unroll 4
+                for (int r = r0; r < TBN; r += RPP) {
+                    const int j = n0 + r;
+                    const int phys = tab[r >> p.bshift];
+                    bool v = j < n_end;
+                    size_t off = 0;
+                    if (v) {
+                        if (phys < 0 || phys >= p.num_blocks) {
+                            report(p.status, PA_ERR_BAD_BLOCK);
+                            v = false;
+                        } else {
+                            off = (((size_t)phys * p.num_heads + h) * B + (j & (B - 1))) * D + c * 8;
+                        }
+                    }
+                    cp_async16(dst + tc::sw128(TBN, r, c), cache + off, v);
+                }
+                cp_async_commit();
+                if (t > 0) {
+                    cp_async_wait<1>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(full, (t - 1) % NST));
                 }
             }
-            float corr[2], ls[2] = {0.f, 0.f};
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                mt[rr] = fmaxf(mt[rr], __shfl_xor_sync(0xffffffffu, mt[rr], 1));
-                mt[rr] = fmaxf(mt[rr], __shfl_xor_sync(0xffffffffu, mt[rr], 2));
-                const float mn = fmaxf(m_run[rr], mt[rr]);  // finite: key 0 is in tile 0
-                corr[rr] = exp2f(m_run[rr] - mn);
-                m_run[rr] = mn;
-            }
-#pragma unroll
-            for (int j = 0; j < kBN / 8; ++j) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float pe = exp2f(sc[j][e] - m_run[e >> 1]);
-                    sc[j][e] = pe;
-                    ls[e >> 1] += pe;
-                }
-            }
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) l_run[rr] = l_run[rr] * corr[rr] + ls[rr];
-#pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                o[i][0] *= corr[0];
-                o[i][1] *= corr[0];
-                o[i][2] *= corr[1];
-                o[i][3] *= corr[1];
-            }
-            // O += P V, P as hi + lo fp16 operands
-            const uint32_t vb = sV + buf * TILE;
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-                uint32_t ah[4], al[4];
-                split_pair(sc[2 * kk][0], sc[2 * kk][1], ah[0], al[0]);
-                split_pair(sc[2 * kk][2], sc[2 * kk][3], ah[1], al[1]);
-                split_pair(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ah[2], al[2]);
-                split_pair(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ah[3], al[3]);
-                const int r = kk * 16 + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vb + swz<D>(r, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-                    mma16816(o[2 * dp], ah, b0, b1);
-                    mma16816(o[2 * dp], al, b0, b1);
-                    mma16816(o[2 * dp + 1], ah, b2, b3);
-                    mma16816(o[2 * dp + 1], al, b2, b3);
-                }
+            cp_async_wait<0>();
+            if (t == n_tiles && n_tiles > 0) {
+                fence_proxy_async_smem();
+                mbar_arrive(bar(full, (n_tiles - 1) % NST));
             }
         }
-        __syncthreads();  // every warp is done with buffer `buf` before it is refilled
+    } else if (warp == kMmaWarp) {
+        // ---- one thread issues the MMAs
+        if (lane == 0) {
+            constexpr uint32_t idS = tc::idesc_f16(TBM, TBN, false);
+            constexpr uint32_t idO = tc::idesc_f16(TBM, D, true);
+            auto issue_s = [&](int t) -> bool {
+                const int st = t % NST;
+                if (!mbar_wait_bounded(bar(bars.k_full, st), (t / NST) & 1, p.status, true))
+                    return false;
+                tc::fence_after();
+                const uint32_t kb = sK + st * L::TILE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+                    tc::mma_ss(tmem + st * 128, tc::smem_desc(sQ + off, 16, 1024),
+                               tc::smem_desc(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(bar(bars.s_full, st));
+                tc::commit(bar(bars.k_empty, st));
+                return true;
+            };
+            bool ok = mbar_wait_bounded(b_q, 0, p.status, true);
+            if (ok) ok = issue_s(0);
+            if (ok && n_tiles > 1) ok = issue_s(1);
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                const int b = t % NST;
+                const uint32_t par = (t / NST) & 1;
+                ok = mbar_wait_bounded(bar(bars.p_full, b), par, p.status, true) &&
+                     mbar_wait_bounded(bar(bars.v_full, b), par, p.status, true);
+                if (!ok) break;
+                tc::fence_after();
+                const uint32_t vb = sV + b * L::TILE;
+#pragma unroll
+                for (int kk = 0; kk < TBN / 16; ++kk) {
+                    const uint64_t dv = tc::smem_desc(vb + kk * 2048, kPanel, 1024);
+                    const uint32_t pa = tmem + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+                    tc::mma_ts(tmem + kOCol, pa, dv, idO, (t > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_ts(tmem + kOCol, pa + 16, dv, idO, 1u);
+                }
+                tc::commit(bar(bars.v_empty, b));
+                tc::commit(bar(bars.pv_done, b));
+                if (t + 2 < n_tiles) {
+                    // S(t+2) goes to the buffer whose P the product of tile t-1 read
+                    if (t >= 1)
+                        ok = mbar_wait_bounded(bar(bars.pv_done, (t - 1) % NST),
+                                               ((t - 1) / NST) & 1, p.status, true);
+                    if (ok) ok = issue_s(t + 2);
+                }
+            }
+            if (!ok) report(p.status, PA_ERR_TIMEOUT);
+            tc::commit(b_done);   // lets the teardown wait for every MMA issued
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax warps: thread tid owns query row tid
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int qi = q0 + tid;
+        const bool valid = qi < ql;
+        const int pos = pos0 + min(qi, ql - 1);
+        const float qs = p.qscale;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int b = t % NST;
+            ok = warp_all(mbar_wait_bounded(bar(bars.s_full, b), (t / NST) & 1, p.status, true));
+            if (!ok) break;
+            tc::fence_after();
+            const uint32_t sb = lane_base + b * 128;
+            const int n0 = t * TBN;
+            // keys past this row's position are masked: key n0 + 32 cc + i with i > lim
+            const bool need_mask = n0 + TBN - 1 > pos0 + q0;
+            float mt = -INFINITY;
+#pragma unroll 1
+            for (int cc = 0; cc < TBN / 32; ++cc) {
+                uint32_t r[32];
+                tc::ld32(sb + cc * 32, r);
+                tc::wait_ld();
+                const int lim = need_mask ? pos - (n0 + cc * 32) : 1 << 30;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float x = i > lim ? -INFINITY : __uint_as_float(r[i]) * qs;
+                    m4[i & 3] = fmaxf(m4[i & 3], x);
+                }
+                mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+            }
+            float corr = 1.f;
+            const bool resc = mt > m_run + kRescaleLog2;
+            if (resc) {
+                corr = ex2(m_run - mt);
+                m_run = mt;
+                l_run *= corr;
+            }
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int cc = 0; cc < TBN / 32; ++cc) {
+                uint32_t r[32], w[32];
+                tc::ld32(sb + cc * 32, r);
+                tc::wait_ld();
+                const int lim = need_mask ? pos - (n0 + cc * 32) : 1 << 30;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float x0 = 2 * i > lim ? -INFINITY
+                                                 : fmaf(__uint_as_float(r[2 * i]), qs, -m_run);
+                    const float x1 = 2 * i + 1 > lim
+                                         ? -INFINITY
+                                         : fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    ls[i & 3] += p0 + p1;
+                    split_pair(p0, p1, w[i], w[16 + i]);
+                }
+                tc::st32(sb + cc * 32, w);
+            }
+            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            tc::wait_st();
+            if (__any_sync(0xffffffffu, resc && t > 0)) {
+                // O holds tiles < t: wait until their product is complete, then scale
+                ok = warp_all(mbar_wait_bounded(bar(bars.pv_done, (t - 1) % NST),
+                                                ((t - 1) / NST) & 1, p.status, true));
+                if (!ok) break;
+                tc::fence_after();
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    tc::ld32(lane_base + kOCol + cc * 32, r);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                    tc::st32(lane_base + kOCol + cc * 32, r);
+                }
+                tc::wait_st();
+            }
+            tc::fence_before();
+            mbar_arrive(bar(bars.p_full, b));
+        }
+        if (ok)
+            ok = warp_all(mbar_wait_bounded(bar(bars.pv_done, (n_tiles - 1) % NST),
+                                            ((n_tiles - 1) / NST) & 1, p.status, true));
+        if (ok) {
+            tc::fence_after();
+            const float inv = 1.f / l_run;
+            __half *dst = p.out + ((size_t)(q_beg + (valid ? qi : q0)) * p.num_heads + h) * D;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t r[32];
+                tc::ld32(lane_base + kOCol + cc * 32, r);
+                tc::wait_ld();
+                if (valid) {
+                    uint32_t hv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const __half2 v2 = __floats2half2_rn(__uint_as_float(r[2 * i]) * inv,
+                                                             __uint_as_float(r[2 * i + 1]) * inv);
+                        hv[i] = *reinterpret_cast<const uint32_t *>(&v2);
+                    }
+                    uint4 *o4 = reinterpret_cast<uint4 *>(dst + cc * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        o4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+                }
+            }
+        } else {
+            report(p.status, PA_ERR_TIMEOUT);
+        }
     }
 
-    // Normalise, stage the warp's rows in its own part of the Q tile, then
-    // store them as 16-byte vectors.
-    if (!active) return;
-    float inv[2];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-        float l = l_run[rr];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        inv[rr] = 1.f / l;
-    }
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-        const __half2 a = __floats2half2_rn(o[i][0] * inv[0], o[i][1] * inv[0]);
-        const __half2 b = __floats2half2_rn(o[i][2] * inv[1], o[i][3] * inv[1]);
-        const int ra = warp * 16 + g, rb = ra + 8;
-        asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(sQ + swz<D>(ra, i) + 4 * tq),
-                     "r"(*reinterpret_cast<const uint32_t *>(&a))
-                     : "memory");
-        asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(sQ + swz<D>(rb, i) + 4 * tq),
-                     "r"(*reinterpret_cast<const uint32_t *>(&b))
-                     : "memory");
-    }
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < 16 * CPR / 32; ++i) {
-        const int idx = lane + 32 * i;
-        const int r = idx / CPR, cc = idx % CPR;
-        if (wq + r < ql) {
-            uint4 val;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(sQ + swz<D>(warp * 16 + r, cc)));
-            *reinterpret_cast<uint4 *>(p.out + ((size_t)(q_beg + wq + r) * p.num_heads + h) * D +
-                                       cc * 8) = val;
-        }
+    // ---- teardown: every MMA drained (bounded), then tensor memory freed
+    tc::fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        if (lane == 0 && !mbar_wait_bounded(b_done, 0, p.status, false))
+            report(p.status, PA_ERR_TIMEOUT);
+        __syncwarp();
+        tc::fence_after();
+        tc::dealloc(tmem, kTmemCols);
     }
 }
 
-template <int D>
+template <int D, bool TMA>
 cudaError_t set_prefill_smem_once() {
     static std::once_flag once[64];
     static cudaError_t err[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [&] {
-        err[dev] = cudaFuncSetAttribute(paged_prefill_mma<D>,
+        err[dev] = cudaFuncSetAttribute(paged_prefill_tc<D, TMA>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        prefill_smem_bytes<D>());
+                                        (int)TcLayout<D>::BYTES);
     });
     return err[dev];
 }
 
-template <int D>
-int launch_d(const PrefillParams &p, int n_seqs, cudaStream_t st) {
-    cudaError_t e = set_prefill_smem_once<D>();
-    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library does not link the driver library itself).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// One layer's cache seen as a 2-D fp16 tensor of num_blocks*H*B rows of D
+// values; a box is 64 values (one 128-byte swizzle row) by B rows, i.e. one
+// (block, head) run of one 64-column panel.
+int encode_cache_map(CUtensorMap *m, const void *cache, const pa_pool_desc *d) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail(PA_ERR_CUDA, "pa_prefill_attention: cuTensorMapEncodeTiled unavailable");
+    const uint64_t rows = (uint64_t)d->num_blocks * d->num_heads * d->block_size;
+    cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)(rows ? rows : 1)};
+    cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)d->block_size};
+    cuuint32_t elem[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(cache), dims,
+                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_CUDA, "pa_prefill_attention: cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return PA_OK;
+}
+
+template <int D, bool TMA>
+int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st) {
+    cudaError_t e = set_prefill_smem_once<D, TMA>();
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
+    CUtensorMap tmk, tmv;
+    std::memset(&tmk, 0, sizeof tmk);
+    std::memset(&tmv, 0, sizeof tmv);
+    if (TMA) {
+        int rc = encode_cache_map(&tmk, p.k_cache, d);
+        if (rc == PA_OK) rc = encode_cache_map(&tmv, p.v_cache, d);
+        if (rc != PA_OK) return rc;
+    }
+    p.q_tiles = (p.max_q_len + TBM - 1) / TBM;
     const dim3 grid((unsigned)p.q_tiles, (unsigned)p.num_heads, (unsigned)n_seqs);
-    paged_prefill_mma<D><<<grid, kThreads, prefill_smem_bytes<D>(), st>>>(p);
+    paged_prefill_tc<D, TMA><<<grid, kTcThreads, TcLayout<D>::BYTES, st>>>(p, tmk, tmv);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PA_OK;
@@ -386,12 +631,15 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     p.num_blocks = d->num_blocks;
     p.max_blocks = max_blocks;
     p.max_q_len = max_q_len;
-    p.q_tiles = (max_q_len + kBM - 1) / kBM;
+    p.q_tiles = 0;   // set by the launcher from its tile height
     p.bshift = bshift;
     p.qscale = scale * 1.4426950408889634f;
     p.status = status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return d->head_dim == 64 ? launch_d<64>(p, n_seqs, st) : launch_d<128>(p, n_seqs, st);
+    const bool tma = d->block_size >= 8;
+    if (d->head_dim == 64)
+        return tma ? launch_d<64, true>(p, n_seqs, d, st) : launch_d<64, false>(p, n_seqs, d, st);
+    return tma ? launch_d<128, true>(p, n_seqs, d, st) : launch_d<128, false>(p, n_seqs, d, st);
 }
 
 }  // namespace pagedkv
