@@ -341,13 +341,15 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
  *   ctx_lens      [n_seqs] int32
  *   q_starts      [n_seqs + 1] int32, non-decreasing
  *   max_q_len     host bound on every q_len (sizes the launch)
+ *   scale         finite and > 0 (1/sqrt(head_dim) in the pages)
  * head_dim 64 or 128, block_size 4..32.  Tensor cores: fp16 products, fp32
  * accumulation; the probabilities enter the second product as the sum of two
  * fp16 terms, so the fp16 rounding of the output dominates the error.
  * Device-side problems go to *status and leave that sequence's rows
  * unwritten: PA_ERR_INVALID_ARG for q_len < 0, q_len > ctx or
  * q_len > max_q_len; PA_ERR_BAD_BLOCK for ctx > max_blocks * B or a table
- * entry outside the pool (that key / value is then read as zeros).
+ * entry outside the pool (that entry is not read and the sequence's output
+ * is unspecified).
  * Errors: PA_ERR_INVALID_ARG (geometry, sizes, NULL or misaligned
  * pointers), PA_ERR_CUDA. */
 int pa_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,

@@ -10,11 +10,13 @@
 // Kernel design (sm_103a, 5th-generation tensor cores through tcgen05):
 //   - one CTA = (sequence, head, tile of 128 consecutive queries); later
 //     query tiles (more keys) are launched first.  Warp roles:
-//       warps 0-3  softmax: thread i owns query row i, i.e. tensor-memory
-//                  lane i, so row maxima and sums need no shuffles;
-//       warp 4     one thread issues every tcgen05.mma and commit;
-//       warps 5-6  gather K tiles, warps 7-8 the Q tile and V tiles.
-//   - keys and values stream through two 3-stage shared-memory rings in
+//       warps 0-7  softmax: query row i is tensor-memory lane i; warps w and
+//                  w + 4 share the 32 rows of lane quarter w % 4, each taking
+//                  half of a tile's key columns, and meet once per tile to
+//                  combine their row maxima;
+//       warp 8     one thread issues every tcgen05.mma and commit;
+//       warps 9-10 gather K tiles, warps 11-12 the Q tile and V tiles.
+//   - keys and values stream through shared-memory rings (3 K stages, 2 V) in
 //     tiles of 128 positions.  Position j lives in block table[j / B] at
 //     offset j % B; in the cache layout [block][head][B][D] each (block,
 //     head) run is B*D*2 contiguous bytes.  For B >= 8 a lane per block
@@ -37,6 +39,8 @@
 //     fp16 rounding of the output dominates the error.
 //   - positions past the causal end of the tile are zero-filled, and scores
 //     of keys after a row's own position are masked to -inf.
+//   - the epilogue stages each row half as fp16 in shared memory and writes
+//     it with one bulk copy (rows of a head are H*D*2 bytes apart in out).
 //   - every mbarrier wait is bounded; a wait that runs out reports
 //     PA_ERR_TIMEOUT, and the CTA drains its MMAs (bounded) and frees its
 //     tensor memory before it returns.
@@ -45,6 +49,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -114,18 +119,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 }
 
 // Two probabilities as fp16 pairs hi + lo (lower column in the low half).
+// hi is p rounded to fp16's 11 significant bits by integer arithmetic (exact
+// in fp16 for p >= 2^-14), so only the two packing conversions use the
+// conversion pipe; lo = p - hi is exact in fp32.  hi + lo carries p to about
+// 2^-22 relative, or to fp16's subnormal spacing (2^-24) for tiny p.
 __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uint32_t &lo) {
-    const __half2 h = __floats2half2_rn(p0, p1);
-    const __half2 l = __floats2half2_rn(p0 - __low2float(h), p1 - __high2float(h));
+    const float h0 = __uint_as_float((__float_as_uint(p0) + 0x1000u) & 0xFFFFE000u);
+    const float h1 = __uint_as_float((__float_as_uint(p1) + 0x1000u) & 0xFFFFE000u);
+    const __half2 h = __floats2half2_rn(h0, h1);
+    const __half2 l = __floats2half2_rn(p0 - h0, p1 - h1);
     hi = *reinterpret_cast<const uint32_t *>(&h);
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
 constexpr int TBM = 128;          // queries per CTA (= tensor-memory lanes)
 constexpr int TBN = 128;          // key positions per tile
-constexpr int NST = 3;            // K / V ring stages and S buffers
-constexpr int kMmaWarp = 4, kKWarp0 = 5, kVWarp0 = 7;
-constexpr int kTcThreads = 288;   // 9 warps
+constexpr int NST = 3;            // K ring stages and S buffers
+constexpr int NSV = 2;            // V ring stages
+constexpr int kMmaWarp = 8, kKWarp0 = 9, kVWarp0 = 11;
+constexpr int kTcThreads = 416;   // 13 warps
 constexpr uint32_t kPanel = TBM * 128;   // bytes of one 64-column panel of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = NST * 128;    // output accumulator after the S buffers
@@ -134,7 +146,8 @@ constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 template <int D>
 struct TcLayout {
     static constexpr uint32_t TILE = (D / 64) * kPanel;
-    static constexpr uint32_t Q = 0, K = TILE, V = K + NST * TILE, END = V + NST * TILE;
+    static constexpr uint32_t Q = 0, K = TILE, V = K + NST * TILE, END = V + NSV * TILE;
+    static constexpr uint32_t OUT_STRIDE = D * 2 + 16;   // output staging rows (in the K ring)
     // at least 116 KB so that one CTA holds an SM (its 512 tensor-memory
     // columns are the whole SM's), plus 1 KB to align the tiles to 1024 bytes
     static constexpr uint32_t BYTES = (END > 116u * 1024u ? END : 116u * 1024u) + 1024u;
@@ -142,11 +155,12 @@ struct TcLayout {
 
 struct TcBars {
     uint64_t q_full;
-    uint64_t k_full[NST], k_empty[NST], v_full[NST], v_empty[NST];
+    uint64_t k_full[NST], k_empty[NST], v_full[NSV], v_empty[NSV];
     uint64_t s_full[NST], p_full[NST], pv_done[NST];
     uint64_t done, v_raw;
     uint32_t tmem;
     int32_t tab[2][2][TBN / 4];   // per loader group, double-buffered block ids of a tile
+    float red[2][2][TBM];         // per tile parity and column half: row maxima, then sums
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
@@ -191,12 +205,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(b_q, 64);
         for (int i = 0; i < NST; ++i) {
             mbar_init(bar(bars.k_full, i), TMA ? 1 : 64);
-            mbar_init(bar(bars.v_full, i), TMA ? 1 : 64);
             mbar_init(bar(bars.k_empty, i), 1);
-            mbar_init(bar(bars.v_empty, i), 1);
             mbar_init(bar(bars.s_full, i), 1);
-            mbar_init(bar(bars.p_full, i), 128);
+            mbar_init(bar(bars.p_full, i), 256);
             mbar_init(bar(bars.pv_done, i), 1);
+        }
+        for (int i = 0; i < NSV; ++i) {
+            mbar_init(bar(bars.v_full, i), TMA ? 1 : 64);
+            mbar_init(bar(bars.v_empty, i), 1);
         }
         mbar_init(b_done, 1);
         mbar_init(smem_addr(&bars.v_raw), 1);
@@ -233,6 +249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint64_t *full = is_k ? bars.k_full : bars.v_full;
         uint64_t *empty = is_k ? bars.k_empty : bars.v_empty;
         const int nb = TBN >> p.bshift;   // blocks per tile (tiles start on a block)
+        const int NS = is_k ? NST : NSV;   // ring stages of this group
         if constexpr (TMA) {
             // One warp per group issues the tensor copies, lane i for block i
             // of the tile; the V group's second warp helps zero the rows past
@@ -242,15 +259,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t b_raw = smem_addr(&bars.v_raw);
             bool dead = false;   // a wait ran out: issue nothing more, but still meet the group
             for (int t = 0; t < n_tiles; ++t) {
-                const int st = t % NST;
+                const int st = t % NS;
                 const int n0 = t * TBN;
                 // rows past the context must read as zeros in V (0 * garbage
                 // could be NaN); only the last tile has such rows
                 const bool fix = !is_k && t == n_tiles - 1 && n_end - n0 < TBN;
                 if (lt < 32 && !dead) {
-                    const bool ok = warp_all(t < NST || mbar_wait_bounded(bar(empty, st),
-                                                                          ((t / NST) - 1) & 1,
-                                                                          p.status, true));
+                    const bool ok = warp_all(t < NS || mbar_wait_bounded(bar(empty, st),
+                                                                         ((t / NS) - 1) & 1,
+                                                                         p.status, true));
                     if (!ok) report(p.status, PA_ERR_TIMEOUT);
                     dead = !ok;
                 }
@@ -300,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // copies are in flight per thread.
             int t = 0;
             for (; t < n_tiles; ++t) {
-                const int st = t % NST;
+                const int st = t % NS;
                 const int n0 = t * TBN;
                 int32_t *tab = bars.tab[g][t & 1];
                 if (lt < nb) {   // the tile's physical block ids, read once by the group
@@ -308,7 +325,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tab[lt] = j < n_end ? __ldg(table + (j >> p.bshift)) : -1;
                 }
                 const bool free_ok =
-                    t < NST || mbar_wait_bounded(bar(empty, st), ((t / NST) - 1) & 1, p.status, true);
+                    t < NS || mbar_wait_bounded(bar(empty, st), ((t / NS) - 1) & 1, p.status, true);
                 // one decision for the whole group, and the block ids visible to it
                 if (!group_all(1 + g, 64, free_ok)) {
                     report(p.status, PA_ERR_TIMEOUT);
@@ -335,13 +352,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (t > 0) {
                     cp_async_wait<1>();
                     fence_proxy_async_smem();
-                    mbar_arrive(bar(full, (t - 1) % NST));
+                    mbar_arrive(bar(full, (t - 1) % NS));
                 }
             }
             cp_async_wait<0>();
             if (t == n_tiles && n_tiles > 0) {
                 fence_proxy_async_smem();
-                mbar_arrive(bar(full, (n_tiles - 1) % NST));
+                mbar_arrive(bar(full, (n_tiles - 1) % NS));
             }
         }
     } else if (warp == kMmaWarp) {
@@ -369,13 +386,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (ok) ok = issue_s(0);
             if (ok && n_tiles > 1) ok = issue_s(1);
             for (int t = 0; ok && t < n_tiles; ++t) {
-                const int b = t % NST;
-                const uint32_t par = (t / NST) & 1;
-                ok = mbar_wait_bounded(bar(bars.p_full, b), par, p.status, true) &&
-                     mbar_wait_bounded(bar(bars.v_full, b), par, p.status, true);
+                const int b = t % NST, bv = t % NSV;
+                ok = mbar_wait_bounded(bar(bars.p_full, b), (t / NST) & 1, p.status, true) &&
+                     mbar_wait_bounded(bar(bars.v_full, bv), (t / NSV) & 1, p.status, true);
                 if (!ok) break;
                 tc::fence_after();
-                const uint32_t vb = sV + b * L::TILE;
+                const uint32_t vb = sV + bv * L::TILE;
 #pragma unroll
                 for (int kk = 0; kk < TBN / 16; ++kk) {
                     const uint64_t dv = tc::smem_desc(vb + kk * 2048, kPanel, 1024);
@@ -383,7 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::mma_ts(tmem + kOCol, pa, dv, idO, (t > 0 || kk > 0) ? 1u : 0u);
                     tc::mma_ts(tmem + kOCol, pa + 16, dv, idO, 1u);
                 }
-                tc::commit(bar(bars.v_empty, b));
+                tc::commit(bar(bars.v_empty, bv));
                 tc::commit(bar(bars.pv_done, b));
                 if (t + 2 < n_tiles) {
                     // S(t+2) goes to the buffer whose P the product of tile t-1 read
@@ -398,9 +414,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- softmax warps: thread tid owns query row tid
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        const int qi = q0 + tid;
+        // ---- softmax warps: warps w and w + 4 share the query rows of tensor-memory
+        // lane quarter w % 4 (row = lane of that quarter); warp w < 4 takes key
+        // columns 0-63 of each tile, warp w + 4 columns 64-127
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int qi = q0 + row;
         const bool valid = qi < ql;
         const int pos = pos0 + min(qi, ql - 1);
         const float qs = p.qscale;
@@ -408,28 +428,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
             const int b = t % NST;
-            ok = warp_all(mbar_wait_bounded(bar(bars.s_full, b), (t / NST) & 1, p.status, true));
-            if (!ok) break;
-            tc::fence_after();
-            const uint32_t sb = lane_base + b * 128;
-            const int n0 = t * TBN;
+            ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, b), (t / NST) & 1, p.status, true));
+            const uint32_t sb = lane_base + b * 128 + half * 64;
+            const int n0 = t * TBN + half * 64;   // first key of this warp's columns
             // keys past this row's position are masked: key n0 + 32 cc + i with i > lim
-            const bool need_mask = n0 + TBN - 1 > pos0 + q0;
+            const bool need_mask = n0 + 63 > pos0 + q0;
             float mt = -INFINITY;
+            if (ok) {
+                tc::fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < TBN / 32; ++cc) {
-                uint32_t r[32];
-                tc::ld32(sb + cc * 32, r);
-                tc::wait_ld();
-                const int lim = need_mask ? pos - (n0 + cc * 32) : 1 << 30;
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t r[32];
+                    tc::ld32(sb + cc * 32, r);
+                    tc::wait_ld();
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    if (need_mask) {
+                        const int lim = pos - (n0 + cc * 32);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float x = i > lim ? -INFINITY : __uint_as_float(r[i]) * qs;
-                    m4[i & 3] = fmaxf(m4[i & 3], x);
+                        for (int i = 0; i < 32; ++i)
+                            m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
+                    }
+                    mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 }
-                mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                mt *= qs;   // scale > 0: the maximum of the scaled scores
             }
+            bars.red[t & 1][half][row] = mt;
+            // the two halves of each row meet here once per tile: one exit
+            // decision for all softmax warps, and the partner's maximum
+            if (!group_all(3, 256, ok)) {
+                ok = false;
+                break;
+            }
+            mt = fmaxf(mt, bars.red[t & 1][half ^ 1][row]);
             float corr = 1.f;
             const bool resc = mt > m_run + kRescaleLog2;
             if (resc) {
@@ -439,43 +472,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-            for (int cc = 0; cc < TBN / 32; ++cc) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t r[32], w[32];
                 tc::ld32(sb + cc * 32, r);
                 tc::wait_ld();
-                const int lim = need_mask ? pos - (n0 + cc * 32) : 1 << 30;
+                if (need_mask) {
+                    const int lim = pos - (n0 + cc * 32);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float x0 = 2 * i > lim ? -INFINITY
-                                                 : fmaf(__uint_as_float(r[2 * i]), qs, -m_run);
-                    const float x1 = 2 * i + 1 > lim
-                                         ? -INFINITY
-                                         : fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    ls[i & 3] += p0 + p1;
-                    split_pair(p0, p1, w[i], w[16 + i]);
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = 2 * i > lim ? 0.f : ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
+                        const float p1 =
+                            2 * i + 1 > lim ? 0.f : ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
+                        ls[i & 3] += p0 + p1;
+                        split_pair(p0, p1, w[i], w[16 + i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
+                        const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
+                        ls[i & 3] += p0 + p1;
+                        split_pair(p0, p1, w[i], w[16 + i]);
+                    }
                 }
                 tc::st32(sb + cc * 32, w);
             }
             l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             tc::wait_st();
             if (__any_sync(0xffffffffu, resc && t > 0)) {
-                // O holds tiles < t: wait until their product is complete, then scale
-                ok = warp_all(mbar_wait_bounded(bar(bars.pv_done, (t - 1) % NST),
-                                                ((t - 1) / NST) & 1, p.status, true));
-                if (!ok) break;
-                tc::fence_after();
+                // O holds tiles < t: wait until their product is complete, then
+                // scale this warp's half of the output columns
+                if (warp_all(mbar_wait_bounded(bar(bars.pv_done, (t - 1) % NST),
+                                               ((t - 1) / NST) & 1, p.status, true))) {
+                    tc::fence_after();
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tc::ld32(lane_base + kOCol + cc * 32, r);
-                    tc::wait_ld();
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        const uint32_t oc = lane_base + kOCol + half * (D / 2) + cc * 32;
+                        uint32_t r[32];
+                        tc::ld32(oc, r);
+                        tc::wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-                    tc::st32(lane_base + kOCol + cc * 32, r);
+                        for (int i = 0; i < 32; ++i)
+                            r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                        tc::st32(oc, r);
+                    }
+                    tc::wait_st();
+                } else {
+                    ok = false;   // every softmax warp leaves at the next meeting
                 }
-                tc::wait_st();
             }
             tc::fence_before();
             mbar_arrive(bar(bars.p_full, b));
@@ -483,28 +527,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok)
             ok = warp_all(mbar_wait_bounded(bar(bars.pv_done, (n_tiles - 1) % NST),
                                             ((n_tiles - 1) / NST) & 1, p.status, true));
-        if (ok) {
+        bars.red[n_tiles & 1][half][row] = l_run;
+        if (group_all(3, 256, ok)) {
+            // this warp's half of the row: normalise, stage as fp16 in the
+            // (now idle) K ring, store with one bulk copy per row half
             tc::fence_after();
-            const float inv = 1.f / l_run;
-            __half *dst = p.out + ((size_t)(q_beg + (valid ? qi : q0)) * p.num_heads + h) * D;
+            const float inv = 1.f / (l_run + bars.red[n_tiles & 1][half ^ 1][row]);
+            const uint32_t stage = sK + (uint32_t)row * L::OUT_STRIDE + half * D;
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t r[32];
-                tc::ld32(lane_base + kOCol + cc * 32, r);
+                tc::ld32(lane_base + kOCol + half * (D / 2) + cc * 32, r);
                 tc::wait_ld();
-                if (valid) {
-                    uint32_t hv[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const __half2 v2 = __floats2half2_rn(__uint_as_float(r[2 * i]) * inv,
-                                                             __uint_as_float(r[2 * i + 1]) * inv);
-                        hv[i] = *reinterpret_cast<const uint32_t *>(&v2);
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t hv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __half2 v2 = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * k]) * inv,
+                                                             __uint_as_float(r[8 * i + 2 * k + 1]) * inv);
+                        hv[k] = *reinterpret_cast<const uint32_t *>(&v2);
                     }
-                    uint4 *o4 = reinterpret_cast<uint4 *>(dst + cc * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        o4[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     stage + cc * 64 + i * 16),
+                                 "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
+                                 : "memory");
                 }
+            }
+            fence_proxy_async_smem();
+            if (valid) {
+                __half *dst = p.out + ((size_t)(q_beg + qi) * p.num_heads + h) * D + half * (D / 2);
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                             "r"(stage), "r"(D)
+                             : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             }
         } else {
             report(p.status, PA_ERR_TIMEOUT);
@@ -617,6 +674,8 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     if (((uintptr_t)out | (uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: out, q and caches must be 16-byte aligned");
     if (max_blocks < 1) return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: max_blocks < 1");
+    if (!(scale > 0.f) || !std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: scale must be finite and > 0");
     int bshift = 0;
     while ((1 << bshift) < d->block_size) ++bshift;
     PrefillParams p;

@@ -302,3 +302,8 @@ def test_prefill_host_side_refusals():
     with pytest.raises(pk.PagedKVError):
         pk.pa_prefill_attention(out2, qbuf[1:].view(8, 2, 64), _dev(kc2), _dev(vc2), _dev(t2),
                                 _dev(c2), _dev(qs2), 0.1, desc2, max_q_len=8)
+    # the scale must be finite and positive
+    for bad in (0.0, -0.1, float("inf"), float("nan")):
+        with pytest.raises(pk.PagedKVError):
+            pk.pa_prefill_attention(out2, _dev(q2), _dev(kc2), _dev(vc2), _dev(t2), _dev(c2),
+                                    _dev(qs2), bad, desc2, max_q_len=8)
