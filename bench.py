@@ -812,7 +812,7 @@ def run_prefill(args):
                        "prompt_tokens": T, "pool_blocks": w.num_blocks,
                        "l2": "K/V written and read back per step ~1.7 GB >> 129 MB L2, no flush"},
             "gpu_launches": 2 * args.steps,
-            "roofline": {"bound": "tensor", "kernel": "paged_prefill_mma<128> (pa_prefill_attention)",
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc<128> (pa_prefill_attention)",
                          "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": None,
                          "algorithmic_flops_per_launch": flops,

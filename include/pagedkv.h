@@ -335,19 +335,20 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
  * first ctx - q_len tokens are already cached (a later chunk of a long
  * prompt, or a prompt whose leading blocks came from the prefix cache).
  * q_len == 1 is a decode query.
- *   out, q        [T][num_heads][head_dim] fp16, T >= q_starts[n_seqs];
- *                 out, q and the caches 16-byte aligned
+ *   out, q        [q_rows][num_heads][head_dim] fp16, 16-byte aligned like
+ *                 the caches; every sequence's rows lie in [0, q_rows)
  *   block_tables  [n_seqs][max_blocks] int32 (entries past ceil(ctx/B) unread)
  *   ctx_lens      [n_seqs] int32
  *   q_starts      [n_seqs + 1] int32, non-decreasing
  *   max_q_len     host bound on every q_len (sizes the launch)
+ *   q_rows        rows of q and out (0: nothing to do)
  *   scale         finite and > 0 (1/sqrt(head_dim) in the pages)
  * head_dim 64 or 128, block_size 4..32.  Tensor cores: fp16 products, fp32
  * accumulation; the probabilities enter the second product as the sum of two
  * fp16 terms, so the fp16 rounding of the output dominates the error.
  * Device-side problems go to *status and leave that sequence's rows
- * unwritten: PA_ERR_INVALID_ARG for q_len < 0, q_len > ctx or
- * q_len > max_q_len; PA_ERR_BAD_BLOCK for ctx > max_blocks * B or a table
+ * unwritten: PA_ERR_INVALID_ARG for q_len < 0, q_len > ctx,
+ * q_len > max_q_len or rows outside [0, q_rows); PA_ERR_BAD_BLOCK for ctx > max_blocks * B or a table
  * entry outside the pool (that entry is not read and the sequence's output
  * is unspecified).
  * Errors: PA_ERR_INVALID_ARG (geometry, sizes, NULL or misaligned
@@ -355,7 +356,7 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
 int pa_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_tables, const int32_t *ctx_lens,
                          const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,
-                         int32_t max_q_len, float scale, int32_t *status,
+                         int32_t max_q_len, int32_t q_rows, float scale, int32_t *status,
                          const pa_pool_desc *desc, void *stream);
 
 /* ---- decode attention without a caller-provided workspace ------------------

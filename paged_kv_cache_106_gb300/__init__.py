@@ -96,8 +96,8 @@ def _load():
                                       vp, P(pa_pool_desc), vp]),
         "pa_decode_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float,
                                               vp, P(pa_pool_desc), vp]),
-        "pa_prefill_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, ctypes.c_float,
-                                       vp, P(pa_pool_desc), vp]),
+        "pa_prefill_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                       ctypes.c_float, vp, P(pa_pool_desc), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -367,15 +367,17 @@ def pa_decode_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, scale:
 
 def pa_prefill_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, q_starts,
                          scale: float, desc: PoolDesc, max_q_len: int, status=None, stream=None,
-                         n_seqs: int | None = None, max_blocks: int | None = None) -> None:
+                         n_seqs: int | None = None, max_blocks: int | None = None,
+                         q_rows: int | None = None) -> None:
     """Causal paged prefill: rows q_starts[s]..q_starts[s+1]-1 of q are the last
     positions of sequence s's context of ctx_lens[s] tokens.  ``max_q_len``
-    (host int) bounds every q_len."""
+    (host int) bounds every q_len; ``q_rows`` defaults to the rows of q and out."""
     n = int(ctx_lens.shape[0]) if n_seqs is None else int(n_seqs)
     mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
+    rows = min(int(q.shape[0]), int(out.shape[0])) if q_rows is None else int(q_rows)
     _check(_lib.pa_prefill_attention(_dev(out), _dev(q), _dev(k_cache), _dev(v_cache),
                                      _dev(block_tables), _dev(ctx_lens), _dev(q_starts), n, mb,
-                                     int(max_q_len), ctypes.c_float(scale), _dev(status),
+                                     int(max_q_len), rows, ctypes.c_float(scale), _dev(status),
                                      desc.ref, _stream(stream)))
 
 

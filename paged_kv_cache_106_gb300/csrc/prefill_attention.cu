@@ -8,24 +8,32 @@
 // PagedAttention notes (§3.1) evaluated for each of those queries.
 //
 // Kernel design (sm_103a, 5th-generation tensor cores through tcgen05):
-//   - one CTA = (sequence, head, tile of 128 consecutive queries); later
-//     query tiles (more keys) are launched first.  Warp roles:
-//       warps 0-7  softmax: query row i is tensor-memory lane i; warps w and
-//                  w + 4 share the 32 rows of lane quarter w % 4, each taking
-//                  half of a tile's key columns, and meet once per tile to
-//                  combine their row maxima;
-//       warp 8     one thread issues every tcgen05.mma and commit;
-//       warps 9-10 gather K tiles, warps 11-12 the Q tile and V tiles.
-//   - keys and values stream through shared-memory rings (3 K stages, 2 V) in
-//     tiles of 128 positions.  Position j lives in block table[j / B] at
-//     offset j % B; in the cache layout [block][head][B][D] each (block,
-//     head) run is B*D*2 contiguous bytes.  For B >= 8 a lane per block
-//     issues one 2-D TMA copy per 64-column panel of the run (a tensor map
-//     over the cache's rows), which lands already in the 128-byte-swizzled
-//     layout the tensor cores read; for B = 4 the loader threads gather the
-//     same layout with 16-byte cp.async.  The same bytes are the K-major B
-//     operand of S = Q K^T and the MN-major B operand of O = P V.  Rows past
-//     the context in the last V tile are zeroed before the product.
+//   - persistent: one CTA per SM walks units of work, a unit being 128
+//     consecutive queries of one (sequence, head); units are taken in the
+//     order (query tile from the last, sequence, head), strided by CTA, so
+//     units with the most keys come first.  Tensor memory, barriers and the
+//     pipeline carry over from unit to unit.  Warp roles:
+//       warps 0-7  softmax and epilogue: query row i is tensor-memory lane i;
+//                  warps w and w + 4 share the 32 rows of lane quarter w % 4,
+//                  each taking half of a tile's key columns, and meet once per
+//                  tile to combine their row maxima;
+//       warp 8     one thread issues every tcgen05.mma and commit, polling its
+//                  dependencies so Q K^T and P V of different tiles interleave;
+//       warp 9     Q rows and K tiles by TMA, warp 10 V tiles by TMA;
+//       warp 11    scheduler: finds this CTA's non-empty units and publishes
+//                  them through a 4-slot descriptor ring.
+//   - Q (two buffers), K and V (two-stage rings) move in tiles of 128
+//     positions.  Position j lives in block table[j / B] at offset j % B; in
+//     the cache layout [block][head][B][D] each (block, head) run is B*D*2
+//     contiguous bytes.  A loader lane per block issues one 2-D TMA copy per
+//     64-column panel of the run (a tensor map over the cache's rows, box
+//     64 x B), which lands already in the 128-byte-swizzled layout the tensor
+//     cores read (the swizzle follows the shared-memory address, so a 4-row
+//     box half-way into a 1024-byte pattern lands right).  The same bytes are
+//     the K-major B operand of S = Q K^T and the MN-major B operand of
+//     O = P V.  The V block holding the context's last position is copied
+//     row by row up to it, and the V ring starts zeroed, so slots past the
+//     context are never read; Q rows come one per copy.
 //   - tensor memory (512 columns): three 128-column S buffers, so Q K^T for
 //     tile t+2 runs while tile t is in softmax, and the fp32 output
 //     accumulator O (D columns).  Softmax overwrites its S buffer with P as
@@ -37,10 +45,12 @@
 //     in fp16.  P enters P V as hi + lo fp16 terms (hi = fp16(p),
 //     lo = fp16(p - hi)), keeping about 22 bits of each probability, so the
 //     fp16 rounding of the output dominates the error.
-//   - positions past the causal end of the tile are zero-filled, and scores
-//     of keys after a row's own position are masked to -inf.
-//   - the epilogue stages each row half as fp16 in shared memory and writes
-//     it with one bulk copy (rows of a head are H*D*2 bytes apart in out).
+//   - blocks past the causal end of a tile are not copied; scores of keys
+//     after a row's own position are masked to -inf (a select, so stale
+//     shared memory there cannot leak in).
+//   - the epilogue stages each row half as fp16 in the unit's Q buffer and
+//     writes it with one bulk copy (rows of a head are H*D*2 bytes apart in
+//     out), then releases the buffer for the unit after next.
 //   - every mbarrier wait is bounded; a wait that runs out reports
 //     PA_ERR_TIMEOUT, and the CTA drains its MMAs (bounded) and frees its
 //     tensor memory before it returns.
@@ -68,23 +78,10 @@ struct PrefillParams {
     const int32_t *tables;
     const int32_t *ctx_lens;
     const int32_t *q_starts;
-    int32_t num_heads, num_blocks, max_blocks, max_q_len, q_tiles, bshift;
+    int32_t num_heads, num_blocks, max_blocks, max_q_len, q_rows, q_tiles, bshift;
     float qscale;  // scale * log2(e): softmax evaluated with exp2
     int32_t *status;
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 // 2^x by the PTX approximation instruction (relative error about 2^-22;
 // -inf gives +0).
@@ -132,447 +129,595 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uin
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-constexpr int TBM = 128;          // queries per CTA (= tensor-memory lanes)
+constexpr int TBM = 128;          // queries per unit (= tensor-memory lanes)
 constexpr int TBN = 128;          // key positions per tile
-constexpr int NST = 3;            // K ring stages and S buffers
+constexpr int NSB = 3;            // S buffers in tensor memory
+constexpr int NSK = 2;            // K ring stages
 constexpr int NSV = 2;            // V ring stages
-constexpr int kMmaWarp = 8, kKWarp0 = 9, kVWarp0 = 11;
+constexpr int NU = 4;             // unit descriptors in flight
+constexpr int kMmaWarp = 8, kKWarp = 9, kVWarp = 10, kSchedWarp = 11, kStoreWarp = 12;
 constexpr int kTcThreads = 416;   // 13 warps
 constexpr uint32_t kPanel = TBM * 128;   // bytes of one 64-column panel of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = NST * 128;    // output accumulator after the S buffers
+constexpr uint32_t kOCol = NSB * 128;    // output accumulator after the S buffers
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
+// readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, store warp
+constexpr uint32_t kUnitReaders = 4 + 8;
+constexpr int kRowMaps = 8;       // boxes of 128, 64, ..., 1 rows for query / output rows
+constexpr int kVPartMaps = 5;     // boxes of 16, 8, 4, 2, 1 cache rows for a partial V block
 
 template <int D>
 struct TcLayout {
     static constexpr uint32_t TILE = (D / 64) * kPanel;
-    static constexpr uint32_t Q = 0, K = TILE, V = K + NST * TILE, END = V + NSV * TILE;
-    static constexpr uint32_t OUT_STRIDE = D * 2 + 16;   // output staging rows (in the K ring)
+    static constexpr uint32_t Q = 0, K = 2 * TILE, V = K + NSK * TILE, END = V + NSV * TILE;
     // at least 116 KB so that one CTA holds an SM (its 512 tensor-memory
     // columns are the whole SM's), plus 1 KB to align the tiles to 1024 bytes
     static constexpr uint32_t BYTES = (END > 116u * 1024u ? END : 116u * 1024u) + 1024u;
 };
 
+// One unit of work: 128 queries of one (sequence, head).
+struct Unit {
+    int32_t s, h, q0, q_beg, ql, pos0, n_end, n_tiles;   // n_tiles == 0: no more units
+};
+
+// Tensor maps: cache rows (K and V, box 64 x B), cache rows for the partial
+// V block (boxes 64 x 16 .. 64 x 1), query rows and output rows as 3-D
+// [rows][H][D] tensors (q: one box of 128 rows; out: boxes of 128 .. 1 rows).
+struct TcMaps {
+    CUtensorMap k, v, v_part[kVPartMaps], q, out[kRowMaps];
+};
+
 struct TcBars {
-    uint64_t q_full;
-    uint64_t k_full[NST], k_empty[NST], v_full[NSV], v_empty[NSV];
-    uint64_t s_full[NST], p_full[NST], pv_done[NST];
-    uint64_t done, v_raw;
+    uint64_t unit_full[NU], unit_empty[NU];
+    uint64_t q_full[2], q_empty[2], staged[2];
+    uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
+    uint64_t s_full[NSB], p_full[NSB], pv_done[NSB];
+    uint64_t done;
     uint32_t tmem;
-    int32_t tab[2][2][TBN / 4];   // per loader group, double-buffered block ids of a tile
-    float red[2][2][TBM];         // per tile parity and column half: row maxima, then sums
+    Unit unit[NU];
+    float red[2][2][TBM];   // per tile parity and column half: row maxima
+    float red_l[2][2][TBM]; // per unit parity and column half: row sums of a finished unit
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
-// TMA: K / V tiles arrive by 2-D tensor copies of whole (block, head) runs
-// (block sizes 8..32, whose runs start on 1024-byte boundaries of the
-// swizzle pattern); otherwise (block size 4) by 16-byte cp.async.
-template <int D, bool TMA>
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void zero_smem(uint32_t addr, uint32_t bytes, int lane) {
+    for (uint32_t o = (uint32_t)lane * 16u; o < bytes; o += 32u * 16u)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr + o), "r"(0) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
+// Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
+// of the list ordered by query tile (last tiles, with the most keys, first),
+// then sequence, then head; a scheduler warp skips the empty ones.
+template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    paged_prefill_tc(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
-                     const __grid_constant__ CUtensorMap tmv) {
+    paged_prefill_tc(const PrefillParams p, const __grid_constant__ TcMaps maps, int32_t n_seqs) {
     using L = TcLayout<D>;
-    constexpr int CPR = D / 8;        // 16-byte chunks per row
-    constexpr int RPP = 64 / CPR;     // rows one pass of a 64-thread loader group covers
+    constexpr int NP = D / 64;   // 64-column panels
     extern __shared__ uint8_t smem_raw[];
     __shared__ TcBars bars;
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     const uint32_t sQ = base + L::Q, sK = base + L::K, sV = base + L::V;
-
-    const int s = blockIdx.z, h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q_beg = p.q_starts[s];
-    const int ql = p.q_starts[s + 1] - q_beg;
-    const int ctx = p.ctx_lens[s];
-    const bool bad_len = ql < 0 || ql > ctx || ql > p.max_q_len;
-    const bool bad_ctx = (int64_t)ctx > ((int64_t)p.max_blocks << p.bshift);
-    if (bad_len || bad_ctx) {
-        if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0)
-            report(p.status, bad_len ? PA_ERR_INVALID_ARG : PA_ERR_BAD_BLOCK);
-        return;
-    }
-    const int q0 = (p.q_tiles - 1 - (int)blockIdx.x) * TBM;  // later tiles first
-    if (q0 >= ql) return;
-    const int pos0 = ctx - ql;                 // position of query 0 of the sequence
-    const int rows = min(TBM, ql - q0);
-    const int n_end = pos0 + q0 + rows;        // this tile needs keys [0, n_end)
-    const int n_tiles = (n_end + TBN - 1) / TBN;
-
-    const uint32_t b_q = smem_addr(&bars.q_full), b_done = smem_addr(&bars.done);
+    const int H = p.num_heads, B = 1 << p.bshift;
     auto bar = [](uint64_t *arr, int i) { return smem_addr(arr + i); };
+
     if (tid == 0) {
-        mbar_init(b_q, 64);
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(bar(bars.k_full, i), TMA ? 1 : 64);
+        for (int i = 0; i < NU; ++i) {
+            mbar_init(bar(bars.unit_full, i), 1);
+            mbar_init(bar(bars.unit_empty, i), kUnitReaders);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(bars.q_full, i), 1);
+            mbar_init(bar(bars.q_empty, i), 2);   // last Q K^T of the unit + its output stored
+            mbar_init(bar(bars.staged, i), 256);  // softmax threads have staged the output
+        }
+        for (int i = 0; i < NSK; ++i) {
+            mbar_init(bar(bars.k_full, i), 1);
             mbar_init(bar(bars.k_empty, i), 1);
+        }
+        for (int i = 0; i < NSV; ++i) {
+            mbar_init(bar(bars.v_full, i), 1);
+            mbar_init(bar(bars.v_empty, i), 1);
+        }
+        for (int i = 0; i < NSB; ++i) {
             mbar_init(bar(bars.s_full, i), 1);
             mbar_init(bar(bars.p_full, i), 256);
             mbar_init(bar(bars.pv_done, i), 1);
         }
-        for (int i = 0; i < NSV; ++i) {
-            mbar_init(bar(bars.v_full, i), TMA ? 1 : 64);
-            mbar_init(bar(bars.v_empty, i), 1);
-        }
-        mbar_init(b_done, 1);
-        mbar_init(smem_addr(&bars.v_raw), 1);
+        mbar_init(smem_addr(&bars.done), 1);
         fence_barrier_init();
     }
     if (warp == kMmaWarp) tc::alloc(smem_addr(&bars.tmem), kTmemCols);
+    // the V ring starts as zeros: rows no copy ever writes (values past a
+    // context) must hold finite numbers, since they meet P = 0
+    if (warp == kVWarp) zero_smem(sV, NSV * L::TILE, lane);
+    fence_proxy_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = bars.tmem;
+    const int q_tiles = p.q_tiles;
 
-    if (warp >= kKWarp0) {
-        // ---- loaders: 64 threads gather K tiles, 64 gather the Q tile and V tiles
-        const bool is_k = warp < kVWarp0;
-        const int g = is_k ? 0 : 1;
-        const int lt = tid - (is_k ? kKWarp0 : kVWarp0) * 32;
-        const int c = lt % CPR, r0 = lt / CPR;
-        const int B = 1 << p.bshift;
-        const int32_t *table = p.tables + (size_t)s * p.max_blocks;
-        if (!is_k) {
-#pragma unroll 4
-            for (int r = r0; r < TBM; r += RPP) {
-                const bool v = r < rows;
-                const __half *src =
-                    p.q + ((size_t)(q_beg + q0 + (v ? r : 0)) * p.num_heads + h) * D + c * 8;
-                cp_async16(sQ + tc::sw128(TBM, r, c), src, v);
-            }
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
-            mbar_arrive(b_q);
+    // Reads unit k of this CTA from the ring (bounded wait); n_tiles < 0 on timeout.
+    auto get_unit = [&](int k, Unit &u) {
+        const bool ok =
+            warp_all(mbar_wait_bounded(bar(bars.unit_full, k % NU), (k / NU) & 1, p.status, true));
+        if (!ok) {
+            u.n_tiles = -1;
+            return;
         }
-        const uint32_t ring = is_k ? sK : sV;
+        u = bars.unit[k % NU];
+    };
+
+    if (warp == kSchedWarp) {
+        // ---- scheduler: lanes test 32 candidate units at a time, the valid ones
+        // are published in order
+        const long long S = n_seqs, SH = S * H, V = (long long)q_tiles * SH;
+        int k = 0;
+        bool ok = true;
+        for (long long base_v = blockIdx.x; ok && base_v < V; base_v += 32ll * gridDim.x) {
+            const long long v = base_v + (long long)lane * gridDim.x;
+            Unit u{};
+            bool valid = false;
+            if (v < V) {
+                const int x = (int)(v / SH);
+                const long long rem = v - (long long)x * SH;
+                u.s = (int)(rem / H);
+                u.h = (int)(rem - (long long)u.s * H);
+                const int qt = q_tiles - 1 - x;
+                u.q_beg = p.q_starts[u.s];
+                u.ql = p.q_starts[u.s + 1] - u.q_beg;
+                const int ctx = p.ctx_lens[u.s];
+                const bool bad_len = u.ql < 0 || u.ql > ctx || u.ql > p.max_q_len ||
+                                     u.q_beg < 0 || (int64_t)u.q_beg + u.ql > p.q_rows;
+                const bool bad_ctx = (int64_t)ctx > ((int64_t)p.max_blocks << p.bshift);
+                if ((bad_len || bad_ctx) && x == 0 && u.h == 0)
+                    report(p.status, bad_len ? PA_ERR_INVALID_ARG : PA_ERR_BAD_BLOCK);
+                u.q0 = qt * TBM;
+                valid = !bad_len && !bad_ctx && u.q0 < u.ql;
+                if (valid) {
+                    u.pos0 = ctx - u.ql;
+                    u.n_end = u.pos0 + u.q0 + min(TBM, u.ql - u.q0);
+                    u.n_tiles = (u.n_end + TBN - 1) / TBN;
+                }
+            }
+            uint32_t mask = __ballot_sync(0xffffffffu, valid);
+            while (mask) {
+                const int src = __ffs(mask) - 1;
+                mask &= mask - 1;
+                if (k >= NU)
+                    ok = warp_all(mbar_wait_bounded(bar(bars.unit_empty, k % NU),
+                                                    ((k / NU) - 1) & 1, p.status, true));
+                if (!ok) break;
+                if (lane == src) {
+                    bars.unit[k % NU] = u;
+                    mbar_arrive(bar(bars.unit_full, k % NU));
+                }
+                __syncwarp();
+                ++k;
+            }
+        }
+        // end marker
+        if (ok && k >= NU)
+            ok = warp_all(mbar_wait_bounded(bar(bars.unit_empty, k % NU), ((k / NU) - 1) & 1,
+                                            p.status, true));
+        if (lane == 0) {
+            if (ok) {
+                bars.unit[k % NU].n_tiles = 0;
+                mbar_arrive(bar(bars.unit_full, k % NU));
+            } else {
+                report(p.status, PA_ERR_TIMEOUT);
+            }
+        }
+    } else if (warp == kStoreWarp) {
+        // ---- output: once the softmax warps have staged a unit's rows (fp16,
+        // swizzled, in the unit's Q buffer), store them with tensor copies, rows
+        // split into boxes of 128, 64, ..., 1 so that only the unit's rows are
+        // written; then the Q buffer may take the unit after next
+        bool ok = true;
+        for (int k = 0;; ++k) {
+            Unit u;
+            get_unit(k, u);
+            if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
+            if (u.n_tiles <= 0) {
+                ok = u.n_tiles == 0;
+                break;
+            }
+            if (!warp_all(mbar_wait_bounded(bar(bars.staged, k & 1), (k >> 1) & 1, p.status, true))) {
+                ok = false;
+                break;
+            }
+            const int rows = min(TBM, u.ql - u.q0);
+            // box i covers rows [start_i, start_i + 2^(7-i)) when bit (7-i) of rows is set
+            const int i = lane % kRowMaps, pn = lane / kRowMaps;
+            const int bit = 7 - i;
+            if (pn < NP && ((rows >> bit) & 1)) {
+                const int start = rows & ~((2 << bit) - 1);   // rows covered by larger boxes
+                tma_store_3d(&maps.out[i], pn * 64, u.h, u.q_beg + u.q0 + start,
+                             sQ + (k & 1) * L::TILE + pn * kPanel + (uint32_t)start * 128u);
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.q_empty, k & 1));
+        }
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores complete
+        if (!ok) report(p.status, PA_ERR_TIMEOUT);
+    } else if (warp == kKWarp || warp == kVWarp) {
+        // ---- loaders: lane i issues the TMA copies of block i of a tile
+        const bool is_k = warp == kKWarp;
+        const uint32_t run_bytes = (uint32_t)B * 128u * NP;
+        const CUtensorMap *map = is_k ? &maps.k : &maps.v;
         uint64_t *full = is_k ? bars.k_full : bars.v_full;
         uint64_t *empty = is_k ? bars.k_empty : bars.v_empty;
+        const uint32_t ring = is_k ? sK : sV;
+        const int NS = is_k ? NSK : NSV;
         const int nb = TBN >> p.bshift;   // blocks per tile (tiles start on a block)
-        const int NS = is_k ? NST : NSV;   // ring stages of this group
-        if constexpr (TMA) {
-            // One warp per group issues the tensor copies, lane i for block i
-            // of the tile; the V group's second warp helps zero the rows past
-            // the context in the last V tile.
-            const CUtensorMap *map = is_k ? &tmk : &tmv;
-            const uint32_t run_bytes = (uint32_t)B * 128u * (D / 64);
-            const uint32_t b_raw = smem_addr(&bars.v_raw);
-            bool dead = false;   // a wait ran out: issue nothing more, but still meet the group
-            for (int t = 0; t < n_tiles; ++t) {
-                const int st = t % NS;
-                const int n0 = t * TBN;
-                // rows past the context must read as zeros in V (0 * garbage
-                // could be NaN); only the last tile has such rows
-                const bool fix = !is_k && t == n_tiles - 1 && n_end - n0 < TBN;
-                if (lt < 32 && !dead) {
-                    const bool ok = warp_all(t < NS || mbar_wait_bounded(bar(empty, st),
-                                                                         ((t / NS) - 1) & 1,
-                                                                         p.status, true));
-                    if (!ok) report(p.status, PA_ERR_TIMEOUT);
-                    dead = !ok;
-                }
-                if (lt < 32 && !dead) {
-                    const int j = n0 + (lt << p.bshift);
-                    const bool valid = lt < nb && j < n_end;
-                    const int phys = valid ? __ldg(table + (j >> p.bshift)) : -1;
-                    const bool in_pool = valid && phys >= 0 && phys < p.num_blocks;
-                    if (valid && !in_pool) report(p.status, PA_ERR_BAD_BLOCK);
-                    const uint32_t n_runs = __popc(__ballot_sync(0xffffffffu, in_pool));
-                    const uint32_t tgt = fix ? b_raw : bar(full, st);
-                    if (lt == 0) mbar_arrive_expect_tx(tgt, n_runs * run_bytes);
-                    __syncwarp();
-                    if (in_pool) {
-                        const uint32_t dst = ring + st * L::TILE + (uint32_t)(lt << p.bshift) * 128u;
-                        const int y = (phys * p.num_heads + h) << p.bshift;
+        int g = 0;                        // tiles issued so far (all units)
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            Unit u;
+            get_unit(k, u);
+            if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
+            if (u.n_tiles <= 0) {
+                ok = u.n_tiles == 0;
+                break;
+            }
+            const int32_t *table = p.tables + (size_t)u.s * p.max_blocks;
+            if (is_k) {
+                // the unit's 128 query rows of head h (rows past the end of q read
+                // as zeros; rows of the next sequence are harmless: never stored)
+                const int qb = k & 1;
+                if (k >= 2)
+                    ok = warp_all(mbar_wait_bounded(bar(bars.q_empty, qb), ((k >> 1) - 1) & 1,
+                                                    p.status, true));
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(bars.q_full, qb), L::TILE);
 #pragma unroll
-                        for (int pn = 0; pn < D / 64; ++pn)
-                            tma_load_2d(dst + pn * kPanel, map, pn * 64, y, tgt);
-                    }
+                    for (int pn = 0; pn < NP; ++pn)
+                        tma_load_3d(sQ + qb * L::TILE + pn * kPanel, &maps.q, pn * 64, u.h,
+                                    u.q_beg + u.q0, bar(bars.q_full, qb));
                 }
-                if (fix) {
-                    // both V warps: wait for the copies, zero rows [n_end - n0, TBN)
-                    const bool ok = mbar_wait_bounded(b_raw, 0, p.status, true);
-                    if (ok) {
-                        const int first = n_end - n0;
-                        const uint32_t span = (uint32_t)(TBN - first) * 128u;
-                        for (int pn = 0; pn < D / 64; ++pn) {
-                            const uint32_t z = ring + st * L::TILE + pn * kPanel + first * 128u;
-                            for (uint32_t o = (uint32_t)lt * 16u; o < span; o += 64u * 16u)
-                                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(z + o),
-                                             "r"(0)
-                                             : "memory");
-                        }
-                        fence_proxy_async_smem();
-                    }
-                    if (group_all(2, 64, ok)) {
-                        if (lt == 0) mbar_arrive(bar(full, st));
-                    } else {
-                        report(p.status, PA_ERR_TIMEOUT);
-                    }
-                }
+                __syncwarp();
             }
-        } else {
-            const __half *cache = is_k ? p.k_cache : p.v_cache;
-            // Tile t is issued before tile t-1 is waited for, so two tiles of
-            // copies are in flight per thread.
-            int t = 0;
-            for (; t < n_tiles; ++t) {
-                const int st = t % NS;
+            for (int t = 0; t < u.n_tiles; ++t, ++g) {
+                const int st = g % NS;
+                if (g >= NS)
+                    ok = warp_all(mbar_wait_bounded(bar(empty, st), ((g / NS) - 1) & 1, p.status, true));
+                if (!ok) break;
                 const int n0 = t * TBN;
-                int32_t *tab = bars.tab[g][t & 1];
-                if (lt < nb) {   // the tile's physical block ids, read once by the group
-                    const int j = n0 + (lt << p.bshift);
-                    tab[lt] = j < n_end ? __ldg(table + (j >> p.bshift)) : -1;
-                }
-                const bool free_ok =
-                    t < NS || mbar_wait_bounded(bar(empty, st), ((t / NS) - 1) & 1, p.status, true);
-                // one decision for the whole group, and the block ids visible to it
-                if (!group_all(1 + g, 64, free_ok)) {
-                    report(p.status, PA_ERR_TIMEOUT);
-                    break;
-                }
-                const uint32_t dst = ring + st * L::TILE;
-#pragma unroll 4
-                for (int r = r0; r < TBN; r += RPP) {
-                    const int j = n0 + r;
-                    const int phys = tab[r >> p.bshift];
-                    bool v = j < n_end;
-                    size_t off = 0;
-                    if (v) {
-                        if (phys < 0 || phys >= p.num_blocks) {
-                            report(p.status, PA_ERR_BAD_BLOCK);
-                            v = false;
-                        } else {
-                            off = (((size_t)phys * p.num_heads + h) * B + (j & (B - 1))) * D + c * 8;
+                const int j = n0 + (lane << p.bshift);   // first position of block `lane`
+                const bool present = lane < nb && j < u.n_end;
+                const int phys = present ? __ldg(table + (j >> p.bshift)) : -1;
+                const bool in_pool = present && phys >= 0 && phys < p.num_blocks;
+                if (present && !in_pool) report(p.status, PA_ERR_BAD_BLOCK);
+                // V: the block holding the context's last position is copied up to
+                // it, in boxes of 16, 8, 4, 2 and 1 rows (slots past it are never read)
+                const int nv = min(B, u.n_end - j);
+                const bool partial = !is_k && in_pool && nv < B;
+                const uint32_t whole = __popc(__ballot_sync(0xffffffffu, in_pool && !partial));
+                const uint32_t part_rows = __reduce_add_sync(0xffffffffu, partial ? (uint32_t)nv : 0u);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar(full, st), whole * run_bytes + part_rows * 128u * NP);
+                __syncwarp();
+                const uint32_t dst = ring + st * L::TILE + (uint32_t)(lane << p.bshift) * 128u;
+                const int y = (phys * H + u.h) << p.bshift;
+                if (in_pool && !partial) {
+#pragma unroll
+                    for (int pn = 0; pn < NP; ++pn)
+                        tma_load_2d(dst + pn * kPanel, map, pn * 64, y, bar(full, st));
+                } else if (partial) {
+                    int r = 0;
+#pragma unroll
+                    for (int m = 0; m < kVPartMaps; ++m) {
+                        const int len = 16 >> m;
+                        if (nv & len) {
+#pragma unroll
+                            for (int pn = 0; pn < NP; ++pn)
+                                tma_load_2d(dst + pn * kPanel + (uint32_t)r * 128u, &maps.v_part[m],
+                                            pn * 64, y + r, bar(full, st));
+                            r += len;
                         }
                     }
-                    cp_async16(dst + tc::sw128(TBN, r, c), cache + off, v);
                 }
-                cp_async_commit();
-                if (t > 0) {
-                    cp_async_wait<1>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(full, (t - 1) % NS));
-                }
-            }
-            cp_async_wait<0>();
-            if (t == n_tiles && n_tiles > 0) {
-                fence_proxy_async_smem();
-                mbar_arrive(bar(full, (n_tiles - 1) % NS));
             }
         }
+        if (!ok) report(p.status, PA_ERR_TIMEOUT);
     } else if (warp == kMmaWarp) {
-        // ---- one thread issues the MMAs
+        // ---- one thread issues the MMAs; it polls its dependencies so that a
+        // P V product never waits behind the next unit's Q K^T
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16(TBM, TBN, false);
             constexpr uint32_t idO = tc::idesc_f16(TBM, D, true);
-            auto issue_s = [&](int t) -> bool {
-                const int st = t % NST;
-                if (!mbar_wait_bounded(bar(bars.k_full, st), (t / NST) & 1, p.status, true))
-                    return false;
-                tc::fence_after();
-                const uint32_t kb = sK + st * L::TILE;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-                    tc::mma_ss(tmem + st * 128, tc::smem_desc(sQ + off, 16, 1024),
-                               tc::smem_desc(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            int ks = 0, ts = 0, gs = 0;   // S cursor: unit, tile in unit, global tile
+            int kp = 0, tp = 0, gp = 0;   // P V cursor
+            int s_tiles = -1;             // tiles of the S cursor's unit; -1: not read yet
+            bool s_end = false, ok = true;
+            uint64_t last = globaltimer_ns();
+            while (ok) {
+                bool progress = false;
+                // read the S cursor's unit once it is published
+                if (!s_end && s_tiles < 0 &&
+                    mbar_test(bar(bars.unit_full, ks % NU), (ks / NU) & 1)) {
+                    s_tiles = bars.unit[ks % NU].n_tiles;
+                    if (s_tiles <= 0) s_end = true;
+                    progress = true;
                 }
-                tc::commit(bar(bars.s_full, st));
-                tc::commit(bar(bars.k_empty, st));
-                return true;
-            };
-            bool ok = mbar_wait_bounded(b_q, 0, p.status, true);
-            if (ok) ok = issue_s(0);
-            if (ok && n_tiles > 1) ok = issue_s(1);
-            for (int t = 0; ok && t < n_tiles; ++t) {
-                const int b = t % NST, bv = t % NSV;
-                ok = mbar_wait_bounded(bar(bars.p_full, b), (t / NST) & 1, p.status, true) &&
-                     mbar_wait_bounded(bar(bars.v_full, bv), (t / NSV) & 1, p.status, true);
-                if (!ok) break;
-                tc::fence_after();
-                const uint32_t vb = sV + bv * L::TILE;
+                // P V of tile gp (its S was issued)
+                if (gp < gs && mbar_test(bar(bars.p_full, gp % NSB), (gp / NSB) & 1) &&
+                    mbar_test(bar(bars.v_full, gp % NSV), (gp / NSV) & 1)) {
+                    tc::fence_after();
+                    const uint32_t vb = sV + (gp % NSV) * L::TILE;
 #pragma unroll
-                for (int kk = 0; kk < TBN / 16; ++kk) {
-                    const uint64_t dv = tc::smem_desc(vb + kk * 2048, kPanel, 1024);
-                    const uint32_t pa = tmem + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
-                    tc::mma_ts(tmem + kOCol, pa, dv, idO, (t > 0 || kk > 0) ? 1u : 0u);
-                    tc::mma_ts(tmem + kOCol, pa + 16, dv, idO, 1u);
+                    for (int kk = 0; kk < TBN / 16; ++kk) {
+                        const uint64_t dv = tc::smem_desc(vb + kk * 2048, kPanel, 1024);
+                        const uint32_t pa = tmem + (gp % NSB) * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+                        tc::mma_ts(tmem + kOCol, pa, dv, idO, (tp > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_ts(tmem + kOCol, pa + 16, dv, idO, 1u);
+                    }
+                    tc::commit(bar(bars.v_empty, gp % NSV));
+                    tc::commit(bar(bars.pv_done, gp % NSB));
+                    ++gp;
+                    if (++tp == bars.unit[kp % NU].n_tiles) {   // unit kp done for this thread
+                        mbar_arrive(bar(bars.unit_empty, kp % NU));
+                        ++kp;
+                        tp = 0;
+                    }
+                    progress = true;
                 }
-                tc::commit(bar(bars.v_empty, bv));
-                tc::commit(bar(bars.pv_done, b));
-                if (t + 2 < n_tiles) {
-                    // S(t+2) goes to the buffer whose P the product of tile t-1 read
-                    if (t >= 1)
-                        ok = mbar_wait_bounded(bar(bars.pv_done, (t - 1) % NST),
-                                               ((t - 1) / NST) & 1, p.status, true);
-                    if (ok) ok = issue_s(t + 2);
+                // Q K^T of tile gs: buffer gs % NSB is free once P V of gs - NSB is done
+                if (!s_end && s_tiles > 0 && gs < gp + NSB &&
+                    (ts > 0 || mbar_test(bar(bars.q_full, ks & 1), (ks >> 1) & 1)) &&
+                    mbar_test(bar(bars.k_full, gs % NSK), (gs / NSK) & 1) &&
+                    (gs < NSB || mbar_test(bar(bars.pv_done, gs % NSB), ((gs - NSB) / NSB) & 1))) {
+                    tc::fence_after();
+                    const uint32_t qb = sQ + (ks & 1) * L::TILE, kb = sK + (gs % NSK) * L::TILE;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
+                        tc::mma_ss(tmem + (gs % NSB) * 128, tc::smem_desc(qb + off, 16, 1024),
+                                   tc::smem_desc(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                    }
+                    tc::commit(bar(bars.s_full, gs % NSB));
+                    tc::commit(bar(bars.k_empty, gs % NSK));
+                    ++gs;
+                    if (++ts == s_tiles) {   // last Q K^T of the unit: its Q buffer may go
+                        tc::commit(bar(bars.q_empty, ks & 1));
+                        ++ks;
+                        ts = 0;
+                        s_tiles = -1;
+                    }
+                    progress = true;
+                }
+                if (s_end && gp == gs) break;   // every issued tile has its product
+                if (progress) {
+                    last = globaltimer_ns();
+                } else if (globaltimer_ns() - last > kWaitLimitNs ||
+                           *(volatile const int32_t *)p.status == PA_ERR_TIMEOUT) {
+                    ok = false;
+                } else {
+                    __nanosleep(32);   // leave the issue slots to the softmax warps
                 }
             }
             if (!ok) report(p.status, PA_ERR_TIMEOUT);
-            tc::commit(b_done);   // lets the teardown wait for every MMA issued
+            if (s_end) mbar_arrive(bar(bars.unit_empty, ks % NU));   // the end marker's slot
+            tc::commit(smem_addr(&bars.done));   // lets the teardown wait for every MMA issued
         }
         __syncwarp();
     } else {
         // ---- softmax warps: warps w and w + 4 share the query rows of tensor-memory
         // lane quarter w % 4 (row = lane of that quarter); warp w < 4 takes key
-        // columns 0-63 of each tile, warp w + 4 columns 64-127
+        // columns 0-63 of each tile, warp w + 4 columns 64-127.  A unit's
+        // epilogue runs inside the next unit's first tile, after its P is
+        // written, so the wait for the unit's last P V product overlaps work.
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int qi = q0 + row;
-        const bool valid = qi < ql;
-        const int pos = pos0 + min(qi, ql - 1);
         const float qs = p.qscale;
-        float m_run = -INFINITY, l_run = 0.f;
         bool ok = true;
-        for (int t = 0; t < n_tiles; ++t) {
-            const int b = t % NST;
-            ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, b), (t / NST) & 1, p.status, true));
-            const uint32_t sb = lane_base + b * 128 + half * 64;
-            const int n0 = t * TBN + half * 64;   // first key of this warp's columns
-            // keys past this row's position are masked: key n0 + 32 cc + i with i > lim
-            const bool need_mask = n0 + 63 > pos0 + q0;
-            float mt = -INFINITY;
-            if (ok) {
-                tc::fence_after();
-#pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t r[32];
-                    tc::ld32(sb + cc * 32, r);
-                    tc::wait_ld();
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    if (need_mask) {
-                        const int lim = pos - (n0 + cc * 32);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
-                    }
-                    mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-                }
-                mt *= qs;   // scale > 0: the maximum of the scaled scores
-            }
-            bars.red[t & 1][half][row] = mt;
-            // the two halves of each row meet here once per tile: one exit
-            // decision for all softmax warps, and the partner's maximum
-            if (!group_all(3, 256, ok)) {
-                ok = false;
-                break;
-            }
-            mt = fmaxf(mt, bars.red[t & 1][half ^ 1][row]);
-            float corr = 1.f;
-            const bool resc = mt > m_run + kRescaleLog2;
-            if (resc) {
-                corr = ex2(m_run - mt);
-                m_run = mt;
-                l_run *= corr;
-            }
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                uint32_t r[32], w[32];
-                tc::ld32(sb + cc * 32, r);
-                tc::wait_ld();
-                if (need_mask) {
-                    const int lim = pos - (n0 + cc * 32);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = 2 * i > lim ? 0.f : ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
-                        const float p1 =
-                            2 * i + 1 > lim ? 0.f : ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
-                        ls[i & 3] += p0 + p1;
-                        split_pair(p0, p1, w[i], w[16 + i]);
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
-                        const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
-                        ls[i & 3] += p0 + p1;
-                        split_pair(p0, p1, w[i], w[16 + i]);
-                    }
-                }
-                tc::st32(sb + cc * 32, w);
-            }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            tc::wait_st();
-            if (__any_sync(0xffffffffu, resc && t > 0)) {
-                // O holds tiles < t: wait until their product is complete, then
-                // scale this warp's half of the output columns
-                if (warp_all(mbar_wait_bounded(bar(bars.pv_done, (t - 1) % NST),
-                                               ((t - 1) / NST) & 1, p.status, true))) {
-                    tc::fence_after();
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 64; ++cc) {
-                        const uint32_t oc = lane_base + kOCol + half * (D / 2) + cc * 32;
-                        uint32_t r[32];
-                        tc::ld32(oc, r);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-                        tc::st32(oc, r);
-                    }
-                    tc::wait_st();
-                } else {
-                    ok = false;   // every softmax warp leaves at the next meeting
-                }
-            }
-            tc::fence_before();
-            mbar_arrive(bar(bars.p_full, b));
-        }
-        if (ok)
-            ok = warp_all(mbar_wait_bounded(bar(bars.pv_done, (n_tiles - 1) % NST),
-                                            ((n_tiles - 1) / NST) & 1, p.status, true));
-        bars.red[n_tiles & 1][half][row] = l_run;
-        if (group_all(3, 256, ok)) {
-            // this warp's half of the row: normalise, stage as fp16 in the
-            // (now idle) K ring, store with one bulk copy per row half
+        int g = 0;                   // tiles processed so far (all units)
+        int pend_k = -1, pend_g = 0; // unit whose output is still in tensor memory, its last tile
+        float pend_l = 0.f;
+        // normalise this warp's half of the pending unit's rows and stage them
+        // (fp16, 128-byte swizzle, in the unit's Q buffer) for the store warp
+        auto epilogue = [&]() -> bool {
+            if (!warp_all(mbar_wait_bounded(bar(bars.pv_done, pend_g % NSB), (pend_g / NSB) & 1,
+                                            p.status, true)))
+                return false;
             tc::fence_after();
-            const float inv = 1.f / (l_run + bars.red[n_tiles & 1][half ^ 1][row]);
-            const uint32_t stage = sK + (uint32_t)row * L::OUT_STRIDE + half * D;
+            const float inv = 1.f / (pend_l + bars.red_l[pend_k & 1][half ^ 1][row]);
+            const uint32_t stage = sQ + (pend_k & 1) * L::TILE;
 #pragma unroll 1
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t r[32];
                 tc::ld32(lane_base + kOCol + half * (D / 2) + cc * 32, r);
                 tc::wait_ld();
+                // columns half*D/2 + 32cc .. +31: panel and 16-byte chunks within it
+                const int col0 = half * (D / 2) + cc * 32;
+                const uint32_t pbase = stage + (col0 / 64) * kPanel + (uint32_t)row * 128u;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     uint32_t hv[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const __half2 v2 = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * k]) * inv,
-                                                             __uint_as_float(r[8 * i + 2 * k + 1]) * inv);
-                        hv[k] = *reinterpret_cast<const uint32_t *>(&v2);
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 v2 = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
+                                                             __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
+                        hv[e] = *reinterpret_cast<const uint32_t *>(&v2);
                     }
+                    const int chunk = ((col0 % 64) >> 3) + i;
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     stage + cc * 64 + i * 16),
+                                     pbase + (uint32_t)((chunk ^ (row & 7)) << 4)),
                                  "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
                                  : "memory");
                 }
             }
             fence_proxy_async_smem();
-            if (valid) {
-                __half *dst = p.out + ((size_t)(q_beg + qi) * p.num_heads + h) * D + half * (D / 2);
-                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                             "r"(stage), "r"(D)
-                             : "memory");
-                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            tc::fence_before();   // O read before the next unit's first product overwrites it
+            mbar_arrive(bar(bars.staged, pend_k & 1));
+            pend_k = -1;
+            return true;
+        };
+        for (int k = 0; ok; ++k) {
+            Unit u;
+            get_unit(k, u);
+            if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
+            if (u.n_tiles <= 0) {
+                ok = u.n_tiles == 0;
+                break;
             }
-        } else {
-            report(p.status, PA_ERR_TIMEOUT);
+            const int qi = u.q0 + row;
+            const int pos = u.pos0 + min(qi, u.ql - 1);
+            float m_run = -INFINITY, l_run = 0.f;
+            for (int t = 0; t < u.n_tiles; ++t, ++g) {
+                const int b = g % NSB;
+                ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, b), (g / NSB) & 1, p.status, true));
+                const uint32_t sb = lane_base + b * 128 + half * 64;
+                const int n0 = t * TBN + half * 64;   // first key of this warp's columns
+                // keys past this row's position are masked: key n0 + 32 cc + i with i > lim
+                const bool need_mask = n0 + 63 > u.pos0 + u.q0;
+                float mt = -INFINITY;
+                if (ok) {
+                    tc::fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t r[32];
+                        tc::ld32(sb + cc * 32, r);
+                        tc::wait_ld();
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        if (need_mask) {
+                            const int lim = pos - (n0 + cc * 32);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
+                        }
+                        mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                    }
+                    mt *= qs;   // scale > 0: the maximum of the scaled scores
+                }
+                bars.red[g & 1][half][row] = mt;
+                if (t == 0 && pend_k >= 0) bars.red_l[pend_k & 1][half][row] = pend_l;
+                // the two halves of each row meet here once per tile: one exit
+                // decision for all softmax warps, and the partner's maximum (and,
+                // on a unit's first tile, the partner's sum for the pending output)
+                if (!group_all(3, 256, ok)) {
+                    ok = false;
+                    break;
+                }
+                mt = fmaxf(mt, bars.red[g & 1][half ^ 1][row]);
+                float corr = 1.f;
+                const bool resc = mt > m_run + kRescaleLog2;
+                if (resc) {
+                    corr = ex2(m_run - mt);
+                    m_run = mt;
+                    l_run *= corr;
+                }
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t r[32], w[32];
+                    tc::ld32(sb + cc * 32, r);
+                    tc::wait_ld();
+                    if (need_mask) {
+                        const int lim = pos - (n0 + cc * 32);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 =
+                                2 * i > lim ? 0.f : ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
+                            const float p1 = 2 * i + 1 > lim
+                                                 ? 0.f
+                                                 : ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
+                            ls[i & 3] += p0 + p1;
+                            split_pair(p0, p1, w[i], w[16 + i]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
+                            const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
+                            ls[i & 3] += p0 + p1;
+                            split_pair(p0, p1, w[i], w[16 + i]);
+                        }
+                    }
+                    tc::st32(sb + cc * 32, w);
+                }
+                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                tc::wait_st();
+                if (t == 0 && pend_k >= 0 && !epilogue()) ok = false;
+                if (__any_sync(0xffffffffu, resc && t > 0)) {
+                    // O holds tiles < t of this unit: wait until their product is
+                    // complete, then scale this warp's half of the output columns
+                    if (warp_all(mbar_wait_bounded(bar(bars.pv_done, (g - 1) % NSB),
+                                                   ((g - 1) / NSB) & 1, p.status, true))) {
+                        tc::fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < D / 64; ++cc) {
+                            const uint32_t oc = lane_base + kOCol + half * (D / 2) + cc * 32;
+                            uint32_t r[32];
+                            tc::ld32(oc, r);
+                            tc::wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                            tc::st32(oc, r);
+                        }
+                        tc::wait_st();
+                    } else {
+                        ok = false;   // every softmax warp leaves at the next meeting
+                    }
+                }
+                tc::fence_before();
+                mbar_arrive(bar(bars.p_full, b));
+            }
+            if (!ok) break;
+            pend_k = k;
+            pend_g = g - 1;
+            pend_l = l_run;
         }
+        if (ok && pend_k >= 0) {
+            // the last unit's output: exchange sums, then stage
+            bars.red_l[pend_k & 1][half][row] = pend_l;
+            ok = group_all(3, 256, true) && epilogue();
+        }
+        if (!ok) report(p.status, PA_ERR_TIMEOUT);
     }
 
     // ---- teardown: every MMA drained (bounded), then tensor memory freed
     tc::fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
-        if (lane == 0 && !mbar_wait_bounded(b_done, 0, p.status, false))
+        if (lane == 0 && !mbar_wait_bounded(smem_addr(&bars.done), 0, p.status, false))
             report(p.status, PA_ERR_TIMEOUT);
         __syncwarp();
         tc::fence_after();
@@ -580,18 +725,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-template <int D, bool TMA>
+template <int D>
 cudaError_t set_prefill_smem_once() {
     static std::once_flag once[64];
     static cudaError_t err[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [&] {
-        err[dev] = cudaFuncSetAttribute(paged_prefill_tc<D, TMA>,
+        err[dev] = cudaFuncSetAttribute(paged_prefill_tc<D>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)TcLayout<D>::BYTES);
     });
     return err[dev];
+}
+
+int sm_count_of_current_device() {
+    static std::once_flag once[64];
+    static int n[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::call_once(once[dev], [&] {
+        if (cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n[dev] = 0;
+    });
+    return n[dev];
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -610,19 +767,28 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// One layer's cache seen as a 2-D fp16 tensor of num_blocks*H*B rows of D
-// values; a box is 64 values (one 128-byte swizzle row) by B rows, i.e. one
-// (block, head) run of one 64-column panel.
-int encode_cache_map(CUtensorMap *m, const void *cache, const pa_pool_desc *d) {
+// fp16 tensor of rank 2 ([rows][D]) or 3 ([rows][H][D]) with a box of 64
+// values (one 128-byte swizzle row) by `box_rows` rows (and one head).
+int encode_map(CUtensorMap *m, const void *base, int rank, uint64_t rows, int H, int D, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return fail(PA_ERR_CUDA, "pa_prefill_attention: cuTensorMapEncodeTiled unavailable");
-    const uint64_t rows = (uint64_t)d->num_blocks * d->num_heads * d->block_size;
-    cuuint64_t dims[2] = {(cuuint64_t)d->head_dim, (cuuint64_t)(rows ? rows : 1)};
-    cuuint64_t strides[1] = {(cuuint64_t)d->head_dim * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)d->block_size};
-    cuuint32_t elem[2] = {1, 1};
-    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(cache), dims,
-                           strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3], elem[3] = {1, 1, 1};
+    dims[0] = (cuuint64_t)D;
+    strides[0] = (cuuint64_t)D * 2;
+    box[0] = 64;
+    if (rank == 2) {
+        dims[1] = rows ? rows : 1;
+        box[1] = (cuuint32_t)box_rows;
+    } else {
+        dims[1] = (cuuint64_t)H;
+        dims[2] = rows ? rows : 1;
+        strides[1] = (cuuint64_t)H * D * 2;
+        box[1] = 1;
+        box[2] = (cuuint32_t)box_rows;
+    }
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+                           dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -630,22 +796,26 @@ int encode_cache_map(CUtensorMap *m, const void *cache, const pa_pool_desc *d) {
     return PA_OK;
 }
 
-template <int D, bool TMA>
+template <int D>
 int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st) {
-    cudaError_t e = set_prefill_smem_once<D, TMA>();
+    cudaError_t e = set_prefill_smem_once<D>();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
-    CUtensorMap tmk, tmv;
-    std::memset(&tmk, 0, sizeof tmk);
-    std::memset(&tmv, 0, sizeof tmv);
-    if (TMA) {
-        int rc = encode_cache_map(&tmk, p.k_cache, d);
-        if (rc == PA_OK) rc = encode_cache_map(&tmv, p.v_cache, d);
-        if (rc != PA_OK) return rc;
-    }
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return fail(PA_ERR_CUDA, "prefill: cannot read the SM count");
+    const uint64_t cache_rows = (uint64_t)d->num_blocks * d->num_heads * d->block_size;
+    const int H = d->num_heads;
+    TcMaps maps;
+    int rc = encode_map(&maps.k, p.k_cache, 2, cache_rows, H, D, d->block_size);
+    if (rc == PA_OK) rc = encode_map(&maps.v, p.v_cache, 2, cache_rows, H, D, d->block_size);
+    for (int m = 0; rc == PA_OK && m < kVPartMaps; ++m)
+        rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 16 >> m);
+    if (rc == PA_OK) rc = encode_map(&maps.q, p.q, 3, (uint64_t)p.q_rows, H, D, TBM);
+    for (int m = 0; rc == PA_OK && m < kRowMaps; ++m)
+        rc = encode_map(&maps.out[m], p.out, 3, (uint64_t)p.q_rows, H, D, TBM >> m);
+    if (rc != PA_OK) return rc;
     p.q_tiles = (p.max_q_len + TBM - 1) / TBM;
-    const dim3 grid((unsigned)p.q_tiles, (unsigned)p.num_heads, (unsigned)n_seqs);
-    paged_prefill_tc<D, TMA><<<grid, kTcThreads, TcLayout<D>::BYTES, st>>>(p, tmk, tmv);
+    paged_prefill_tc<D><<<sms, kTcThreads, TcLayout<D>::BYTES, st>>>(p, maps, n_seqs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PA_OK;
@@ -656,7 +826,7 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
 int launch_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_tables, const int32_t *ctx_lens,
                              const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,
-                             int32_t max_q_len, float scale, int32_t *status,
+                             int32_t max_q_len, int32_t q_rows, float scale, int32_t *status,
                              const pa_pool_desc *d, void *stream) {
     if (!d) return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: desc is NULL");
     std::string why;
@@ -664,11 +834,11 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     if (d->head_dim != 64 && d->head_dim != 128)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: head_dim %d not in {64, 128}",
                     d->head_dim);
-    if (n_seqs < 0 || max_blocks < 0 || max_q_len < 0)
+    if (n_seqs < 0 || max_blocks < 0 || max_q_len < 0 || q_rows < 0)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: negative size");
     if (n_seqs > 65535 || d->num_heads > 65535)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: more than 65535 sequences or heads");
-    if (n_seqs == 0 || max_q_len == 0) return PA_OK;
+    if (n_seqs == 0 || max_q_len == 0 || q_rows == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !ctx_lens || !q_starts)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: NULL pointer");
     if (((uintptr_t)out | (uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
@@ -690,15 +860,13 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     p.num_blocks = d->num_blocks;
     p.max_blocks = max_blocks;
     p.max_q_len = max_q_len;
+    p.q_rows = q_rows;
     p.q_tiles = 0;   // set by the launcher from its tile height
     p.bshift = bshift;
     p.qscale = scale * 1.4426950408889634f;
     p.status = status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool tma = d->block_size >= 8;
-    if (d->head_dim == 64)
-        return tma ? launch_d<64, true>(p, n_seqs, d, st) : launch_d<64, false>(p, n_seqs, d, st);
-    return tma ? launch_d<128, true>(p, n_seqs, d, st) : launch_d<128, false>(p, n_seqs, d, st);
+    return d->head_dim == 64 ? launch_d<64>(p, n_seqs, d, st) : launch_d<128>(p, n_seqs, d, st);
 }
 
 }  // namespace pagedkv

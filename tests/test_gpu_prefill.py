@@ -284,6 +284,17 @@ def test_prefill_status_reports_bad_lengths_and_blocks():
     c3[0] = tables.shape[1] * B + 1
     _gpu_prefill(q, kc, vc, tables, c3, qs, 0.1, B, status=st)
     assert st.item() == pk.PA_ERR_BAD_BLOCK
+    # rows past q_rows: that sequence is refused, the other one computed
+    desc = pk.PoolDesc(kc.shape[0], B, num_heads=H, head_dim=D)
+    out = torch.full((int(qs[-1]), H, D), float("nan"), dtype=torch.float16, device="cuda")
+    st = _status()
+    pk.pa_prefill_attention(out, _dev(q), _dev(kc), _dev(vc), _dev(tables), _dev(ctxa), _dev(qs),
+                            0.1, desc, max_q_len=10, status=st, q_rows=int(qs[-1]) - 1)
+    torch.cuda.synchronize()
+    assert st.item() == pk.PA_ERR_INVALID_ARG
+    got = out.cpu().numpy()
+    assert np.all(np.isnan(got[qs[1]:].astype(np.float32)))
+    _check(got[:qs[1]], oa.paged_prefill(q[:qs[1]], kc, vc, tables[:1], ctxa[:1], qs[:2], 0.1))
 
 
 def test_prefill_host_side_refusals():
