@@ -10,8 +10,9 @@
 // Kernel design (sm_103a, 5th-generation tensor cores through tcgen05):
 //   - persistent: one CTA per SM walks units of work, a unit being 128
 //     consecutive queries of one (sequence, head); units are taken in the
-//     order (query tile from the last, sequence, head), strided by CTA, so
-//     units with the most keys come first.  Tensor memory, barriers and the
+//     order (group of 8 sequences, query tile from the last, sequence,
+//     head), strided by CTA: long units first within a group, and the tiles
+//     sharing keys and values close in time (L2 reuse).  Tensor memory, barriers and the
 //     pipeline carry over from unit to unit.  Warp roles:
 //       warps 0-7  softmax and epilogue: query row i is tensor-memory lane i;
 //                  warps w and w + 4 share the 32 rows of lane quarter w % 4,
@@ -143,6 +144,7 @@ constexpr uint32_t kOCol = NSB * 128;    // output accumulator after the S buffe
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 // readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, store warp
 constexpr uint32_t kUnitReaders = 4 + 8;
+constexpr int kSeqGroup = 8;     // sequences whose query tiles are interleaved (L2 reuse)
 constexpr int kRowMaps = 8;       // boxes of 128, 64, ..., 1 rows for query / output rows
 constexpr int kVPartMaps = 5;     // boxes of 16, 8, 4, 2, 1 cache rows for a partial V block
 
@@ -214,8 +216,11 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int 
 }
 
 // Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
-// of the list ordered by query tile (last tiles, with the most keys, first),
-// then sequence, then head; a scheduler warp skips the empty ones.
+// of the list ordered by group of kSeqGroup sequences, then query tile (the
+// last, with the most keys, first), then sequence, then head; a scheduler
+// warp skips the empty ones.  Within a group the query tiles of one
+// (sequence, head) come a few units apart, while the group's keys and values
+// are still in L2, and concurrent CTAs work on different (sequence, head).
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc(const PrefillParams p, const __grid_constant__ TcMaps maps, int32_t n_seqs) {
@@ -280,7 +285,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == kSchedWarp) {
         // ---- scheduler: lanes test 32 candidate units at a time, the valid ones
         // are published in order
-        const long long S = n_seqs, SH = S * H, V = (long long)q_tiles * SH;
+        const long long V = (long long)n_seqs * H * q_tiles;
+        const long long group_units = (long long)kSeqGroup * H * q_tiles;
         int k = 0;
         bool ok = true;
         for (long long base_v = blockIdx.x; ok && base_v < V; base_v += 32ll * gridDim.x) {
@@ -288,10 +294,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             Unit u{};
             bool valid = false;
             if (v < V) {
-                const int x = (int)(v / SH);
-                const long long rem = v - (long long)x * SH;
-                u.s = (int)(rem / H);
-                u.h = (int)(rem - (long long)u.s * H);
+                // v -> (group of kSeqGroup sequences, query tile from the last,
+                // sequence in the group, head)
+                const int grp = (int)(v / group_units);
+                const int gsz = min(kSeqGroup, n_seqs - grp * kSeqGroup);
+                const long long r = v - (long long)grp * group_units;
+                const int x = (int)(r / ((long long)gsz * H));
+                const int r2 = (int)(r - (long long)x * gsz * H);
+                u.s = grp * kSeqGroup + r2 / H;
+                u.h = r2 - (r2 / H) * H;
                 const int qt = q_tiles - 1 - x;
                 u.q_beg = p.q_starts[u.s];
                 u.ql = p.q_starts[u.s + 1] - u.q_beg;
