@@ -57,11 +57,11 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _kernel_traffic(kernel_src: str):
+def _kernel_traffic(kernel_src: str, name: str = "decode_attention_traffic.json"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current source of the kernel (else None)."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "decode_attention_traffic.json")
+    p = os.path.join(ROOT, "profiles", name)
     try:
         with open(p) as f:
             d = json.load(f)
@@ -802,6 +802,11 @@ def run_prefill(args):
         except Exception:
             peak, kind = 1900.0, "fallback"
         achieved = flops / attn_s / 1e12
+        traffic = _kernel_traffic(os.path.join(ROOT, "paged_kv_cache_106_gb300", "csrc",
+                                               "prefill_attention.cu"),
+                                  "prefill_attention_traffic.json")
+        if args.prompts:
+            traffic = None   # the committed capture is of the full batch
         line = {
             "metric": PREFILL_METRIC, "value": tok_all / el_max, "unit": PREFILL_UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -814,7 +819,8 @@ def run_prefill(args):
             "gpu_launches": 2 * args.steps,
             "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc<128> (pa_prefill_attention)",
                          "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                          "algorithmic_flops_per_launch": flops,
                          "attn_ms_per_launch": attn_s * 1e3},
             "kernels": {"pa_write_kv": {"us_per_launch": (el / args.steps - attn_s) * 1e6,
