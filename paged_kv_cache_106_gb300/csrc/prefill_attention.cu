@@ -23,7 +23,8 @@
 //       warp 9     Q rows and K tiles by TMA, warp 10 V tiles by TMA;
 //       warp 11    scheduler: finds this CTA's non-empty units and publishes
 //                  them through a 4-slot descriptor ring.
-//   - Q (two buffers), K and V (two-stage rings) move in tiles of 128
+//   - Q (two buffers), K and V (two-stage rings, with the runs of the tile
+//     two steps further prefetched into L2) move in tiles of 128
 //     positions.  Position j lives in block table[j / B] at offset j % B; in
 //     the cache layout [block][head][B][D] each (block, head) run is B*D*2
 //     contiguous bytes.  A loader lane per block issues one 2-D TMA copy per
@@ -144,6 +145,7 @@ constexpr uint32_t kOCol = NSB * 128;    // output accumulator after the S buffe
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 // readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, store warp
 constexpr uint32_t kUnitReaders = 4 + 8;
+constexpr int kPrefetchTiles = 2;  // K/V tiles prefetched into L2 ahead of their copies
 constexpr int kSeqGroup = 8;     // sequences whose query tiles are interleaved (L2 reuse)
 constexpr int kRowMaps = 8;       // boxes of 128, 64, ..., 1 rows for query / output rows
 constexpr int kVPartMaps = 5;     // boxes of 16, 8, 4, 2, 1 cache rows for a partial V block
@@ -420,15 +422,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 __syncwarp();
             }
+            // block ids are read one tile ahead (and the runs of the tile
+            // kPrefetchTiles ahead prefetched into L2), so that neither the table
+            // read nor the copy waits on the other
+            auto entry = [&](int t) {
+                const int jt = t * TBN + (lane << p.bshift);
+                return (t < u.n_tiles && lane < nb && jt < u.n_end) ? __ldg(table + (jt >> p.bshift)) : -1;
+            };
+            int phys_next = entry(0);
             for (int t = 0; t < u.n_tiles; ++t, ++g) {
                 const int st = g % NS;
+                const int phys = phys_next;
+                phys_next = entry(t + 1);
                 if (g >= NS)
                     ok = warp_all(mbar_wait_bounded(bar(empty, st), ((g / NS) - 1) & 1, p.status, true));
                 if (!ok) break;
                 const int n0 = t * TBN;
                 const int j = n0 + (lane << p.bshift);   // first position of block `lane`
                 const bool present = lane < nb && j < u.n_end;
-                const int phys = present ? __ldg(table + (j >> p.bshift)) : -1;
                 const bool in_pool = present && phys >= 0 && phys < p.num_blocks;
                 if (present && !in_pool) report(p.status, PA_ERR_BAD_BLOCK);
                 // V: the block holding the context's last position is copied up to
@@ -460,6 +471,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     }
                 }
+                if (t + kPrefetchTiles < u.n_tiles) {
+                    const int pp = entry(t + kPrefetchTiles);
+                    if (pp >= 0 && pp < p.num_blocks)
+                        prefetch_l2((is_k ? p.k_cache : p.v_cache) + ((size_t)pp * H + u.h) * ((size_t)B * D),
+                                    (uint32_t)B * D * 2);
+                }
             }
         }
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
@@ -474,6 +491,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int s_tiles = -1;             // tiles of the S cursor's unit; -1: not read yet
             bool s_end = false, ok = true;
             uint64_t last = globaltimer_ns();
+            uint32_t idle = 0;   // passes without progress
             while (ok) {
                 bool progress = false;
                 // read the S cursor's unit once it is published
@@ -530,13 +548,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     progress = true;
                 }
                 if (s_end && gp == gs) break;   // every issued tile has its product
+                // timeout check every 256 idle passes (reading the timer is not free)
                 if (progress) {
-                    last = globaltimer_ns();
-                } else if (globaltimer_ns() - last > kWaitLimitNs ||
-                           *(volatile const int32_t *)p.status == PA_ERR_TIMEOUT) {
-                    ok = false;
-                } else {
-                    __nanosleep(32);   // leave the issue slots to the softmax warps
+                    idle = 0;
+                } else if ((++idle & 255) == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (idle == 256) last = now;
+                    if (now - last > kWaitLimitNs ||
+                        *(volatile const int32_t *)p.status == PA_ERR_TIMEOUT)
+                        ok = false;
                 }
             }
             if (!ok) report(p.status, PA_ERR_TIMEOUT);
