@@ -70,8 +70,10 @@ class DecodeStepRunner:
                 a[self.off_tab:self.off_tab + 4 * S * MB].view(np.int32).reshape(S, MB),
                 a[self.off_cp:self.off_cp + 8 * S].view(np.int32).reshape(S, 2))
 
-    def prepare(self) -> int:
-        """Host bookkeeping for one step and the upload of its metadata."""
+    def prepare_host(self) -> None:
+        """Host bookkeeping of the next step (block manager) into a pinned
+        staging buffer; no device work.  May run while the previous step's
+        kernels are in flight."""
         k = self.i & 1
         self.i += 1
         if self.events[k] is not None:
@@ -80,16 +82,25 @@ class DecodeStepRunner:
         slots, ctx, tables, copies = self._views(self.host[k])
         _, cp = pa_alloc_slots(self.pool, self.ids, copies_cap=self.S, slot_out=slots,
                                copies_out=copies)
-        self.n_copies = int(cp.shape[0])
         pa_get_block_tables(self.pool, self.ids, self.max_blocks, tables_out=tables, ctx_out=ctx)
-        self.ctx_host = ctx
         self.host_seconds = time.perf_counter() - t0   # block manager work of this step
+        self._pending = (k, int(cp.shape[0]), ctx)
+
+    def upload(self) -> int:
+        """Enqueue the prepared step's metadata upload on the stream."""
+        k, n_copies, ctx = self._pending
         with torch.cuda.stream(self.stream):
             self.dev.copy_(self.host[k], non_blocking=True)
             ev = torch.cuda.Event()
             ev.record(self.stream)
         self.events[k] = ev
-        return self.n_copies
+        self.n_copies, self.ctx_host = n_copies, ctx
+        return n_copies
+
+    def prepare(self) -> int:
+        """Host bookkeeping for one step and the upload of its metadata."""
+        self.prepare_host()
+        return self.upload()
 
     def copy_blocks(self, k_caches, v_caches):
         if self.n_copies:
