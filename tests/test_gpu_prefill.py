@@ -318,3 +318,68 @@ def test_prefill_host_side_refusals():
         with pytest.raises(pk.PagedKVError):
             pk.pa_prefill_attention(out2, _dev(q2), _dev(kc2), _dev(vc2), _dev(t2), _dev(c2),
                                     _dev(qs2), bad, desc2, max_q_len=8)
+
+
+def test_prefill_after_a_prefix_cache_hit_computes_only_the_new_tokens():
+    """Two prompts share a 48-token system prompt in a pool with prefix
+    caching: the second finds those three blocks cached, writes K/V for its
+    own tokens only and prefills only them (q_len < ctx).  Its rows agree
+    with the oracle and bitwise with prefilling the whole prompt in a fresh
+    pool (each query row is computed on its own)."""
+    H, D, B = 2, 64, 16
+    rng = np.random.default_rng(21)
+    system = rng.integers(0, 50000, 48).tolist()
+    toks_a = system + rng.integers(0, 50000, 20).tolist()
+    toks_b = system + rng.integers(0, 50000, 30).tolist()
+
+    def kv_of(tokens):   # K/V of a position: a function of (position, token) only
+        out_k, out_v = [], []
+        for p_, t_ in enumerate(tokens):
+            g = np.random.default_rng(1_000_003 * p_ + t_)
+            out_k.append(_f16(g, (H, D)))
+            out_v.append(_f16(g, (H, D)))
+        return np.stack(out_k), np.stack(out_v)
+
+    def prefill(pool, desc, kc, vc, sid, tokens, q_all):
+        slots, n_cached = pk.pa_seq_add_tokens(pool, sid, tokens)
+        k_all, v_all = kv_of(tokens)
+        new = slice(n_cached, len(tokens))
+        st = _status()
+        pk.pa_write_kv(_dev(k_all[new]), _dev(v_all[new]), _dev(slots[new]), kc, vc, desc, status=st)
+        tables, ctx = pk.pa_get_block_tables(pool, [sid], 8)
+        q = q_all[new]
+        qs = np.array([0, q.shape[0]], np.int32)
+        out = torch.empty((q.shape[0], H, D), dtype=torch.float16, device="cuda")
+        pk.pa_prefill_attention(out, _dev(q), kc, vc, _dev(tables), _dev(ctx), _dev(qs), 0.125,
+                                desc, max_q_len=q.shape[0], status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        return n_cached, out.cpu().numpy(), tables, ctx, q, qs
+
+    q_b = _f16(rng, (len(toks_b), H, D))
+    q_a = _f16(rng, (len(toks_a), H, D))
+    NB = 32
+    desc = pk.PoolDesc(NB, B, num_heads=H, head_dim=D, flags=pk.PA_POOL_PREFIX_CACHING)
+    pool = pk.pa_pool_create(desc)
+    kc = torch.zeros((NB, H, B, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    try:
+        n0, _, _, _, _, _ = prefill(pool, desc, kc, vc, 0, toks_a, q_a)
+        assert n0 == 0
+        n1, got, tables, ctx, q, qs = prefill(pool, desc, kc, vc, 1, toks_b, q_b)
+        assert n1 == 48 and list(ctx) == [len(toks_b)] and q.shape[0] == 30
+        ref = oa.paged_prefill(q, kc.cpu().numpy(), vc.cpu().numpy(), tables, ctx, qs, 0.125)
+        _check(got, ref)
+    finally:
+        pk.pa_pool_destroy(pool)
+    # the same prompt prefilled whole in a fresh pool
+    desc2 = pk.PoolDesc(NB, B, num_heads=H, head_dim=D)
+    pool2 = pk.pa_pool_create(desc2)
+    kc2 = torch.zeros((NB, H, B, D), dtype=torch.float16, device="cuda")
+    vc2 = torch.zeros_like(kc2)
+    try:
+        n2, whole, _, _, _, _ = prefill(pool2, desc2, kc2, vc2, 7, toks_b, q_b)
+        assert n2 == 0
+        assert np.array_equal(whole[48:].view(np.uint16), got.view(np.uint16))
+    finally:
+        pk.pa_pool_destroy(pool2)
