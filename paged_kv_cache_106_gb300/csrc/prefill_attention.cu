@@ -12,8 +12,8 @@
 //     consecutive queries of one (sequence, head); units are taken in the
 //     order (group of 8 sequences, query tile from the last, sequence,
 //     head), strided by CTA: long units first within a group, and the tiles
-//     sharing keys and values close in time (L2 reuse).  Tensor memory, barriers and the
-//     pipeline carry over from unit to unit.  Warp roles:
+//     sharing keys and values close in time (L2 reuse).  Tensor memory,
+//     barriers and the pipeline carry over from unit to unit.  Warp roles:
 //       warps 0-7  softmax and epilogue: query row i is tensor-memory lane i;
 //                  warps w and w + 4 share the 32 rows of lane quarter w % 4,
 //                  each taking half of a tile's key columns, and meet once per
@@ -22,7 +22,8 @@
 //                  dependencies so Q K^T and P V of different tiles interleave;
 //       warp 9     Q rows and K tiles by TMA, warp 10 V tiles by TMA;
 //       warp 11    scheduler: finds this CTA's non-empty units and publishes
-//                  them through a 4-slot descriptor ring.
+//                  them through a 4-slot descriptor ring;
+//       warp 12    output: TMA tensor stores of each unit's staged rows.
 //   - Q (two buffers), K and V (two-stage rings, with the runs of the tile
 //     two steps further prefetched into L2) move in tiles of 128
 //     positions.  Position j lives in block table[j / B] at offset j % B; in
@@ -34,8 +35,10 @@
 //     box half-way into a 1024-byte pattern lands right).  The same bytes are
 //     the K-major B operand of S = Q K^T and the MN-major B operand of
 //     O = P V.  The V block holding the context's last position is copied
-//     row by row up to it, and the V ring starts zeroed, so slots past the
-//     context are never read; Q rows come one per copy.
+//     up to it in boxes of 16, 8, 4, 2 and 1 rows, and the V ring starts
+//     zeroed, so slots past the context are never read.  Q arrives as one
+//     128-row box per panel of a [rows][H][D] tensor map (rows past q_rows
+//     read as zeros).
 //   - tensor memory (512 columns): three 128-column S buffers, so Q K^T for
 //     tile t+2 runs while tile t is in softmax, and the fp32 output
 //     accumulator O (D columns).  Softmax overwrites its S buffer with P as
@@ -50,9 +53,11 @@
 //   - blocks past the causal end of a tile are not copied; scores of keys
 //     after a row's own position are masked to -inf (a select, so stale
 //     shared memory there cannot leak in).
-//   - the epilogue stages each row half as fp16 in the unit's Q buffer and
-//     writes it with one bulk copy (rows of a head are H*D*2 bytes apart in
-//     out), then releases the buffer for the unit after next.
+//   - a unit's epilogue runs inside the next unit's first tile (hiding the
+//     wait for its last P V): the softmax warps normalise O and stage it as
+//     swizzled fp16 in the unit's Q buffer; the store warp writes it with TMA
+//     tensor stores in boxes of 128, 64, ..., 1 rows (only the unit's rows),
+//     then releases the buffer for the unit after next.
 //   - every mbarrier wait is bounded; a wait that runs out reports
 //     PA_ERR_TIMEOUT, and the CTA drains its MMAs (bounded) and frees its
 //     tensor memory before it returns.
