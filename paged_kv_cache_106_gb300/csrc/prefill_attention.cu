@@ -10,9 +10,11 @@
 // Kernel design (sm_103a, 5th-generation tensor cores through tcgen05):
 //   - persistent: one CTA per SM walks units of work, a unit being 128
 //     consecutive queries of one (sequence, head); units are taken in the
-//     order (group of 8 sequences, query tile from the last, sequence,
-//     head), strided by CTA: long units first within a group, and the tiles
-//     sharing keys and values close in time (L2 reuse).  Tensor memory,
+//     order (sequence, query tile from the last, head), strided by CTA: all
+//     heads of a query tile run side by side (different keys and values, no
+//     hot spots), and the next tile of the same (sequence, head), which
+//     re-reads a prefix of those keys and values, follows while they are
+//     still in L2 (measured: 5 % faster than interleaving 8 sequences).  Tensor memory,
 //     barriers and the pipeline carry over from unit to unit.  Warp roles:
 //       warps 0-7  softmax and epilogue: query row i is tensor-memory lane i;
 //                  warps w and w + 4 share the 32 rows of lane quarter w % 4,
@@ -151,7 +153,7 @@ constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 // readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, store warp
 constexpr uint32_t kUnitReaders = 4 + 8;
 constexpr int kPrefetchTiles = 2;  // K/V tiles prefetched into L2 ahead of their copies
-constexpr int kSeqGroup = 8;     // sequences whose query tiles are interleaved (L2 reuse)
+constexpr int kSeqGroup = 1;     // sequences whose query tiles are interleaved (L2 reuse)
 constexpr int kRowMaps = 8;       // boxes of 128, 64, ..., 1 rows for query / output rows
 constexpr int kVPartMaps = 5;     // boxes of 16, 8, 4, 2, 1 cache rows for a partial V block
 
@@ -225,9 +227,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int 
 // Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
 // of the list ordered by group of kSeqGroup sequences, then query tile (the
 // last, with the most keys, first), then sequence, then head; a scheduler
-// warp skips the empty ones.  Within a group the query tiles of one
-// (sequence, head) come a few units apart, while the group's keys and values
-// are still in L2, and concurrent CTAs work on different (sequence, head).
+// warp skips the empty ones.  The query tiles of one (sequence, head) come
+// about H units apart, while the keys and values they share are still in L2,
+// and concurrent CTAs work on different (sequence, head).
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc(const PrefillParams p, const __grid_constant__ TcMaps maps, int32_t n_seqs) {
