@@ -116,12 +116,20 @@ __device__ __forceinline__ bool group_all(int id, int count, bool v) {
 // 2-D tensor copy global -> shared (box of the tensor map at element
 // coordinates x, y); completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
+}
+
+// L2 policies: keys and values are re-read by later query tiles (keep them),
+// queries are read and outputs written once (let them go first).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // Two probabilities as fp16 pairs hi + lo (lower column in the low half).
@@ -210,18 +218,20 @@ __device__ __forceinline__ void zero_smem(uint32_t addr, uint32_t bytes, int lan
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
         : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z), "r"(src)
-                 : "memory");
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(src), "l"(policy)
+        : "memory");
 }
 
 // Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
@@ -382,7 +392,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (pn < NP && ((rows >> bit) & 1)) {
                 const int start = rows & ~((2 << bit) - 1);   // rows covered by larger boxes
                 tma_store_3d(&maps.out[i], pn * 64, u.h, u.q_beg + u.q0 + start,
-                             sQ + (k & 1) * L::TILE + pn * kPanel + (uint32_t)start * 128u);
+                             sQ + (k & 1) * L::TILE + pn * kPanel + (uint32_t)start * 128u,
+                             l2_evict_first_policy());
             }
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -401,6 +412,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t ring = is_k ? sK : sV;
         const int NS = is_k ? NSK : NSV;
         const int nb = TBN >> p.bshift;   // blocks per tile (tiles start on a block)
+        const uint64_t keep = l2_policy_evict_last();
         int g = 0;                        // tiles issued so far (all units)
         bool ok = true;
         for (int k = 0; ok; ++k) {
@@ -425,7 +437,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int pn = 0; pn < NP; ++pn)
                         tma_load_3d(sQ + qb * L::TILE + pn * kPanel, &maps.q, pn * 64, u.h,
-                                    u.q_beg + u.q0, bar(bars.q_full, qb));
+                                    u.q_beg + u.q0, bar(bars.q_full, qb), l2_evict_first_policy());
                 }
                 __syncwarp();
             }
@@ -463,7 +475,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (in_pool && !partial) {
 #pragma unroll
                     for (int pn = 0; pn < NP; ++pn)
-                        tma_load_2d(dst + pn * kPanel, map, pn * 64, y, bar(full, st));
+                        tma_load_2d(dst + pn * kPanel, map, pn * 64, y, bar(full, st), keep);
                 } else if (partial) {
                     int r = 0;
 #pragma unroll
@@ -473,7 +485,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                             for (int pn = 0; pn < NP; ++pn)
                                 tma_load_2d(dst + pn * kPanel + (uint32_t)r * 128u, &maps.v_part[m],
-                                            pn * 64, y + r, bar(full, st));
+                                            pn * 64, y + r, bar(full, st), keep);
                             r += len;
                         }
                     }
