@@ -30,17 +30,20 @@
 //     two steps further prefetched into L2) move in tiles of 128
 //     positions.  Position j lives in block table[j / B] at offset j % B; in
 //     the cache layout [block][head][B][D] each (block, head) run is B*D*2
-//     contiguous bytes.  A loader lane per block issues one 2-D TMA copy per
-//     64-column panel of the run (a tensor map over the cache's rows, box
-//     64 x B), which lands already in the 128-byte-swizzled layout the tensor
-//     cores read (the swizzle follows the shared-memory address, so a 4-row
-//     box half-way into a 1024-byte pattern lands right).  The same bytes are
-//     the K-major B operand of S = Q K^T and the MN-major B operand of
-//     O = P V.  The V block holding the context's last position is copied
-//     up to it in boxes of 16, 8, 4, 2 and 1 rows, and the V ring starts
-//     zeroed, so slots past the context are never read.  Q arrives as one
-//     128-row box per panel of a [rows][H][D] tensor map (rows past q_rows
-//     read as zeros).
+//     contiguous bytes.  K and V tiles sit in shared memory as 8-row groups,
+//     [j / 8][64-column panel][j % 8][128 bytes], 128-byte swizzled, so that
+//     a run of B >= 8 rows is whole groups: a loader lane per block moves it
+//     with one 4-D TMA copy (at D = 128, 4 KB at B = 16; per-SM copy
+//     throughput is higher for bigger boxes, and the copies bound the loop)
+//     and it lands already in the layout the tensor cores read (the swizzle
+//     follows the shared-memory address).  At B = 4, or D = 64, one 2-D copy
+//     per panel (box 64 x B).  The same bytes are the K-major B operand of
+//     S = Q K^T (8-row groups D/64 KB apart) and the MN-major B operand of
+//     O = P V (panels 1 KB apart).  The V block holding the context's last
+//     position is copied up to it in boxes of 8, 4, 2 and 1 rows, and the V
+//     ring starts zeroed, so slots past the context are never read.  Q
+//     arrives as one 128-row box per panel of a [rows][H][D] tensor map, in
+//     [panel][128 rows] layout (rows past q_rows read as zeros).
 //   - tensor memory (512 columns): three 128-column S buffers, so Q K^T for
 //     tile t+2 runs while tile t is in softmax, and the fp32 output
 //     accumulator O (D columns).  Softmax overwrites its S buffer with P as
@@ -48,10 +51,11 @@
 //     tensor memory.
 //   - the softmax is online, in base 2 (ex2.approx), with a lazy rescale: a row's
 //     reference maximum moves only when a tile raises it by more than 2^8,
-//     so O is rescaled in tensor memory rarely; P <= 2^8 stays exact enough
-//     in fp16.  P enters P V as hi + lo fp16 terms (hi = fp16(p),
-//     lo = fp16(p - hi)), keeping about 22 bits of each probability, so the
-//     fp16 rounding of the output dominates the error.
+//     so O is rescaled in tensor memory rarely.  P (<= 2^8) enters P V as
+//     fp16, 11 significant bits like the output: rounding p perturbs each
+//     weight by at most 2^-12 relative, and the fp16 rounding of the output
+//     stays the larger error (simulated: max |error| 1.03e-3 against 0.98e-3
+//     with exact p, for prompts up to 1536 and peaked scores).
 //   - blocks past the causal end of a tile are not copied; scores of keys
 //     after a row's own position are masked to -inf (a select, so stale
 //     shared memory there cannot leak in).
@@ -132,18 +136,10 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return pol;
 }
 
-// Two probabilities as fp16 pairs hi + lo (lower column in the low half).
-// hi is p rounded to fp16's 11 significant bits by integer arithmetic (exact
-// in fp16 for p >= 2^-14), so only the two packing conversions use the
-// conversion pipe; lo = p - hi is exact in fp32.  hi + lo carries p to about
-// 2^-22 relative, or to fp16's subnormal spacing (2^-24) for tiny p.
-__device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uint32_t &lo) {
-    const float h0 = __uint_as_float((__float_as_uint(p0) + 0x1000u) & 0xFFFFE000u);
-    const float h1 = __uint_as_float((__float_as_uint(p1) + 0x1000u) & 0xFFFFE000u);
-    const __half2 h = __floats2half2_rn(h0, h1);
-    const __half2 l = __floats2half2_rn(p0 - h0, p1 - h1);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
+// Two probabilities as one fp16 pair (lower column in the low half).
+__device__ __forceinline__ uint32_t pack_pair(float p0, float p1) {
+    const __half2 h = __floats2half2_rn(p0, p1);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 constexpr int TBM = 128;          // queries per unit (= tensor-memory lanes)
@@ -163,7 +159,7 @@ constexpr uint32_t kUnitReaders = 4 + 8;
 constexpr int kPrefetchTiles = 2;  // K/V tiles prefetched into L2 ahead of their copies
 constexpr int kSeqGroup = 1;     // sequences whose query tiles are interleaved (L2 reuse)
 constexpr int kRowMaps = 8;       // boxes of 128, 64, ..., 1 rows for query / output rows
-constexpr int kVPartMaps = 5;     // boxes of 16, 8, 4, 2, 1 cache rows for a partial V block
+constexpr int kVPartMaps = 4;     // boxes of 8, 4, 2, 1 cache rows for a partial V block
 
 template <int D>
 struct TcLayout {
@@ -174,13 +170,25 @@ struct TcLayout {
     static constexpr uint32_t BYTES = (END > 116u * 1024u ? END : 116u * 1024u) + 1024u;
 };
 
+// Byte offset of row r (panel 0) in a K or V tile.  Those tiles are laid out
+// [r / 8][panel][r % 8][128 bytes]: 8-row groups of (D / 64) KB, each holding
+// its rows' 64-column panels one after the other, so that a (block, head)
+// run of B >= 8 rows is B / 8 whole groups, contiguous in shared memory, and
+// one TMA box moves it.  Panel pn of a row is 1024 * pn bytes further.
+template <int D>
+__device__ __forceinline__ uint32_t kv_row_off(uint32_t r) {
+    return (r >> 3) * (uint32_t)(D / 64) * 1024u + (r & 7u) * 128u;
+}
+
 // One unit of work: 128 queries of one (sequence, head).
 struct Unit {
     int32_t s, h, q0, q_beg, ql, pos0, n_end, n_tiles;   // n_tiles == 0: no more units
 };
 
-// Tensor maps: cache rows (K and V, box 64 x B), cache rows for the partial
-// V block (boxes 64 x 16 .. 64 x 1), query rows and output rows as 3-D
+// Tensor maps: K and V cache runs (D = 128 with B >= 8: a 4-D view
+// [row / 8][panel][row % 8][64] with one box per (block, head) run; otherwise
+// rows of D values, box 64 x B, one copy per panel), cache rows for the
+// partial V block (boxes 64 x 8 .. 64 x 1), query rows and output rows as 3-D
 // [rows][H][D] tensors (q: one box of 128 rows; out: boxes of 128 .. 1 rows).
 struct TcMaps {
     CUtensorMap k, v, v_part[kVPartMaps], q, out[kRowMaps];
@@ -223,6 +231,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
         "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src,
@@ -470,25 +486,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar(full, st), whole * run_bytes + part_rows * 128u * NP);
                 __syncwarp();
-                const uint32_t dst = ring + st * L::TILE + (uint32_t)(lane << p.bshift) * 128u;
+                const uint32_t jrow = (uint32_t)(lane << p.bshift);   // block's first tile row
+                const uint32_t tile = ring + st * L::TILE;
                 const int y = (phys * H + u.h) << p.bshift;
                 if (in_pool && !partial) {
+                    if (NP == 2 && B >= 8) {
+                        tma_load_4d(tile + kv_row_off<D>(jrow), map, 0, 0, 0, y >> 3, bar(full, st), keep);
+                    } else {
 #pragma unroll
-                    for (int pn = 0; pn < NP; ++pn)
-                        tma_load_2d(dst + pn * kPanel, map, pn * 64, y, bar(full, st), keep);
-                } else if (partial) {
-                    int r = 0;
-#pragma unroll
-                    for (int m = 0; m < kVPartMaps; ++m) {
-                        const int len = 16 >> m;
-                        if (nv & len) {
-#pragma unroll
-                            for (int pn = 0; pn < NP; ++pn)
-                                tma_load_2d(dst + pn * kPanel + (uint32_t)r * 128u, &maps.v_part[m],
-                                            pn * 64, y + r, bar(full, st), keep);
-                            r += len;
-                        }
+                        for (int pn = 0; pn < NP; ++pn)
+                            tma_load_2d(tile + kv_row_off<D>(jrow) + pn * 1024u, map, pn * 64, y,
+                                        bar(full, st), keep);
                     }
+                } else if (partial) {
+                    // pieces of 8 rows (each one whole group), then 4, 2 and 1
+                    // (never crossing a group: the block starts on a group or, at
+                    // B = 4, half-way into one)
+                    int r = 0;
+                    auto piece = [&](int m) {
+#pragma unroll
+                        for (int pn = 0; pn < NP; ++pn)
+                            tma_load_2d(tile + kv_row_off<D>(jrow + (uint32_t)r) + pn * 1024u,
+                                        &maps.v_part[m], pn * 64, y + r, bar(full, st), keep);
+                        r += 8 >> m;
+                    };
+                    while (r + 8 <= nv) piece(0);
+#pragma unroll
+                    for (int m = 1; m < kVPartMaps; ++m)
+                        if (nv & (8 >> m)) piece(m);
                 }
                 if (t + kPrefetchTiles < u.n_tiles) {
                     const int pp = entry(t + kPrefetchTiles);
@@ -527,10 +552,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t vb = sV + (gp % NSV) * L::TILE;
 #pragma unroll
                     for (int kk = 0; kk < TBN / 16; ++kk) {
-                        const uint64_t dv = tc::smem_desc(vb + kk * 2048, kPanel, 1024);
-                        const uint32_t pa = tmem + (gp % NSB) * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+                        // 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart
+                        const uint64_t dv = tc::smem_desc(vb + kk * 2048u * NP, 1024, 1024u * NP);
+                        // P of keys 16 kk .. 16 kk + 15: column half (kk / 4) * 64, then
+                        // 16 columns per 32 keys, 8 columns (16 fp16) per slice
+                        const uint32_t pa = tmem + (gp % NSB) * 128 + (kk >> 2) * 64 +
+                                            ((kk >> 1) & 1) * 16 + (kk & 1) * 8;
                         tc::mma_ts(tmem + kOCol, pa, dv, idO, (tp > 0 || kk > 0) ? 1u : 0u);
-                        tc::mma_ts(tmem + kOCol, pa + 16, dv, idO, 1u);
                     }
                     tc::commit(bar(bars.v_empty, gp % NSV));
                     tc::commit(bar(bars.pv_done, gp % NSB));
@@ -551,9 +579,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t qb = sQ + (ks & 1) * L::TILE, kb = sK + (gs % NSK) * L::TILE;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kPanel + (kk & 3) * 32;
-                        tc::mma_ss(tmem + (gs % NSB) * 128, tc::smem_desc(qb + off, 16, 1024),
-                                   tc::smem_desc(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+                        // Q: [panel][128 rows]; K: 8-row groups of NP panels
+                        const uint32_t col = (kk & 3) * 32;
+                        tc::mma_ss(tmem + (gs % NSB) * 128,
+                                   tc::smem_desc(qb + (kk >> 2) * kPanel + col, 16, 1024),
+                                   tc::smem_desc(kb + (kk >> 2) * 1024u + col, 16, 1024u * NP), idS,
+                                   kk > 0 ? 1u : 0u);
                     }
                     tc::commit(bar(bars.s_full, gs % NSB));
                     tc::commit(bar(bars.k_empty, gs % NSK));
@@ -696,7 +727,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t r[32], w[32];
+                    uint32_t r[32], w[16];
                     tc::ld32(sb + cc * 32, r);
                     tc::wait_ld();
                     if (need_mask) {
@@ -709,7 +740,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                  ? 0.f
                                                  : ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
                             ls[i & 3] += p0 + p1;
-                            split_pair(p0, p1, w[i], w[16 + i]);
+                            w[i] = pack_pair(p0, p1);
                         }
                     } else {
 #pragma unroll
@@ -717,10 +748,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
                             const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
                             ls[i & 3] += p0 + p1;
-                            split_pair(p0, p1, w[i], w[16 + i]);
+                            w[i] = pack_pair(p0, p1);
                         }
                     }
-                    tc::st32(sb + cc * 32, w);
+                    // P of these 32 keys as 16 fp16 pairs over S columns already read
+                    tc::st16(sb + cc * 16, w);
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 tc::wait_st();
@@ -846,6 +878,23 @@ int encode_map(CUtensorMap *m, const void *base, int rank, uint64_t rows, int H,
     return PA_OK;
 }
 
+// The cache as [row / 8][panel][row % 8][64] fp16 (D = 128, rows a multiple
+// of 8), with a box of B / 8 such groups: one copy per (block, head) run that
+// lands in the grouped shared-memory layout of the K and V tiles.
+int encode_run_map(CUtensorMap *m, const void *base, uint64_t rows, int B) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return fail(PA_ERR_CUDA, "pa_prefill_attention: cuTensorMapEncodeTiled unavailable");
+    const cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+    const cuuint64_t strides[3] = {256, 128, 2048};   // bytes: next row, panel, 8-row group
+    const cuuint32_t box[4] = {64, 8, 2, (cuuint32_t)(B / 8)}, elem[4] = {1, 1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(base), dims, strides,
+                           box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PA_ERR_CUDA, "pa_prefill_attention: cuTensorMapEncodeTiled (run map) failed (%d)", (int)r);
+    return PA_OK;
+}
+
 template <int D>
 int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st) {
     cudaError_t e = set_prefill_smem_once<D>();
@@ -856,10 +905,16 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
     const uint64_t cache_rows = (uint64_t)d->num_blocks * d->num_heads * d->block_size;
     const int H = d->num_heads;
     TcMaps maps;
-    int rc = encode_map(&maps.k, p.k_cache, 2, cache_rows, H, D, d->block_size);
-    if (rc == PA_OK) rc = encode_map(&maps.v, p.v_cache, 2, cache_rows, H, D, d->block_size);
+    int rc;
+    if (D == 128 && d->block_size >= 8) {   // the kernel's one-box-per-run path
+        rc = encode_run_map(&maps.k, p.k_cache, cache_rows, d->block_size);
+        if (rc == PA_OK) rc = encode_run_map(&maps.v, p.v_cache, cache_rows, d->block_size);
+    } else {
+        rc = encode_map(&maps.k, p.k_cache, 2, cache_rows, H, D, d->block_size);
+        if (rc == PA_OK) rc = encode_map(&maps.v, p.v_cache, 2, cache_rows, H, D, d->block_size);
+    }
     for (int m = 0; rc == PA_OK && m < kVPartMaps; ++m)
-        rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 16 >> m);
+        rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 8 >> m);
     if (rc == PA_OK) rc = encode_map(&maps.q, p.q, 3, (uint64_t)p.q_rows, H, D, TBM);
     for (int m = 0; rc == PA_OK && m < kRowMaps; ++m)
         rc = encode_map(&maps.out[m], p.out, 3, (uint64_t)p.q_rows, H, D, TBM >> m);
