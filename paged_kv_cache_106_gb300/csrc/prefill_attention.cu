@@ -25,7 +25,8 @@
 //       warp 9     Q rows and K tiles by TMA, warp 10 V tiles by TMA;
 //       warp 11    scheduler: finds this CTA's non-empty units and publishes
 //                  them through a 4-slot descriptor ring;
-//       warp 12    output: TMA tensor stores of each unit's staged rows.
+//       warps 12-15 epilogue: warp 12 + q normalises and writes the rows of
+//                  lane quarter q once a unit's last P V is done.
 //   - Q (two buffers), K and V (two-stage rings, with the runs of the tile
 //     two steps further prefetched into L2) move in tiles of 128
 //     positions.  Position j lives in block table[j / B] at offset j % B; in
@@ -59,11 +60,14 @@
 //   - blocks past the causal end of a tile are not copied; scores of keys
 //     after a row's own position are masked to -inf (a select, so stale
 //     shared memory there cannot leak in).
-//   - a unit's epilogue runs inside the next unit's first tile (hiding the
-//     wait for its last P V): the softmax warps normalise O and stage it as
-//     swizzled fp16 in the unit's Q buffer; the store warp writes it with TMA
-//     tensor stores in boxes of 128, 64, ..., 1 rows (only the unit's rows),
-//     then releases the buffer for the unit after next.
+//   - the epilogue warps wait for a unit's last P V, read O from tensor
+//     memory into registers (normalised, as fp16) and release it to the next
+//     unit's first P V, which overwrites O; so the tensor pipe idles at a
+//     unit boundary only for that read, and the softmax warps never stop
+//     for an epilogue.  They write the rows with 16-byte streaming stores,
+//     exchanged within groups of 8 lanes so that each store instruction
+//     covers 4 whole 128-byte row segments (only the unit's rows).  A Q
+//     buffer is free as soon as its unit's last Q K^T is done.
 //   - every mbarrier wait is bounded; a wait that runs out reports
 //     PA_ERR_TIMEOUT, and the CTA drains its MMAs (bounded) and frees its
 //     tensor memory before it returns.
@@ -148,17 +152,16 @@ constexpr int NSB = 3;            // S buffers in tensor memory
 constexpr int NSK = 2;            // K ring stages
 constexpr int NSV = 2;            // V ring stages
 constexpr int NU = 4;             // unit descriptors in flight
-constexpr int kMmaWarp = 8, kKWarp = 9, kVWarp = 10, kSchedWarp = 11, kStoreWarp = 12;
-constexpr int kTcThreads = 416;   // 13 warps
+constexpr int kMmaWarp = 8, kKWarp = 9, kVWarp = 10, kSchedWarp = 11;   // 12-15: epilogue
+constexpr int kTcThreads = 512;   // 16 warps
 constexpr uint32_t kPanel = TBM * 128;   // bytes of one 64-column panel of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = NSB * 128;    // output accumulator after the S buffers
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
-// readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, store warp
-constexpr uint32_t kUnitReaders = 4 + 8;
+// readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, 4 epilogue warps
+constexpr uint32_t kUnitReaders = 3 + 8 + 4;
 constexpr int kPrefetchTiles = 2;  // K/V tiles prefetched into L2 ahead of their copies
 constexpr int kSeqGroup = 1;     // sequences whose query tiles are interleaved (L2 reuse)
-constexpr int kRowMaps = 8;       // boxes of 128, 64, ..., 1 rows for query / output rows
 constexpr int kVPartMaps = 4;     // boxes of 8, 4, 2, 1 cache rows for a partial V block
 
 template <int D>
@@ -191,19 +194,21 @@ struct Unit {
 // partial V block (boxes 64 x 8 .. 64 x 1), query rows and output rows as 3-D
 // [rows][H][D] tensors (q: one box of 128 rows; out: boxes of 128 .. 1 rows).
 struct TcMaps {
-    CUtensorMap k, v, v_part[kVPartMaps], q, out[kRowMaps];
+    CUtensorMap k, v, v_part[kVPartMaps], q;
 };
 
 struct TcBars {
     uint64_t unit_full[NU], unit_empty[NU];
-    uint64_t q_full[2], q_empty[2], staged[2];
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
     uint64_t s_full[NSB], p_full[NSB], pv_done[NSB];
+    uint64_t o_free;               // the epilogue has read a unit's O (one phase per unit)
+    uint64_t l_full[2], l_empty[2]; // a unit's row sums (slot k & 1) written / read
     uint64_t done;
     uint32_t tmem;
     Unit unit[NU];
     float red[2][2][TBM];   // per tile parity and column half: row maxima
-    float red_l[2][2][TBM]; // per unit parity and column half: row sums of a finished unit
+    float red_l[2][2][TBM]; // per unit parity and column half: a finished unit's row sums
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
@@ -241,14 +246,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
         : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src,
-                                             uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(y), "r"(z), "r"(src), "l"(policy)
-        : "memory");
-}
 
 // Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
 // of the list ordered by group of kSeqGroup sequences, then query tile (the
@@ -276,8 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(bars.q_full, i), 1);
-            mbar_init(bar(bars.q_empty, i), 2);   // last Q K^T of the unit + its output stored
-            mbar_init(bar(bars.staged, i), 256);  // softmax threads have staged the output
+            mbar_init(bar(bars.q_empty, i), 1);   // the unit's last Q K^T is done
         }
         for (int i = 0; i < NSK; ++i) {
             mbar_init(bar(bars.k_full, i), 1);
@@ -291,6 +287,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(bars.s_full, i), 1);
             mbar_init(bar(bars.p_full, i), 256);
             mbar_init(bar(bars.pv_done, i), 1);
+        }
+        mbar_init(smem_addr(&bars.o_free), 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(bars.l_full, i), 256);
+            mbar_init(bar(bars.l_empty, i), 128);
         }
         mbar_init(smem_addr(&bars.done), 1);
         fence_barrier_init();
@@ -383,41 +384,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 report(p.status, PA_ERR_TIMEOUT);
             }
         }
-    } else if (warp == kStoreWarp) {
-        // ---- output: once the softmax warps have staged a unit's rows (fp16,
-        // swizzled, in the unit's Q buffer), store them with tensor copies, rows
-        // split into boxes of 128, 64, ..., 1 so that only the unit's rows are
-        // written; then the Q buffer may take the unit after next
-        bool ok = true;
-        for (int k = 0;; ++k) {
-            Unit u;
-            get_unit(k, u);
-            if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
-            if (u.n_tiles <= 0) {
-                ok = u.n_tiles == 0;
-                break;
-            }
-            if (!warp_all(mbar_wait_bounded(bar(bars.staged, k & 1), (k >> 1) & 1, p.status, true))) {
-                ok = false;
-                break;
-            }
-            const int rows = min(TBM, u.ql - u.q0);
-            // box i covers rows [start_i, start_i + 2^(7-i)) when bit (7-i) of rows is set
-            const int i = lane % kRowMaps, pn = lane / kRowMaps;
-            const int bit = 7 - i;
-            if (pn < NP && ((rows >> bit) & 1)) {
-                const int start = rows & ~((2 << bit) - 1);   // rows covered by larger boxes
-                tma_store_3d(&maps.out[i], pn * 64, u.h, u.q_beg + u.q0 + start,
-                             sQ + (k & 1) * L::TILE + pn * kPanel + (uint32_t)start * 128u,
-                             l2_evict_first_policy());
-            }
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bars.q_empty, k & 1));
-        }
-        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores complete
-        if (!ok) report(p.status, PA_ERR_TIMEOUT);
     } else if (warp == kKWarp || warp == kVWarp) {
         // ---- loaders: lane i issues the TMA copies of block i of a tile
         const bool is_k = warp == kKWarp;
@@ -545,9 +511,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (s_tiles <= 0) s_end = true;
                     progress = true;
                 }
-                // P V of tile gp (its S was issued)
+                // P V of tile gp (its S was issued); a unit's first one overwrites O,
+                // so it also waits for the epilogue to have read the previous unit's
                 if (gp < gs && mbar_test(bar(bars.p_full, gp % NSB), (gp / NSB) & 1) &&
-                    mbar_test(bar(bars.v_full, gp % NSV), (gp / NSV) & 1)) {
+                    mbar_test(bar(bars.v_full, gp % NSV), (gp / NSV) & 1) &&
+                    (tp > 0 || kp == 0 || mbar_test(smem_addr(&bars.o_free), (kp - 1) & 1))) {
                     tc::fence_after();
                     const uint32_t vb = sV + (gp % NSV) * L::TILE;
 #pragma unroll
@@ -614,67 +582,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc::commit(smem_addr(&bars.done));   // lets the teardown wait for every MMA issued
         }
         __syncwarp();
-    } else {
+    } else if (warp < kMmaWarp) {
         // ---- softmax warps: warps w and w + 4 share the query rows of tensor-memory
         // lane quarter w % 4 (row = lane of that quarter); warp w < 4 takes key
-        // columns 0-63 of each tile, warp w + 4 columns 64-127.  A unit's
-        // epilogue runs inside the next unit's first tile, after its P is
-        // written, so the wait for the unit's last P V product overlaps work.
+        // columns 0-63 of each tile, warp w + 4 columns 64-127.  They leave the
+        // loops only together, at a meeting (a unit's start or a tile's maxima
+        // exchange), so that no meeting ever waits for a warp that has gone.
         const int quarter = warp & 3, half = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float qs = p.qscale;
-        bool ok = true;
-        int g = 0;                   // tiles processed so far (all units)
-        int pend_k = -1, pend_g = 0; // unit whose output is still in tensor memory, its last tile
-        float pend_l = 0.f;
-        // normalise this warp's half of the pending unit's rows and stage them
-        // (fp16, 128-byte swizzle, in the unit's Q buffer) for the store warp
-        auto epilogue = [&]() -> bool {
-            if (!warp_all(mbar_wait_bounded(bar(bars.pv_done, pend_g % NSB), (pend_g / NSB) & 1,
-                                            p.status, true)))
-                return false;
-            tc::fence_after();
-            const float inv = 1.f / (pend_l + bars.red_l[pend_k & 1][half ^ 1][row]);
-            const uint32_t stage = sQ + (pend_k & 1) * L::TILE;
-#pragma unroll 1
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t r[32];
-                tc::ld32(lane_base + kOCol + half * (D / 2) + cc * 32, r);
-                tc::wait_ld();
-                // columns half*D/2 + 32cc .. +31: panel and 16-byte chunks within it
-                const int col0 = half * (D / 2) + cc * 32;
-                const uint32_t pbase = stage + (col0 / 64) * kPanel + (uint32_t)row * 128u;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t hv[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half2 v2 = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * e]) * inv,
-                                                             __uint_as_float(r[8 * i + 2 * e + 1]) * inv);
-                        hv[e] = *reinterpret_cast<const uint32_t *>(&v2);
-                    }
-                    const int chunk = ((col0 % 64) >> 3) + i;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     pbase + (uint32_t)((chunk ^ (row & 7)) << 4)),
-                                 "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
-                                 : "memory");
-                }
-            }
-            fence_proxy_async_smem();
-            tc::fence_before();   // O read before the next unit's first product overwrites it
-            mbar_arrive(bar(bars.staged, pend_k & 1));
-            pend_k = -1;
-            return true;
-        };
-        for (int k = 0; ok; ++k) {
+        bool ok = true, stop = false;
+        int g = 0;   // tiles processed so far (all units)
+        for (int k = 0; !stop; ++k) {
             Unit u;
             get_unit(k, u);
             if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
-            if (u.n_tiles <= 0) {
-                ok = u.n_tiles == 0;
-                break;
-            }
+            ok = ok && u.n_tiles >= 0;
+            if (!group_all(3, 256, ok && u.n_tiles > 0)) break;   // end marker or a failure
             const int qi = u.q0 + row;
             const int pos = u.pos0 + min(qi, u.ql - 1);
             float m_run = -INFINITY, l_run = 0.f;
@@ -708,12 +633,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mt *= qs;   // scale > 0: the maximum of the scaled scores
                 }
                 bars.red[g & 1][half][row] = mt;
-                if (t == 0 && pend_k >= 0) bars.red_l[pend_k & 1][half][row] = pend_l;
                 // the two halves of each row meet here once per tile: one exit
-                // decision for all softmax warps, and the partner's maximum (and,
-                // on a unit's first tile, the partner's sum for the pending output)
+                // decision for all softmax warps, and the partner's maximum
                 if (!group_all(3, 256, ok)) {
-                    ok = false;
+                    stop = true;
                     break;
                 }
                 mt = fmaxf(mt, bars.red[g & 1][half ^ 1][row]);
@@ -756,7 +679,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 tc::wait_st();
-                if (t == 0 && pend_k >= 0 && !epilogue()) ok = false;
                 if (__any_sync(0xffffffffu, resc && t > 0)) {
                     // O holds tiles < t of this unit: wait until their product is
                     // complete, then scale this warp's half of the output columns
@@ -782,15 +704,92 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc::fence_before();
                 mbar_arrive(bar(bars.p_full, b));
             }
-            if (!ok) break;
-            pend_k = k;
-            pend_g = g - 1;
-            pend_l = l_run;
+            if (stop) break;
+            // the unit's row sums for the epilogue warps (slot k & 1 is free once
+            // the epilogue of unit k - 2 has read it)
+            if (k >= 2)
+                ok = ok && warp_all(mbar_wait_bounded(bar(bars.l_empty, k & 1), ((k >> 1) - 1) & 1,
+                                                      p.status, true));
+            if (ok) bars.red_l[k & 1][half][row] = l_run;
+            mbar_arrive(bar(bars.l_full, k & 1));
         }
-        if (ok && pend_k >= 0) {
-            // the last unit's output: exchange sums, then stage
-            bars.red_l[pend_k & 1][half][row] = pend_l;
-            ok = group_all(3, 256, true) && epilogue();
+        if (!ok) report(p.status, PA_ERR_TIMEOUT);
+    } else {
+        // ---- epilogue warps 12-15: warp 12 + q takes the rows of tensor-memory
+        // lane quarter q.  After a unit's last P V: read O, normalised and as
+        // fp16, into registers, release O to the next unit's first product, then
+        // write the rows.  Rows past the unit's queries are not written.
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        bool ok = true;
+        int g = 0;   // tiles of this CTA's units so far
+        for (int k = 0; ok; ++k) {
+            Unit u;
+            get_unit(k, u);
+            if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
+            if (u.n_tiles <= 0) {
+                ok = u.n_tiles == 0;
+                break;
+            }
+            g += u.n_tiles;
+            const int last = g - 1;
+            ok = warp_all(mbar_wait_bounded(bar(bars.l_full, k & 1), (k >> 1) & 1, p.status, true));
+            const float inv = ok ? 1.f / (bars.red_l[k & 1][0][row] + bars.red_l[k & 1][1][row]) : 0.f;
+            mbar_arrive(bar(bars.l_empty, k & 1));
+            ok = ok && warp_all(mbar_wait_bounded(bar(bars.pv_done, last % NSB), (last / NSB) & 1,
+                                                  p.status, true));
+            uint32_t hv[D / 2];   // the row as fp16 pairs
+            if (ok) {
+                tc::fence_after();
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    tc::ld32(lane_base + kOCol + cc * 32, r);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        hv[cc * 16 + i] = pack_pair(__uint_as_float(r[2 * i]) * inv,
+                                                    __uint_as_float(r[2 * i + 1]) * inv);
+                }
+            }
+            tc::fence_before();
+            mbar_arrive(smem_addr(&bars.o_free));
+            if (!ok) break;
+            // 16-byte chunks transposed within groups of 8 lanes (an 8 x 8
+            // exchange per 64 columns), so that each store instruction writes 4
+            // whole 128-byte row segments
+            const int qi = u.q0 + row;
+            const unsigned long long mine =
+                qi < u.ql ? reinterpret_cast<unsigned long long>(p.out + ((size_t)(u.q_beg + qi) * H + u.h) * D)
+                          : 0ull;
+            const int c = lane & 7;
+#pragma unroll
+            for (int pass = 0; pass < D / 64; ++pass) {
+                uint32_t *x = hv + pass * 32;   // chunk e = x[4e .. 4e + 3]
+#pragma unroll
+                for (int m = 1; m < 8; m <<= 1) {
+                    const bool up = (c & m) != 0;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (e & m) continue;
+#pragma unroll
+                        for (int wd = 0; wd < 4; ++wd) {
+                            uint32_t &a = x[4 * e + wd], &b2 = x[4 * (e | m) + wd];
+                            const uint32_t r = __shfl_xor_sync(0xffffffffu, up ? a : b2, m);
+                            if (up) a = r; else b2 = r;
+                        }
+                    }
+                }
+                // lane c now holds chunk c of rows (lane - c) + e in x[4e ..]
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const unsigned long long ptr = __shfl_sync(0xffffffffu, mine, (lane & ~7) + e);
+                    if (ptr)
+                        __stcs(reinterpret_cast<uint4 *>(ptr) + pass * 8 + c,
+                               make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]));
+                }
+            }
         }
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
     }
@@ -916,8 +915,6 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
     for (int m = 0; rc == PA_OK && m < kVPartMaps; ++m)
         rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 8 >> m);
     if (rc == PA_OK) rc = encode_map(&maps.q, p.q, 3, (uint64_t)p.q_rows, H, D, TBM);
-    for (int m = 0; rc == PA_OK && m < kRowMaps; ++m)
-        rc = encode_map(&maps.out[m], p.out, 3, (uint64_t)p.q_rows, H, D, TBM >> m);
     if (rc != PA_OK) return rc;
     p.q_tiles = (p.max_q_len + TBM - 1) / TBM;
     paged_prefill_tc<D><<<sms, kTcThreads, TcLayout<D>::BYTES, st>>>(p, maps, n_seqs);
