@@ -775,6 +775,8 @@ def run_prefill(args):
     flops = prefill_flops(ctx.tolist(), lens.tolist(), H, D)
 
     def step(ev=None):
+        if ev is not None:
+            ev[2].record(stream)
         pk.pa_write_kv(k_new, v_new, d_slots, kc, vc, desc, status=status, stream=stream)
         if ev is not None:
             ev[0].record(stream)
@@ -787,8 +789,7 @@ def run_prefill(args):
         for _ in range(args.warmup):
             step()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -801,7 +802,8 @@ def run_prefill(args):
     clk = clocks.stop()
     assert status.item() == 0, status.item()
     el = t0.elapsed_time(t1) / 1e3
-    attn_s = sum(a.elapsed_time(b) for a, b in evs) / len(evs) / 1e3
+    attn_s = sum(a.elapsed_time(b) for a, b, _ in evs) / len(evs) / 1e3
+    wkv_s = sum(c.elapsed_time(a) for a, _, c in evs) / len(evs) / 1e3
     # end to end through the same calls: the step's new K/V and queries come
     # from pinned host memory, the output goes back to it
     h_k, h_v, h_q = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
@@ -851,7 +853,7 @@ def run_prefill(args):
                          "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
                          "algorithmic_flops_per_launch": flops,
                          "attn_ms_per_launch": attn_s * 1e3},
-            "kernels": {"pa_write_kv": {"us_per_launch": (el / args.steps - attn_s) * 1e6,
+            "kernels": {"pa_write_kv": {"us_per_launch": wkv_s * 1e6,
                                         "tokens": T, "algorithmic_bytes": T * H * D * 2 * 4}},
             "e2e": {"value": e2e_tok / e2e_max, "unit": PREFILL_UNIT,
                     "h2d_bytes_per_step": 3 * T * H * D * 2, "d2h_bytes_per_step": T * H * D * 2,
