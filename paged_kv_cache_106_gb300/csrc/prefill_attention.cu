@@ -8,66 +8,38 @@
 // PagedAttention notes (§3.1) evaluated for each of those queries.
 //
 // Kernel design (sm_103a, 5th-generation tensor cores through tcgen05):
-//   - persistent: one CTA per SM walks units of work, a unit being 128
-//     consecutive queries of one (sequence, head); units are taken in the
-//     order (sequence, query tile from the last, head), strided by CTA: all
-//     heads of a query tile run side by side (different keys and values, no
-//     hot spots), and the next tile of the same (sequence, head), which
-//     re-reads a prefix of those keys and values, follows while they are
-//     still in L2 (measured: 5 % faster than interleaving 8 sequences).  Tensor memory,
-//     barriers and the pipeline carry over from unit to unit.  Warp roles:
-//       warps 0-7  softmax and epilogue: query row i is tensor-memory lane i;
-//                  warps w and w + 4 share the 32 rows of lane quarter w % 4,
-//                  each taking half of a tile's key columns, and meet once per
-//                  tile to combine their row maxima;
-//       warp 8     one thread issues every tcgen05.mma and commit, polling its
-//                  dependencies so Q K^T and P V of different tiles interleave;
-//       warp 9     Q rows and K tiles by TMA, warp 10 V tiles by TMA;
-//       warp 11    scheduler: finds this CTA's non-empty units and publishes
-//                  them through a 4-slot descriptor ring;
-//       warps 12-15 epilogue: warp 12 + q normalises and writes the rows of
-//                  lane quarter q once a unit's last P V is done.
-//   - Q (two buffers), K and V (two-stage rings, with the runs of the tile
-//     two steps further prefetched into L2) move in tiles of 128
-//     positions.  Position j lives in block table[j / B] at offset j % B; in
-//     the cache layout [block][head][B][D] each (block, head) run is B*D*2
-//     contiguous bytes.  K and V tiles sit in shared memory as 8-row groups,
-//     [j / 8][64-column panel][j % 8][128 bytes], 128-byte swizzled, so that
-//     a run of B >= 8 rows is whole groups: a loader lane per block moves it
-//     with one 4-D TMA copy (at D = 128, 4 KB at B = 16; per-SM copy
-//     throughput is higher for bigger boxes, and the copies bound the loop)
-//     and it lands already in the layout the tensor cores read (the swizzle
-//     follows the shared-memory address).  At B = 4, or D = 64, one 2-D copy
-//     per panel (box 64 x B).  The same bytes are the K-major B operand of
-//     S = Q K^T (8-row groups D/64 KB apart) and the MN-major B operand of
-//     O = P V (panels 1 KB apart).  The V block holding the context's last
-//     position is copied up to it in boxes of 8, 4, 2 and 1 rows, and the V
-//     ring starts zeroed, so slots past the context are never read.  Q
-//     arrives as one 128-row box per panel of a [rows][H][D] tensor map, in
-//     [panel][128 rows] layout (rows past q_rows read as zeros).
-//   - tensor memory (512 columns): three 128-column S buffers, so Q K^T for
-//     tile t+2 runs while tile t is in softmax, and the fp32 output
-//     accumulator O (D columns).  Softmax overwrites its S buffer with P as
-//     fp16 pairs, which the P V product reads as its A operand straight from
-//     tensor memory.
-//   - the softmax is online, in base 2 (ex2.approx), with a lazy rescale: a row's
-//     reference maximum moves only when a tile raises it by more than 2^8,
-//     so O is rescaled in tensor memory rarely.  P (<= 2^8) enters P V as
-//     fp16, 11 significant bits like the output: rounding p perturbs each
-//     weight by at most 2^-12 relative, and the fp16 rounding of the output
-//     stays the larger error (simulated: max |error| 1.03e-3 against 0.98e-3
-//     with exact p, for prompts up to 1536 and peaked scores).
-//   - blocks past the causal end of a tile are not copied; scores of keys
-//     after a row's own position are masked to -inf (a select, so stale
-//     shared memory there cannot leak in).
-//   - the epilogue warps wait for a unit's last P V, read O from tensor
-//     memory into registers (normalised, as fp16) and release it to the next
-//     unit's first P V, which overwrites O; so the tensor pipe idles at a
-//     unit boundary only for that read, and the softmax warps never stop
-//     for an epilogue.  They write the rows with 16-byte streaming stores,
-//     exchanged within groups of 8 lanes so that each store instruction
-//     covers 4 whole 128-byte row segments (only the unit's rows).  A Q
-//     buffer is free as soon as its unit's last Q K^T is done.
+//   - persistent: one CTA per SM walks units of work; a unit is one or two
+//     query tiles (128 queries each) of one (sequence, head): tiles x and
+//     x - 1 of a prompt share their keys and values, so each K/V tile is
+//     copied once for both.  Each query tile has a slot: a Q buffer, S and O
+//     in tensor memory (S0, S1, O0, O1: 128 columns each) and a softmax
+//     warpgroup; a unit with one query tile takes the slots in turn.
+//       warps 0-3 / 4-7  softmax of slot 0 / 1, one query row per thread;
+//       warp 8     one thread issues every tcgen05.mma and commit, in the
+//                  order P V (slot 0), Q K^T of the next key tile (slot 0),
+//                  then the same for slot 1, so one slot's products run on
+//                  the tensor pipe while the other slot's softmax works;
+//       warp 9     Q tiles and K tiles by TMA, warp 10 V tiles by TMA;
+//       warp 11    scheduler: publishes this CTA's non-empty units through a
+//                  4-slot descriptor ring;
+//       warps 12-15 epilogue: normalise and write a job's rows once its last
+//                  P V is done, releasing O to the slot's next job.
+//   - K and V tiles sit in shared memory as 8-row groups, [j / 8][64-column
+//     panel][j % 8][128 bytes], 128-byte swizzled; a (block, head) run of
+//     B >= 8 rows is whole groups and one 4-D TMA copy moves it (at D = 128;
+//     at B = 4 or D = 64, one 2-D copy per panel).  The same bytes are the
+//     K-major B operand of S = Q K^T and the MN-major B operand of O = P V.
+//     The V block holding the context's last position is copied up to it in
+//     boxes of 8, 4, 2 and 1 rows, and the V ring starts zeroed, so slots
+//     past the context are never read.
+//   - the softmax is online, in base 2 (ex2.approx), with a lazy rescale: a
+//     row's reference maximum moves only when a tile raises it by more than
+//     2^8.  P (<= 2^8) is written over S as fp16 and read by P V straight
+//     from tensor memory; fp16, like the output, keeps the output rounding
+//     the larger error.
+//   - keys after a row's own position are masked to -inf (a select, so
+//     stale shared memory cannot leak in); blocks past the causal end of a
+//     tile are not copied.
 //   - every mbarrier wait is bounded; a wait that runs out reports
 //     PA_ERR_TIMEOUT, and the CTA drains its MMAs (bounded) and frees its
 //     tensor memory before it returns.
@@ -95,7 +67,7 @@ struct PrefillParams {
     const int32_t *tables;
     const int32_t *ctx_lens;
     const int32_t *q_starts;
-    int32_t num_heads, num_blocks, max_blocks, max_q_len, q_rows, q_tiles, bshift;
+    int32_t num_heads, num_blocks, max_blocks, max_q_len, q_rows, q_pairs, bshift;
     float qscale;  // scale * log2(e): softmax evaluated with exp2
     int32_t *status;
 };
@@ -106,19 +78,6 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// Barrier among `count` threads of the CTA (ids 1.. are free; 0 is
-// __syncthreads) that also returns whether `v` held for all of them.
-__device__ __forceinline__ bool group_all(int id, int count, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
 }
 
 // 2-D tensor copy global -> shared (box of the tensor map at element
@@ -146,22 +105,21 @@ __device__ __forceinline__ uint32_t pack_pair(float p0, float p1) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-constexpr int TBM = 128;          // queries per unit (= tensor-memory lanes)
-constexpr int TBN = 128;          // key positions per tile
-constexpr int NSB = 3;            // S buffers in tensor memory
+constexpr int TBM = 128;          // queries per query tile (= tensor-memory lanes)
+constexpr int TBN = 128;          // key positions per key tile
 constexpr int NSK = 2;            // K ring stages
 constexpr int NSV = 2;            // V ring stages
 constexpr int NU = 4;             // unit descriptors in flight
-constexpr int kMmaWarp = 8, kKWarp = 9, kVWarp = 10, kSchedWarp = 11;   // 12-15: epilogue
+// warps 0-3: softmax of slot 0, 4-7: softmax of slot 1, 12-15: epilogue
+constexpr int kMmaWarp = 8, kKWarp = 9, kVWarp = 10, kSchedWarp = 11;
 constexpr int kTcThreads = 512;   // 16 warps
 constexpr uint32_t kPanel = TBM * 128;   // bytes of one 64-column panel of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = NSB * 128;    // output accumulator after the S buffers
+constexpr uint32_t kOCol = 256;          // S of slot x at columns 128 x, its O at kOCol + 128 x
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
 // readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, 4 epilogue warps
 constexpr uint32_t kUnitReaders = 3 + 8 + 4;
 constexpr int kPrefetchTiles = 2;  // K/V tiles prefetched into L2 ahead of their copies
-constexpr int kSeqGroup = 1;     // sequences whose query tiles are interleaved (L2 reuse)
 constexpr int kVPartMaps = 4;     // boxes of 8, 4, 2, 1 cache rows for a partial V block
 
 template <int D>
@@ -183,9 +141,14 @@ __device__ __forceinline__ uint32_t kv_row_off(uint32_t r) {
     return (r >> 3) * (uint32_t)(D / 64) * 1024u + (r & 7u) * 128u;
 }
 
-// One unit of work: 128 queries of one (sequence, head).
+// One unit of work: one or two query tiles of one (sequence, head) that share
+// their keys and values, each on a slot (tensor-memory S and O, a Q buffer
+// and a softmax warpgroup of its own).  A pair is query tiles x and x - 1;
+// slot 0 takes x (the one with the most keys).
 struct Unit {
-    int32_t s, h, q0, q_beg, ql, pos0, n_end, n_tiles;   // n_tiles == 0: no more units
+    int32_t s, h, q_beg, ql, pos0;
+    int32_t n_end, n_tiles;   // keys of the unit (its slots' union) and their key tiles; 0: no more units
+    int32_t q0[2], nt[2];     // per slot: first query (within the prompt) and key tiles; nt 0: no job
 };
 
 // Tensor maps: K and V cache runs (D = 128 with B >= 8: a 4-D view
@@ -199,31 +162,18 @@ struct TcMaps {
 
 struct TcBars {
     uint64_t unit_full[NU], unit_empty[NU];
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full[2], q_empty[2];           // per slot
     uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-    uint64_t s_full[NSB], p_full[NSB], pv_done[NSB];
-    uint64_t o_free;               // the epilogue has read a unit's O (one phase per unit)
-    uint64_t l_full[2], l_empty[2]; // a unit's row sums (slot k & 1) written / read
+    uint64_t s_full[2], p_full[2];            // per slot: S written, P written
+    uint64_t o_full[2], o_free[2];            // per slot: a job's O complete, read by the epilogue
+    uint64_t l_full[2][2], l_empty[2][2];     // per slot and job parity: row sums written, read
     uint64_t done;
     uint32_t tmem;
     Unit unit[NU];
-    float red[2][2][TBM];   // per tile parity and column half: row maxima
-    float red_l[2][2][TBM]; // per unit parity and column half: a finished unit's row sums
+    float red_l[2][2][TBM];                   // per slot and job parity: a finished job's row sums
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
-
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 
 __device__ __forceinline__ void zero_smem(uint32_t addr, uint32_t bytes, int lane) {
     for (uint32_t o = (uint32_t)lane * 16u; o < bytes; o += 32u * 16u)
@@ -248,11 +198,11 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
 }
 
 // Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
-// of the list ordered by group of kSeqGroup sequences, then query tile (the
-// last, with the most keys, first), then sequence, then head; a scheduler
-// warp skips the empty ones.  The query tiles of one (sequence, head) come
-// about H units apart, while the keys and values they share are still in L2,
-// and concurrent CTAs work on different (sequence, head).
+// of the list ordered by sequence, then query-tile pair (the last, with the
+// most keys, first), then head; a scheduler warp skips the empty ones.  All
+// heads of a pair run side by side on different SMs (different keys and
+// values), and the next pair of the same (sequence, head), which re-reads a
+// prefix of its keys and values, follows while they are still in L2.
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc(const PrefillParams p, const __grid_constant__ TcMaps maps, int32_t n_seqs) {
@@ -271,9 +221,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(bars.unit_full, i), 1);
             mbar_init(bar(bars.unit_empty, i), kUnitReaders);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(bars.q_full, i), 1);
-            mbar_init(bar(bars.q_empty, i), 1);   // the unit's last Q K^T is done
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(bars.q_full, x), 1);
+            mbar_init(bar(bars.q_empty, x), 1);   // the job's last Q K^T is done
+            mbar_init(bar(bars.s_full, x), 1);
+            mbar_init(bar(bars.p_full, x), 128);  // the slot's softmax threads
+            mbar_init(bar(bars.o_full, x), 1);
+            mbar_init(bar(bars.o_free, x), 128);  // the epilogue threads
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(bar(bars.l_full[x], i), 128);
+                mbar_init(bar(bars.l_empty[x], i), 128);
+            }
         }
         for (int i = 0; i < NSK; ++i) {
             mbar_init(bar(bars.k_full, i), 1);
@@ -282,16 +240,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = 0; i < NSV; ++i) {
             mbar_init(bar(bars.v_full, i), 1);
             mbar_init(bar(bars.v_empty, i), 1);
-        }
-        for (int i = 0; i < NSB; ++i) {
-            mbar_init(bar(bars.s_full, i), 1);
-            mbar_init(bar(bars.p_full, i), 256);
-            mbar_init(bar(bars.pv_done, i), 1);
-        }
-        mbar_init(smem_addr(&bars.o_free), 128);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(bars.l_full, i), 256);
-            mbar_init(bar(bars.l_empty, i), 128);
         }
         mbar_init(smem_addr(&bars.done), 1);
         fence_barrier_init();
@@ -305,7 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = bars.tmem;
-    const int q_tiles = p.q_tiles;
+    const int q_pairs = p.q_pairs;
 
     // Reads unit k of this CTA from the ring (bounded wait); n_tiles < 0 on timeout.
     auto get_unit = [&](int k, Unit &u) {
@@ -320,54 +268,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kSchedWarp) {
         // ---- scheduler: lanes test 32 candidate units at a time, the valid ones
-        // are published in order
-        const long long V = (long long)n_seqs * H * q_tiles;
-        const long long group_units = (long long)kSeqGroup * H * q_tiles;
-        int k = 0;
+        // are published in order; a unit with one query tile takes the slots in
+        // turn, so that consecutive such units overlap
+        const long long V = (long long)n_seqs * H * q_pairs;
+        int k = 0, singles = 0;
         bool ok = true;
         for (long long base_v = blockIdx.x; ok && base_v < V; base_v += 32ll * gridDim.x) {
             const long long v = base_v + (long long)lane * gridDim.x;
             Unit u{};
             bool valid = false;
             if (v < V) {
-                // v -> (group of kSeqGroup sequences, query tile from the last,
-                // sequence in the group, head)
-                const int grp = (int)(v / group_units);
-                const int gsz = min(kSeqGroup, n_seqs - grp * kSeqGroup);
-                const long long r = v - (long long)grp * group_units;
-                const int x = (int)(r / ((long long)gsz * H));
-                const int r2 = (int)(r - (long long)x * gsz * H);
-                u.s = grp * kSeqGroup + r2 / H;
-                u.h = r2 - (r2 / H) * H;
-                const int qt = q_tiles - 1 - x;
+                // v -> (sequence, pair of query tiles from the last, head)
+                u.s = (int)(v / ((long long)H * q_pairs));
+                const int r = (int)(v - (long long)u.s * H * q_pairs);
+                const int pr = r / H;
+                u.h = r - pr * H;
                 u.q_beg = p.q_starts[u.s];
                 u.ql = p.q_starts[u.s + 1] - u.q_beg;
                 const int ctx = p.ctx_lens[u.s];
                 const bool bad_len = u.ql < 0 || u.ql > ctx || u.ql > p.max_q_len ||
                                      u.q_beg < 0 || (int64_t)u.q_beg + u.ql > p.q_rows;
                 const bool bad_ctx = (int64_t)ctx > ((int64_t)p.max_blocks << p.bshift);
-                if ((bad_len || bad_ctx) && x == 0 && u.h == 0)
+                if ((bad_len || bad_ctx) && pr == 0 && u.h == 0)
                     report(p.status, bad_len ? PA_ERR_INVALID_ARG : PA_ERR_BAD_BLOCK);
-                u.q0 = qt * TBM;
-                valid = !bad_len && !bad_ctx && u.q0 < u.ql;
+                const int xa = (u.ql + TBM - 1) / TBM - 1 - 2 * pr;   // the pair's later query tile
+                valid = !bad_len && !bad_ctx && xa >= 0;
                 if (valid) {
                     u.pos0 = ctx - u.ql;
-                    u.n_end = u.pos0 + u.q0 + min(TBM, u.ql - u.q0);
-                    u.n_tiles = (u.n_end + TBN - 1) / TBN;
+                    for (int x = 0; x < 2; ++x) {
+                        const int qt = xa - x;
+                        u.q0[x] = qt * TBM;
+                        const int end = u.pos0 + u.q0[x] + min(TBM, u.ql - u.q0[x]);
+                        u.nt[x] = qt >= 0 ? (end + TBN - 1) / TBN : 0;
+                    }
+                    u.n_end = u.pos0 + u.q0[0] + min(TBM, u.ql - u.q0[0]);
+                    u.n_tiles = u.nt[0];
                 }
             }
             uint32_t mask = __ballot_sync(0xffffffffu, valid);
             while (mask) {
                 const int src = __ffs(mask) - 1;
                 mask &= mask - 1;
+                const bool single = __shfl_sync(0xffffffffu, u.nt[1] == 0, src);
                 if (k >= NU)
                     ok = warp_all(mbar_wait_bounded(bar(bars.unit_empty, k % NU),
                                                     ((k / NU) - 1) & 1, p.status, true));
                 if (!ok) break;
                 if (lane == src) {
+                    if (single && (singles & 1)) {   // the lone tile goes to slot 1
+                        u.q0[1] = u.q0[0];
+                        u.nt[1] = u.nt[0];
+                        u.nt[0] = 0;
+                    }
                     bars.unit[k % NU] = u;
                     mbar_arrive(bar(bars.unit_full, k % NU));
                 }
+                singles += single ? 1 : 0;
                 __syncwarp();
                 ++k;
             }
@@ -385,7 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     } else if (warp == kKWarp || warp == kVWarp) {
-        // ---- loaders: lane i issues the TMA copies of block i of a tile
+        // ---- loaders: lane i issues the TMA copies of block i of a key tile
         const bool is_k = warp == kKWarp;
         const uint32_t run_bytes = (uint32_t)B * 128u * NP;
         const CUtensorMap *map = is_k ? &maps.k : &maps.v;
@@ -393,9 +349,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint64_t *empty = is_k ? bars.k_empty : bars.v_empty;
         const uint32_t ring = is_k ? sK : sV;
         const int NS = is_k ? NSK : NSV;
-        const int nb = TBN >> p.bshift;   // blocks per tile (tiles start on a block)
+        const int nb = TBN >> p.bshift;   // blocks per key tile (tiles start on a block)
         const uint64_t keep = l2_policy_evict_last();
-        int g = 0;                        // tiles issued so far (all units)
+        int g = 0;                        // key tiles issued so far (all units)
+        int job[2] = {0, 0};              // Q tiles loaded per slot (K loader)
         bool ok = true;
         for (int k = 0; ok; ++k) {
             Unit u;
@@ -407,21 +364,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             const int32_t *table = p.tables + (size_t)u.s * p.max_blocks;
             if (is_k) {
-                // the unit's 128 query rows of head h (rows past the end of q read
+                // each slot's 128 query rows of head h, into the slot's Q buffer once
+                // its previous job's last Q K^T is done (rows past the end of q read
                 // as zeros; rows of the next sequence are harmless: never stored)
-                const int qb = k & 1;
-                if (k >= 2)
-                    ok = warp_all(mbar_wait_bounded(bar(bars.q_empty, qb), ((k >> 1) - 1) & 1,
-                                                    p.status, true));
-                if (!ok) break;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(bars.q_full, qb), L::TILE);
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (u.nt[x] == 0) continue;
+                    if (job[x] >= 1)
+                        ok = warp_all(mbar_wait_bounded(bar(bars.q_empty, x), (job[x] - 1) & 1,
+                                                        p.status, true));
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar(bars.q_full, x), L::TILE);
 #pragma unroll
-                    for (int pn = 0; pn < NP; ++pn)
-                        tma_load_3d(sQ + qb * L::TILE + pn * kPanel, &maps.q, pn * 64, u.h,
-                                    u.q_beg + u.q0, bar(bars.q_full, qb), l2_evict_first_policy());
+                        for (int pn = 0; pn < NP; ++pn)
+                            tma_load_3d(sQ + x * L::TILE + pn * kPanel, &maps.q, pn * 64, u.h,
+                                        u.q_beg + u.q0[x], bar(bars.q_full, x), l2_evict_first_policy());
+                    }
+                    __syncwarp();
+                    ++job[x];
                 }
-                __syncwarp();
+                if (!ok) break;
             }
             // block ids are read one tile ahead (and the runs of the tile
             // kPrefetchTiles ahead prefetched into L2), so that neither the table
@@ -491,155 +453,140 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
     } else if (warp == kMmaWarp) {
-        // ---- one thread issues the MMAs; it polls its dependencies so that a
-        // P V product never waits behind the next unit's Q K^T
+        // ---- one thread issues the MMAs in a fixed order, per key tile j of a
+        // unit: P V of slot 0, then its Q K^T of key tile j + 1, then the same
+        // for slot 1.  A Q K^T that overwrites a slot's S (where its P lies) is
+        // issued right after the P V that reads that P: tcgen05.mma operations
+        // of one thread execute in issue order.  While slot 0's softmax works,
+        // the tensor pipe runs slot 1's products, and the other way round.
         if (lane == 0) {
             constexpr uint32_t idS = tc::idesc_f16(TBM, TBN, false);
             constexpr uint32_t idO = tc::idesc_f16(TBM, D, true);
-            int ks = 0, ts = 0, gs = 0;   // S cursor: unit, tile in unit, global tile
-            int kp = 0, tp = 0, gp = 0;   // P V cursor
-            int s_tiles = -1;             // tiles of the S cursor's unit; -1: not read yet
-            bool s_end = false, ok = true;
-            uint64_t last = globaltimer_ns();
-            uint32_t idle = 0;   // passes without progress
-            while (ok) {
-                bool progress = false;
-                // read the S cursor's unit once it is published
-                if (!s_end && s_tiles < 0 &&
-                    mbar_test(bar(bars.unit_full, ks % NU), (ks / NU) & 1)) {
-                    s_tiles = bars.unit[ks % NU].n_tiles;
-                    if (s_tiles <= 0) s_end = true;
-                    progress = true;
-                }
-                // P V of tile gp (its S was issued); a unit's first one overwrites O,
-                // so it also waits for the epilogue to have read the previous unit's
-                if (gp < gs && mbar_test(bar(bars.p_full, gp % NSB), (gp / NSB) & 1) &&
-                    mbar_test(bar(bars.v_full, gp % NSV), (gp / NSV) & 1) &&
-                    (tp > 0 || kp == 0 || mbar_test(smem_addr(&bars.o_free), (kp - 1) & 1))) {
-                    tc::fence_after();
-                    const uint32_t vb = sV + (gp % NSV) * L::TILE;
+            int g = 0;                    // key tiles of the units so far (K/V ring position)
+            int job[2] = {0, 0};          // jobs started per slot
+            int pc[2] = {0, 0};           // P tiles consumed per slot
+            bool ok = true;
+            auto wait = [&](uint32_t b, uint32_t par) {
+                if (ok) ok = mbar_wait_bounded(b, par, p.status, true);
+                return ok;
+            };
+            // S_x = Q_x K^T for the key tile in K ring stage st
+            auto issue_s = [&](int x, int st) {
+                const uint32_t qb = sQ + x * L::TILE, kb = sK + st * L::TILE;
 #pragma unroll
-                    for (int kk = 0; kk < TBN / 16; ++kk) {
-                        // 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart
-                        const uint64_t dv = tc::smem_desc(vb + kk * 2048u * NP, 1024, 1024u * NP);
-                        // P of keys 16 kk .. 16 kk + 15: column half (kk / 4) * 64, then
-                        // 16 columns per 32 keys, 8 columns (16 fp16) per slice
-                        const uint32_t pa = tmem + (gp % NSB) * 128 + (kk >> 2) * 64 +
-                                            ((kk >> 1) & 1) * 16 + (kk & 1) * 8;
-                        tc::mma_ts(tmem + kOCol, pa, dv, idO, (tp > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc::commit(bar(bars.v_empty, gp % NSV));
-                    tc::commit(bar(bars.pv_done, gp % NSB));
-                    ++gp;
-                    if (++tp == bars.unit[kp % NU].n_tiles) {   // unit kp done for this thread
-                        mbar_arrive(bar(bars.unit_empty, kp % NU));
-                        ++kp;
-                        tp = 0;
-                    }
-                    progress = true;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // Q: [panel][128 rows]; K: 8-row groups of NP panels
+                    const uint32_t col = (kk & 3) * 32;
+                    tc::mma_ss(tmem + x * 128, tc::smem_desc(qb + (kk >> 2) * kPanel + col, 16, 1024),
+                               tc::smem_desc(kb + (kk >> 2) * 1024u + col, 16, 1024u * NP), idS,
+                               kk > 0 ? 1u : 0u);
                 }
-                // Q K^T of tile gs: buffer gs % NSB is free once P V of gs - NSB is done
-                if (!s_end && s_tiles > 0 && gs < gp + NSB &&
-                    (ts > 0 || mbar_test(bar(bars.q_full, ks & 1), (ks >> 1) & 1)) &&
-                    mbar_test(bar(bars.k_full, gs % NSK), (gs / NSK) & 1) &&
-                    (gs < NSB || mbar_test(bar(bars.pv_done, gs % NSB), ((gs - NSB) / NSB) & 1))) {
+                tc::commit(bar(bars.s_full, x));
+            };
+            for (int k = 0; ok; ++k) {
+                if (!wait(bar(bars.unit_full, k % NU), (k / NU) & 1)) break;
+                const Unit u = bars.unit[k % NU];
+                mbar_arrive(bar(bars.unit_empty, k % NU));
+                if (u.n_tiles <= 0) break;
+                // first key tile: S of each slot with a job
+                if (!wait(bar(bars.k_full, g % NSK), (g / NSK) & 1)) break;
+                for (int x = 0; x < 2; ++x) {
+                    if (u.nt[x] == 0) continue;
+                    if (!wait(bar(bars.q_full, x), job[x] & 1)) break;
                     tc::fence_after();
-                    const uint32_t qb = sQ + (ks & 1) * L::TILE, kb = sK + (gs % NSK) * L::TILE;
+                    issue_s(x, g % NSK);
+                    if (u.nt[x] == 1) tc::commit(bar(bars.q_empty, x));
+                }
+                tc::commit(bar(bars.k_empty, g % NSK));
+                for (int j = 0; ok && j < u.n_tiles; ++j) {
+                    const int gj = g + j;
+                    if (!wait(bar(bars.v_full, gj % NSV), (gj / NSV) & 1)) break;
+                    bool k_next = false;   // key tile j + 1 waited for
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= u.nt[x]) continue;
+                        if (!wait(bar(bars.p_full, x), pc[x] & 1)) break;
+                        ++pc[x];
+                        // a job's first P V overwrites O: the epilogue must have read
+                        // the slot's previous job
+                        if (j == 0 && job[x] > 0 && !wait(bar(bars.o_free, x), (job[x] - 1) & 1)) break;
+                        tc::fence_after();
+                        const uint32_t vb = sV + (gj % NSV) * L::TILE;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        // Q: [panel][128 rows]; K: 8-row groups of NP panels
-                        const uint32_t col = (kk & 3) * 32;
-                        tc::mma_ss(tmem + (gs % NSB) * 128,
-                                   tc::smem_desc(qb + (kk >> 2) * kPanel + col, 16, 1024),
-                                   tc::smem_desc(kb + (kk >> 2) * 1024u + col, 16, 1024u * NP), idS,
-                                   kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < TBN / 16; ++kk) {
+                            // V: 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart.
+                            // P of keys 16 kk .. 16 kk + 15: 8 columns (16 fp16) at 8 kk
+                            const uint64_t dv = tc::smem_desc(vb + kk * 2048u * NP, 1024, 1024u * NP);
+                            tc::mma_ts(tmem + kOCol + x * 128, tmem + x * 128 + kk * 8, dv, idO,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (j + 1 < u.nt[x]) {
+                            if (!k_next && !wait(bar(bars.k_full, (gj + 1) % NSK), ((gj + 1) / NSK) & 1)) break;
+                            k_next = true;
+                            tc::fence_after();
+                            issue_s(x, (gj + 1) % NSK);
+                            if (j + 2 == u.nt[x]) tc::commit(bar(bars.q_empty, x));   // its last Q K^T
+                        } else {
+                            tc::commit(bar(bars.o_full, x));   // the job's O is complete
+                            ++job[x];
+                        }
                     }
-                    tc::commit(bar(bars.s_full, gs % NSB));
-                    tc::commit(bar(bars.k_empty, gs % NSK));
-                    ++gs;
-                    if (++ts == s_tiles) {   // last Q K^T of the unit: its Q buffer may go
-                        tc::commit(bar(bars.q_empty, ks & 1));
-                        ++ks;
-                        ts = 0;
-                        s_tiles = -1;
-                    }
-                    progress = true;
+                    if (!ok) break;
+                    tc::commit(bar(bars.v_empty, gj % NSV));
+                    if (k_next) tc::commit(bar(bars.k_empty, (gj + 1) % NSK));
                 }
-                if (s_end && gp == gs) break;   // every issued tile has its product
-                // timeout check every 256 idle passes (reading the timer is not free)
-                if (progress) {
-                    idle = 0;
-                } else if ((++idle & 255) == 0) {
-                    const uint64_t now = globaltimer_ns();
-                    if (idle == 256) last = now;
-                    if (now - last > kWaitLimitNs ||
-                        *(volatile const int32_t *)p.status == PA_ERR_TIMEOUT)
-                        ok = false;
-                }
+                g += u.n_tiles;
             }
             if (!ok) report(p.status, PA_ERR_TIMEOUT);
-            if (s_end) mbar_arrive(bar(bars.unit_empty, ks % NU));   // the end marker's slot
             tc::commit(smem_addr(&bars.done));   // lets the teardown wait for every MMA issued
         }
         __syncwarp();
     } else if (warp < kMmaWarp) {
-        // ---- softmax warps: warps w and w + 4 share the query rows of tensor-memory
-        // lane quarter w % 4 (row = lane of that quarter); warp w < 4 takes key
-        // columns 0-63 of each tile, warp w + 4 columns 64-127.  They leave the
-        // loops only together, at a meeting (a unit's start or a tile's maxima
-        // exchange), so that no meeting ever waits for a warp that has gone.
-        const int quarter = warp & 3, half = warp >> 2;
+        // ---- softmax: warps 4x .. 4x + 3 serve slot x; warp w takes the 32 query
+        // rows of tensor-memory lane quarter w % 4, one row per thread, all 128
+        // key columns of each tile
+        const int x = warp >> 2, quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t sb = lane_base + x * 128, ob = lane_base + kOCol + x * 128;
         const float qs = p.qscale;
-        bool ok = true, stop = false;
-        int g = 0;   // tiles processed so far (all units)
-        for (int k = 0; !stop; ++k) {
+        bool ok = true;
+        int job = 0, sc = 0;   // jobs and S tiles of this slot so far
+        for (int k = 0; ok; ++k) {
             Unit u;
             get_unit(k, u);
             if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
-            ok = ok && u.n_tiles >= 0;
-            if (!group_all(3, 256, ok && u.n_tiles > 0)) break;   // end marker or a failure
-            const int qi = u.q0 + row;
-            const int pos = u.pos0 + min(qi, u.ql - 1);
+            if (u.n_tiles <= 0) {
+                ok = u.n_tiles == 0;
+                break;
+            }
+            if (u.nt[x] == 0) continue;
+            const int q0 = u.q0[x];
+            const int pos = u.pos0 + min(q0 + row, u.ql - 1);   // this row's position
             float m_run = -INFINITY, l_run = 0.f;
-            for (int t = 0; t < u.n_tiles; ++t, ++g) {
-                const int b = g % NSB;
-                ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, b), (g / NSB) & 1, p.status, true));
-                const uint32_t sb = lane_base + b * 128 + half * 64;
-                const int n0 = t * TBN + half * 64;   // first key of this warp's columns
-                // keys past this row's position are masked: key n0 + 32 cc + i with i > lim
-                const bool need_mask = n0 + 63 > u.pos0 + u.q0;
-                float mt = -INFINITY;
-                if (ok) {
-                    tc::fence_after();
+            for (int t = 0; ok && t < u.nt[x]; ++t, ++sc) {
+                ok = warp_all(mbar_wait_bounded(bar(bars.s_full, x), sc & 1, p.status, true));
+                if (!ok) break;
+                tc::fence_after();
+                const int n0 = t * TBN;
+                // keys past a row's position are masked: key n0 + 32 cc + i with i > lim
+                const bool need_mask = n0 + TBN - 1 > u.pos0 + q0;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t r[32];
-                        tc::ld32(sb + cc * 32, r);
-                        tc::wait_ld();
-                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                        if (need_mask) {
-                            const int lim = pos - (n0 + cc * 32);
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t r[32];
+                    tc::ld32(sb + cc * 32, r);
+                    tc::wait_ld();
+                    if (need_mask) {
+                        const int lim = pos - (n0 + cc * 32);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
-                        } else {
+                        for (int i = 0; i < 32; ++i)
+                            m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
+                    } else {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
-                        }
-                        mt = fmaxf(mt, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
                     }
-                    mt *= qs;   // scale > 0: the maximum of the scaled scores
                 }
-                bars.red[g & 1][half][row] = mt;
-                // the two halves of each row meet here once per tile: one exit
-                // decision for all softmax warps, and the partner's maximum
-                if (!group_all(3, 256, ok)) {
-                    stop = true;
-                    break;
-                }
-                mt = fmaxf(mt, bars.red[g & 1][half ^ 1][row]);
+                const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qs;   // scale > 0
                 float corr = 1.f;
                 const bool resc = mt > m_run + kRescaleLog2;
                 if (resc) {
@@ -649,7 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                for (int cc = 0; cc < 2; ++cc) {
+                for (int cc = 0; cc < 4; ++cc) {
                     uint32_t r[32], w[16];
                     tc::ld32(sb + cc * 32, r);
                     tc::wait_ld();
@@ -674,56 +621,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             w[i] = pack_pair(p0, p1);
                         }
                     }
-                    // P of these 32 keys as 16 fp16 pairs over S columns already read
+                    // P of these 32 keys as 16 fp16 pairs, over S columns already read
                     tc::st16(sb + cc * 16, w);
                 }
                 l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
                 tc::wait_st();
                 if (__any_sync(0xffffffffu, resc && t > 0)) {
-                    // O holds tiles < t of this unit: wait until their product is
-                    // complete, then scale this warp's half of the output columns
-                    if (warp_all(mbar_wait_bounded(bar(bars.pv_done, (g - 1) % NSB),
-                                                   ((g - 1) / NSB) & 1, p.status, true))) {
-                        tc::fence_after();
+                    // O holds the job's tiles < t, complete (S of tile t was committed
+                    // after their products): scale this thread's row
 #pragma unroll 1
-                        for (int cc = 0; cc < D / 64; ++cc) {
-                            const uint32_t oc = lane_base + kOCol + half * (D / 2) + cc * 32;
-                            uint32_t r[32];
-                            tc::ld32(oc, r);
-                            tc::wait_ld();
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tc::ld32(ob + cc * 32, r);
+                        tc::wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-                            tc::st32(oc, r);
-                        }
-                        tc::wait_st();
-                    } else {
-                        ok = false;   // every softmax warp leaves at the next meeting
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+                        tc::st32(ob + cc * 32, r);
                     }
+                    tc::wait_st();
                 }
                 tc::fence_before();
-                mbar_arrive(bar(bars.p_full, b));
+                mbar_arrive(bar(bars.p_full, x));
             }
-            if (stop) break;
-            // the unit's row sums for the epilogue warps (slot k & 1 is free once
-            // the epilogue of unit k - 2 has read it)
-            if (k >= 2)
-                ok = ok && warp_all(mbar_wait_bounded(bar(bars.l_empty, k & 1), ((k >> 1) - 1) & 1,
-                                                      p.status, true));
-            if (ok) bars.red_l[k & 1][half][row] = l_run;
-            mbar_arrive(bar(bars.l_full, k & 1));
+            if (!ok) break;
+            // the job's row sums for the epilogue (slot job & 1 is free once the
+            // epilogue has read the sums of job - 2)
+            const int jb = job & 1;
+            if (job >= 2)
+                ok = warp_all(mbar_wait_bounded(bar(bars.l_empty[x], jb), ((job >> 1) - 1) & 1,
+                                                p.status, true));
+            if (!ok) break;
+            bars.red_l[x][jb][row] = l_run;
+            mbar_arrive(bar(bars.l_full[x], jb));
+            ++job;
         }
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
     } else {
-        // ---- epilogue warps 12-15: warp 12 + q takes the rows of tensor-memory
-        // lane quarter q.  After a unit's last P V: read O, normalised and as
-        // fp16, into registers, release O to the next unit's first product, then
-        // write the rows.  Rows past the unit's queries are not written.
+        // ---- epilogue: warp 12 + q takes the rows of tensor-memory lane quarter q.
+        // For each job: the row sums, then (once the job's last P V is done) O,
+        // normalised and as fp16, into registers; O is then released to the
+        // slot's next job, and the rows are written (only the unit's queries).
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        int job[2] = {0, 0};
         bool ok = true;
-        int g = 0;   // tiles of this CTA's units so far
         for (int k = 0; ok; ++k) {
             Unit u;
             get_unit(k, u);
@@ -732,62 +674,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = u.n_tiles == 0;
                 break;
             }
-            g += u.n_tiles;
-            const int last = g - 1;
-            ok = warp_all(mbar_wait_bounded(bar(bars.l_full, k & 1), (k >> 1) & 1, p.status, true));
-            const float inv = ok ? 1.f / (bars.red_l[k & 1][0][row] + bars.red_l[k & 1][1][row]) : 0.f;
-            mbar_arrive(bar(bars.l_empty, k & 1));
-            ok = ok && warp_all(mbar_wait_bounded(bar(bars.pv_done, last % NSB), (last / NSB) & 1,
-                                                  p.status, true));
-            uint32_t hv[D / 2];   // the row as fp16 pairs
-            if (ok) {
-                tc::fence_after();
+            for (int x = 0; x < 2 && ok; ++x) {
+                if (u.nt[x] == 0) continue;
+                const int jx = job[x]++, jb = jx & 1;
+                ok = warp_all(mbar_wait_bounded(bar(bars.l_full[x], jb), (jx >> 1) & 1, p.status, true));
+                const float inv = ok ? 1.f / bars.red_l[x][jb][row] : 0.f;
+                mbar_arrive(bar(bars.l_empty[x], jb));
+                ok = ok && warp_all(mbar_wait_bounded(bar(bars.o_full, x), jx & 1, p.status, true));
+                uint32_t hv[D / 2];   // the row as fp16 pairs
+                if (ok) {
+                    tc::fence_after();
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tc::ld32(lane_base + kOCol + cc * 32, r);
-                    tc::wait_ld();
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tc::ld32(lane_base + kOCol + x * 128 + cc * 32, r);
+                        tc::wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        hv[cc * 16 + i] = pack_pair(__uint_as_float(r[2 * i]) * inv,
-                                                    __uint_as_float(r[2 * i + 1]) * inv);
-                }
-            }
-            tc::fence_before();
-            mbar_arrive(smem_addr(&bars.o_free));
-            if (!ok) break;
-            // 16-byte chunks transposed within groups of 8 lanes (an 8 x 8
-            // exchange per 64 columns), so that each store instruction writes 4
-            // whole 128-byte row segments
-            const int qi = u.q0 + row;
-            const unsigned long long mine =
-                qi < u.ql ? reinterpret_cast<unsigned long long>(p.out + ((size_t)(u.q_beg + qi) * H + u.h) * D)
-                          : 0ull;
-            const int c = lane & 7;
-#pragma unroll
-            for (int pass = 0; pass < D / 64; ++pass) {
-                uint32_t *x = hv + pass * 32;   // chunk e = x[4e .. 4e + 3]
-#pragma unroll
-                for (int m = 1; m < 8; m <<= 1) {
-                    const bool up = (c & m) != 0;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        if (e & m) continue;
-#pragma unroll
-                        for (int wd = 0; wd < 4; ++wd) {
-                            uint32_t &a = x[4 * e + wd], &b2 = x[4 * (e | m) + wd];
-                            const uint32_t r = __shfl_xor_sync(0xffffffffu, up ? a : b2, m);
-                            if (up) a = r; else b2 = r;
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            hv[cc * 16 + i] = pack_pair(__uint_as_float(r[2 * i]) * inv,
+                                                        __uint_as_float(r[2 * i + 1]) * inv);
                     }
                 }
-                // lane c now holds chunk c of rows (lane - c) + e in x[4e ..]
+                tc::fence_before();
+                mbar_arrive(bar(bars.o_free, x));
+                if (!ok) break;
+                // 16-byte chunks exchanged within groups of 8 lanes (an 8 x 8
+                // transpose per 64 columns), so that each store instruction writes 4
+                // whole 128-byte row segments
+                const int qi = u.q0[x] + row;
+                const unsigned long long mine =
+                    qi < u.ql ? reinterpret_cast<unsigned long long>(p.out + ((size_t)(u.q_beg + qi) * H + u.h) * D)
+                              : 0ull;
+                const int c = lane & 7;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const unsigned long long ptr = __shfl_sync(0xffffffffu, mine, (lane & ~7) + e);
-                    if (ptr)
-                        __stcs(reinterpret_cast<uint4 *>(ptr) + pass * 8 + c,
-                               make_uint4(x[4 * e], x[4 * e + 1], x[4 * e + 2], x[4 * e + 3]));
+                for (int pass = 0; pass < D / 64; ++pass) {
+                    uint32_t *xv = hv + pass * 32;   // chunk e = xv[4e .. 4e + 3]
+#pragma unroll
+                    for (int m = 1; m < 8; m <<= 1) {
+                        const bool up = (c & m) != 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            if (e & m) continue;
+#pragma unroll
+                            for (int wd = 0; wd < 4; ++wd) {
+                                uint32_t &a = xv[4 * e + wd], &b2 = xv[4 * (e | m) + wd];
+                                const uint32_t r = __shfl_xor_sync(0xffffffffu, up ? a : b2, m);
+                                if (up) a = r; else b2 = r;
+                            }
+                        }
+                    }
+                    // lane c now holds chunk c of row (lane - c) + e in xv[4e ..]
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const unsigned long long ptr = __shfl_sync(0xffffffffu, mine, (lane & ~7) + e);
+                        if (ptr)
+                            __stcs(reinterpret_cast<uint4 *>(ptr) + pass * 8 + c,
+                                   make_uint4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]));
+                    }
                 }
             }
         }
@@ -916,7 +859,7 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
         rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 8 >> m);
     if (rc == PA_OK) rc = encode_map(&maps.q, p.q, 3, (uint64_t)p.q_rows, H, D, TBM);
     if (rc != PA_OK) return rc;
-    p.q_tiles = (p.max_q_len + TBM - 1) / TBM;
+    p.q_pairs = ((p.max_q_len + TBM - 1) / TBM + 1) / 2;
     paged_prefill_tc<D><<<sms, kTcThreads, TcLayout<D>::BYTES, st>>>(p, maps, n_seqs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -963,7 +906,7 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     p.max_blocks = max_blocks;
     p.max_q_len = max_q_len;
     p.q_rows = q_rows;
-    p.q_tiles = 0;   // set by the launcher from its tile height
+    p.q_pairs = 0;   // set by the launcher from its tile height
     p.bshift = bshift;
     p.qscale = scale * 1.4426950408889634f;
     p.status = status;
