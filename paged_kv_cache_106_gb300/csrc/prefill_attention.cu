@@ -14,16 +14,21 @@
 //     copied once for both.  Each query tile has a slot: a Q buffer, S and O
 //     in tensor memory (S0, S1, O0, O1: 128 columns each) and a softmax
 //     warpgroup; a unit with one query tile takes the slots in turn.
-//       warps 0-3 / 4-7  softmax of slot 0 / 1, one query row per thread;
-//       warp 8     one thread issues every tcgen05.mma and commit, in the
+//       warps 0-7 / 8-15  softmax and epilogue of slot 0 / 1: warps w and
+//                  w + 4 share the query rows of tensor-memory lane quarter
+//                  w % 4, each half of a tile's key columns, and meet once per
+//                  tile (a named barrier per slot) to combine row maxima;
+//       warp 16    one thread issues every tcgen05.mma and commit, in the
 //                  order P V (slot 0), Q K^T of the next key tile (slot 0),
 //                  then the same for slot 1, so one slot's products run on
 //                  the tensor pipe while the other slot's softmax works;
-//       warp 9     Q tiles and K tiles by TMA, warp 10 V tiles by TMA;
-//       warp 11    scheduler: publishes this CTA's non-empty units through a
-//                  4-slot descriptor ring;
-//       warps 12-15 epilogue: normalise and write a job's rows once its last
-//                  P V is done, releasing O to the slot's next job.
+//       warp 17    Q tiles and K tiles by TMA, warp 18 V tiles by TMA;
+//       warp 19    scheduler: publishes this CTA's non-empty units through a
+//                  4-slot descriptor ring.
+//     A job's output is written by its softmax warps at the slot's next job:
+//     after writing that job's first P they read the old O (complete: the
+//     new S was committed after its last P V), release it to the first P V,
+//     and normalise and store while the tensor pipe works.
 //   - K and V tiles sit in shared memory as 8-row groups, [j / 8][64-column
 //     panel][j % 8][128 bytes], 128-byte swizzled; a (block, head) run of
 //     B >= 8 rows is whole groups and one 4-D TMA copy moves it (at D = 128;
@@ -80,6 +85,19 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Barrier among `count` threads of the CTA (ids 1.. are free; 0 is
+// __syncthreads) that also returns whether `v` held for all of them.
+__device__ __forceinline__ bool group_all(int id, int count, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // 2-D tensor copy global -> shared (box of the tensor map at element
 // coordinates x, y); completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -110,15 +128,15 @@ constexpr int TBN = 128;          // key positions per key tile
 constexpr int NSK = 2;            // K ring stages
 constexpr int NSV = 2;            // V ring stages
 constexpr int NU = 4;             // unit descriptors in flight
-// warps 0-3: softmax of slot 0, 4-7: softmax of slot 1, 12-15: epilogue
-constexpr int kMmaWarp = 8, kKWarp = 9, kVWarp = 10, kSchedWarp = 11;
-constexpr int kTcThreads = 512;   // 16 warps
+// warps 0-7: softmax and epilogue of slot 0, 8-15: of slot 1
+constexpr int kMmaWarp = 16, kKWarp = 17, kVWarp = 18, kSchedWarp = 19;
+constexpr int kTcThreads = 640;   // 20 warps
 constexpr uint32_t kPanel = TBM * 128;   // bytes of one 64-column panel of a 128-row tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;          // S of slot x at columns 128 x, its O at kOCol + 128 x
 constexpr float kRescaleLog2 = 8.f;      // lazy-rescale threshold (log2 units)
-// readers of a unit descriptor: K loader, V loader, MMA thread, 8 softmax warps, 4 epilogue warps
-constexpr uint32_t kUnitReaders = 3 + 8 + 4;
+// readers of a unit descriptor: K loader, V loader, MMA thread, 16 softmax warps
+constexpr uint32_t kUnitReaders = 3 + 16;
 constexpr int kPrefetchTiles = 2;  // K/V tiles prefetched into L2 ahead of their copies
 constexpr int kVPartMaps = 4;     // boxes of 8, 4, 2, 1 cache rows for a partial V block
 
@@ -165,12 +183,13 @@ struct TcBars {
     uint64_t q_full[2], q_empty[2];           // per slot
     uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
     uint64_t s_full[2], p_full[2];            // per slot: S written, P written
-    uint64_t o_full[2], o_free[2];            // per slot: a job's O complete, read by the epilogue
-    uint64_t l_full[2][2], l_empty[2][2];     // per slot and job parity: row sums written, read
+    uint64_t o_full[2];                       // per slot: a job's O complete
+    uint64_t o_free[2];                       // per slot: a job's O read (the next job may overwrite it)
     uint64_t done;
     uint32_t tmem;
     Unit unit[NU];
-    float red_l[2][2][TBM];                   // per slot and job parity: a finished job's row sums
+    float red[2][2][2][TBM];                  // per slot, tile parity and column half: row maxima
+    float red_l[2][2][TBM];                   // per slot and column half: a finished job's row sums
 };
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
@@ -225,13 +244,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(bars.q_full, x), 1);
             mbar_init(bar(bars.q_empty, x), 1);   // the job's last Q K^T is done
             mbar_init(bar(bars.s_full, x), 1);
-            mbar_init(bar(bars.p_full, x), 128);  // the slot's softmax threads
+            mbar_init(bar(bars.p_full, x), 256);  // the slot's softmax threads
             mbar_init(bar(bars.o_full, x), 1);
-            mbar_init(bar(bars.o_free, x), 128);  // the epilogue threads
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(bar(bars.l_full[x], i), 128);
-                mbar_init(bar(bars.l_empty[x], i), 128);
-            }
+            mbar_init(bar(bars.o_free, x), 256);  // the slot's softmax threads
         }
         for (int i = 0; i < NSK; ++i) {
             mbar_init(bar(bars.k_full, i), 1);
@@ -514,10 +529,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < TBN / 16; ++kk) {
                             // V: 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart.
-                            // P of keys 16 kk .. 16 kk + 15: 8 columns (16 fp16) at 8 kk
+                            // P of keys 16 kk .. 16 kk + 15: column half (kk / 4) * 64, then
+                            // 16 columns per 32 keys, 8 columns (16 fp16) per slice
                             const uint64_t dv = tc::smem_desc(vb + kk * 2048u * NP, 1024, 1024u * NP);
-                            tc::mma_ts(tmem + kOCol + x * 128, tmem + x * 128 + kk * 8, dv, idO,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
+                            const uint32_t pa =
+                                tmem + x * 128 + (kk >> 2) * 64 + ((kk >> 1) & 1) * 16 + (kk & 1) * 8;
+                            tc::mma_ts(tmem + kOCol + x * 128, pa, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
                         }
                         if (j + 1 < u.nt[x]) {
                             if (!k_next && !wait(bar(bars.k_full, (gj + 1) % NSK), ((gj + 1) / NSK) & 1)) break;
@@ -541,52 +558,117 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         __syncwarp();
     } else if (warp < kMmaWarp) {
-        // ---- softmax: warps 4x .. 4x + 3 serve slot x; warp w takes the 32 query
-        // rows of tensor-memory lane quarter w % 4, one row per thread, all 128
-        // key columns of each tile
-        const int x = warp >> 2, quarter = warp & 3;
+        // ---- softmax and epilogue: warps 8x .. 8x + 7 serve slot x.  Warps w and
+        // w + 4 of the slot share the query rows of tensor-memory lane quarter
+        // w % 4; the first takes key columns 0-63 of each tile, the second
+        // 64-127, and they meet once per tile (a named barrier per slot) to
+        // combine their row maxima.  The slot's warps leave their loops only
+        // together, at a meeting.  A job's output is written at the start of
+        // the slot's next job, when its O is complete (that job's first S was
+        // committed after the last P V of the previous one), or after the last.
+        const int x = warp >> 3, quarter = warp & 3, half = (warp >> 2) & 1;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t sb = lane_base + x * 128, ob = lane_base + kOCol + x * 128;
+        const uint32_t sb = lane_base + x * 128 + half * 64;
+        const uint32_t ob = lane_base + kOCol + x * 128 + half * (D / 2);
+        const int meet = 1 + x;   // named barrier of the slot (0 is __syncthreads)
         const float qs = p.qscale;
-        bool ok = true;
-        int job = 0, sc = 0;   // jobs and S tiles of this slot so far
-        for (int k = 0; ok; ++k) {
+        bool ok = true, stop = false;
+        int sc = 0, job = 0;     // S tiles and jobs of this slot so far
+        bool pend = false;       // the previous job's output is still in O
+        float pend_l = 0.f;
+        unsigned long long pend_out = 0;   // its row's half (none: a padded row)
+        constexpr int NCH = D / 16;   // 16-byte chunks of a half row
+        // this thread's half of the pending row, normalised, as fp16 pairs; after
+        // a meeting, so that the partner's sum is in red_l
+        auto epi_read = [&](uint32_t (&hv)[4 * NCH]) {
+            const float inv = 1.f / (pend_l + bars.red_l[x][half ^ 1][row]);
+            tc::fence_after();
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t r[32];
+                tc::ld32(ob + cc * 32, r);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    hv[cc * 16 + i] = pack_pair(__uint_as_float(r[2 * i]) * inv,
+                                                __uint_as_float(r[2 * i + 1]) * inv);
+            }
+        };
+        // write it: chunks exchanged within groups of NCH lanes (an NCH x NCH
+        // transpose), so that each store instruction writes whole row segments
+        auto epi_store = [&](uint32_t (&hv)[4 * NCH]) {
+            const int c = lane % NCH;
+#pragma unroll
+            for (int m = 1; m < NCH; m <<= 1) {
+                const bool up = (c & m) != 0;
+#pragma unroll
+                for (int e = 0; e < NCH; ++e) {
+                    if (e & m) continue;
+#pragma unroll
+                    for (int wd = 0; wd < 4; ++wd) {
+                        uint32_t &a = hv[4 * e + wd], &b2 = hv[4 * (e | m) + wd];
+                        const uint32_t r = __shfl_xor_sync(0xffffffffu, up ? a : b2, m);
+                        if (up) a = r; else b2 = r;
+                    }
+                }
+            }
+            // lane c now holds chunk c of row (lane - c) + e in hv[4e ..]
+#pragma unroll
+            for (int e = 0; e < NCH; ++e) {
+                const unsigned long long ptr = __shfl_sync(0xffffffffu, pend_out, lane - c + e);
+                if (ptr)
+                    __stcs(reinterpret_cast<uint4 *>(ptr) + c,
+                           make_uint4(hv[4 * e], hv[4 * e + 1], hv[4 * e + 2], hv[4 * e + 3]));
+            }
+            pend = false;
+        };
+        for (int k = 0;; ++k) {
             Unit u;
             get_unit(k, u);
             if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
-            if (u.n_tiles <= 0) {
-                ok = u.n_tiles == 0;
-                break;
-            }
+            ok = ok && u.n_tiles >= 0;
+            if (!group_all(meet, 256, ok && u.n_tiles > 0)) break;   // end marker or a failure
             if (u.nt[x] == 0) continue;
-            const int q0 = u.q0[x];
-            const int pos = u.pos0 + min(q0 + row, u.ql - 1);   // this row's position
+            const int q0 = u.q0[x], qi = q0 + row;
+            const int pos = u.pos0 + min(qi, u.ql - 1);   // this row's position
             float m_run = -INFINITY, l_run = 0.f;
-            for (int t = 0; ok && t < u.nt[x]; ++t, ++sc) {
-                ok = warp_all(mbar_wait_bounded(bar(bars.s_full, x), sc & 1, p.status, true));
-                if (!ok) break;
-                tc::fence_after();
-                const int n0 = t * TBN;
+            for (int t = 0; t < u.nt[x]; ++t, ++sc) {
+                ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, x), sc & 1, p.status, true));
+                const int n0 = t * TBN + half * 64;   // first key of this warp's columns
                 // keys past a row's position are masked: key n0 + 32 cc + i with i > lim
-                const bool need_mask = n0 + TBN - 1 > u.pos0 + q0;
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                const bool need_mask = n0 + 63 > u.pos0 + q0;
+                float mt = -INFINITY;
+                if (ok) {
+                    tc::fence_after();
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t r[32];
-                    tc::ld32(sb + cc * 32, r);
-                    tc::wait_ld();
-                    if (need_mask) {
-                        const int lim = pos - (n0 + cc * 32);
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t r[32];
+                        tc::ld32(sb + cc * 32, r);
+                        tc::wait_ld();
+                        if (need_mask) {
+                            const int lim = pos - (n0 + cc * 32);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
-                    } else {
+                            for (int i = 0; i < 32; ++i)
+                                m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
+                            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
+                        }
                     }
+                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qs;   // scale > 0
                 }
-                const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qs;   // scale > 0
+                bars.red[x][sc & 1][half][row] = mt;
+                if (t == 0 && pend) bars.red_l[x][half][row] = pend_l;
+                // the two halves of each row meet: one exit decision for the slot's
+                // warps, the partner's maximum (and, on a job's first tile, the
+                // partner's sum for the pending output)
+                if (!group_all(meet, 256, ok)) {
+                    stop = true;
+                    break;
+                }
+                mt = fmaxf(mt, bars.red[x][sc & 1][half ^ 1][row]);
                 float corr = 1.f;
                 const bool resc = mt > m_run + kRescaleLog2;
                 if (resc) {
@@ -596,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t r[32], w[16];
                     tc::ld32(sb + cc * 32, r);
                     tc::wait_ld();
@@ -628,9 +710,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc::wait_st();
                 if (__any_sync(0xffffffffu, resc && t > 0)) {
                     // O holds the job's tiles < t, complete (S of tile t was committed
-                    // after their products): scale this thread's row
+                    // after their products): scale this warp's half of the columns
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < D / 64; ++cc) {
                         uint32_t r[32];
                         tc::ld32(ob + cc * 32, r);
                         tc::wait_ld();
@@ -642,96 +724,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc::fence_before();
                 mbar_arrive(bar(bars.p_full, x));
+                if (t == 0 && pend) {
+                    // the previous job's O (complete: this tile's S was committed after
+                    // its last P V) is read, then released to this job's first P V;
+                    // its rows are written while the tensor pipe works
+                    uint32_t hv[4 * NCH];
+                    epi_read(hv);
+                    tc::fence_before();
+                    mbar_arrive(bar(bars.o_free, x));
+                    epi_store(hv);
+                }
             }
-            if (!ok) break;
-            // the job's row sums for the epilogue (slot job & 1 is free once the
-            // epilogue has read the sums of job - 2)
-            const int jb = job & 1;
-            if (job >= 2)
-                ok = warp_all(mbar_wait_bounded(bar(bars.l_empty[x], jb), ((job >> 1) - 1) & 1,
-                                                p.status, true));
-            if (!ok) break;
-            bars.red_l[x][jb][row] = l_run;
-            mbar_arrive(bar(bars.l_full[x], jb));
+            if (stop) break;
+            pend = true;
+            pend_l = l_run;
+            pend_out = qi < u.ql ? reinterpret_cast<unsigned long long>(
+                                       p.out + ((size_t)(u.q_beg + qi) * H + u.h) * D + half * (D / 2))
+                                 : 0ull;
             ++job;
         }
-        if (!ok) report(p.status, PA_ERR_TIMEOUT);
-    } else {
-        // ---- epilogue: warp 12 + q takes the rows of tensor-memory lane quarter q.
-        // For each job: the row sums, then (once the job's last P V is done) O,
-        // normalised and as fp16, into registers; O is then released to the
-        // slot's next job, and the rows are written (only the unit's queries).
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        int job[2] = {0, 0};
-        bool ok = true;
-        for (int k = 0; ok; ++k) {
-            Unit u;
-            get_unit(k, u);
-            if (lane == 0 && u.n_tiles >= 0) mbar_arrive(bar(bars.unit_empty, k % NU));
-            if (u.n_tiles <= 0) {
-                ok = u.n_tiles == 0;
-                break;
-            }
-            for (int x = 0; x < 2 && ok; ++x) {
-                if (u.nt[x] == 0) continue;
-                const int jx = job[x]++, jb = jx & 1;
-                ok = warp_all(mbar_wait_bounded(bar(bars.l_full[x], jb), (jx >> 1) & 1, p.status, true));
-                const float inv = ok ? 1.f / bars.red_l[x][jb][row] : 0.f;
-                mbar_arrive(bar(bars.l_empty[x], jb));
-                ok = ok && warp_all(mbar_wait_bounded(bar(bars.o_full, x), jx & 1, p.status, true));
-                uint32_t hv[D / 2];   // the row as fp16 pairs
-                if (ok) {
-                    tc::fence_after();
-#pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t r[32];
-                        tc::ld32(lane_base + kOCol + x * 128 + cc * 32, r);
-                        tc::wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            hv[cc * 16 + i] = pack_pair(__uint_as_float(r[2 * i]) * inv,
-                                                        __uint_as_float(r[2 * i + 1]) * inv);
-                    }
-                }
-                tc::fence_before();
-                mbar_arrive(bar(bars.o_free, x));
-                if (!ok) break;
-                // 16-byte chunks exchanged within groups of 8 lanes (an 8 x 8
-                // transpose per 64 columns), so that each store instruction writes 4
-                // whole 128-byte row segments
-                const int qi = u.q0[x] + row;
-                const unsigned long long mine =
-                    qi < u.ql ? reinterpret_cast<unsigned long long>(p.out + ((size_t)(u.q_beg + qi) * H + u.h) * D)
-                              : 0ull;
-                const int c = lane & 7;
-#pragma unroll
-                for (int pass = 0; pass < D / 64; ++pass) {
-                    uint32_t *xv = hv + pass * 32;   // chunk e = xv[4e .. 4e + 3]
-#pragma unroll
-                    for (int m = 1; m < 8; m <<= 1) {
-                        const bool up = (c & m) != 0;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            if (e & m) continue;
-#pragma unroll
-                            for (int wd = 0; wd < 4; ++wd) {
-                                uint32_t &a = xv[4 * e + wd], &b2 = xv[4 * (e | m) + wd];
-                                const uint32_t r = __shfl_xor_sync(0xffffffffu, up ? a : b2, m);
-                                if (up) a = r; else b2 = r;
-                            }
-                        }
-                    }
-                    // lane c now holds chunk c of row (lane - c) + e in xv[4e ..]
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const unsigned long long ptr = __shfl_sync(0xffffffffu, mine, (lane & ~7) + e);
-                        if (ptr)
-                            __stcs(reinterpret_cast<uint4 *>(ptr) + pass * 8 + c,
-                                   make_uint4(xv[4 * e], xv[4 * e + 1], xv[4 * e + 2], xv[4 * e + 3]));
-                    }
-                }
+        // the last job's output, once its last P V is done
+        if (!stop && pend) {
+            ok = ok && warp_all(mbar_wait_bounded(bar(bars.o_full, x), (job - 1) & 1, p.status, true));
+            bars.red_l[x][half][row] = pend_l;
+            if (group_all(meet, 256, ok)) {
+                uint32_t hv[4 * NCH];
+                epi_read(hv);
+                epi_store(hv);
             }
         }
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
