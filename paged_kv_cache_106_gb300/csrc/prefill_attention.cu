@@ -28,7 +28,12 @@
 //     A job's output is written by its softmax warps at the slot's next job:
 //     after writing that job's first P they read the old O (complete: the
 //     new S was committed after its last P V), release it to the first P V,
-//     and normalise and store while the tensor pipe works.
+//     and normalise and store while the tensor pipe works (16-byte streaming
+//     stores, chunks exchanged between lanes so that each store instruction
+//     writes whole row segments; only the unit's rows).
+//   - K/V tiles are copied with an evict-last L2 policy (later query tiles
+//     re-read them), query tiles with evict-first; the runs of the key tile
+//     two steps ahead are prefetched into L2.
 //   - K and V tiles sit in shared memory as 8-row groups, [j / 8][64-column
 //     panel][j % 8][128 bytes], 128-byte swizzled; a (block, head) run of
 //     B >= 8 rows is whole groups and one 4-D TMA copy moves it (at D = 128;
