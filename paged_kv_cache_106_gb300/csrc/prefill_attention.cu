@@ -637,6 +637,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (u.nt[x] == 0) continue;
             const int q0 = u.q0[x], qi = q0 + row;
             const int pos = u.pos0 + min(qi, u.ql - 1);   // this row's position
+            // the last position among this warp's rows: key chunks after it are
+            // masked for every row of the warp
+            const int pos_w = u.pos0 + min(q0 + quarter * 32 + 31, u.ql - 1);
             float m_run = -INFINITY, l_run = 0.f;
             for (int t = 0; t < u.nt[x]; ++t, ++sc) {
                 ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, x), sc & 1, p.status, true));
@@ -649,6 +652,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
                     for (int cc = 0; cc < 2; ++cc) {
+                        if (n0 + cc * 32 > pos_w) break;   // this chunk and the next: all masked
                         uint32_t r[32];
                         tc::ld32(sb + cc * 32, r);
                         tc::wait_ld();
@@ -685,6 +689,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll 1
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t r[32], w[16];
+                    if (n0 + cc * 32 > pos_w) {   // all masked: P = 0, nothing to read
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = 0u;
+                        tc::st16(sb + cc * 16, w);
+                        continue;
+                    }
                     tc::ld32(sb + cc * 32, r);
                     tc::wait_ld();
                     if (need_mask) {

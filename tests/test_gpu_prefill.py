@@ -83,9 +83,13 @@ def test_prefill_matches_oracle(D, B):
     rng = np.random.default_rng(1000 + D + B)
     H = 3
     # (ctx, q_len): whole prompts of 1, 63, 64, 65, 200 tokens; chunks after
-    # a cached prefix (q_len < ctx), one-query sequences, an empty query set
+    # a cached prefix (q_len < ctx), one-query sequences, an empty query set,
+    # and prompts spanning several 128-query tiles
     pairs = [(1, 1), (63, 63), (64, 64), (65, 65), (200, 200), (150, 37), (300, 129),
-             (77, 1), (5, 0), (129, 128), (2 * B + 1, 2)]
+             (77, 1), (5, 0), (129, 128), (2 * B + 1, 2),
+             # several query tiles: two pairs; two pairs and a lone first tile;
+             # a chunk of 4 tiles after a prefix that is not tile-aligned
+             (400, 400), (520, 520), (700, 450)]
     ctx = [c for c, _ in pairs]
     ql = [x for _, x in pairs]
     q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ql, H, D, B)
