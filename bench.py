@@ -295,6 +295,17 @@ def run_ours(args):
     # into the other pinned buffer); then it waits for step i's output to be
     # on the host.  Stream order keeps each step's inputs and output intact.
     h_out = [h_o, torch.empty_like(h_o).pin_memory()]
+    # untimed passes through the copy path: the first transfers through freshly
+    # pinned pages run several times slower than the steady state (measured on
+    # the Grace host: 6-37 GB/s for the first two, then 190-210 GB/s)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            q.copy_(h_q, non_blocking=True)
+            k_new.copy_(h_k, non_blocking=True)
+            v_new.copy_(h_v, non_blocking=True)
+            for h in h_out:
+                h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
 
     def host_prep():
         batch.admit(ids)
@@ -811,16 +822,25 @@ def run_prefill(args):
     for h in (h_k, h_v, h_q):
         h.normal_()
     e2e_steps = max(1, min(args.e2e_steps, 20))
+
+    def e2e_step():
+        k_new.copy_(h_k, non_blocking=True)
+        v_new.copy_(h_v, non_blocking=True)
+        q.copy_(h_q, non_blocking=True)
+        step()
+        h_o.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    # untimed steps first: the first transfers through freshly pinned pages run
+    # several times slower than the steady state
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
     torch.cuda.synchronize()
     w0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
-            k_new.copy_(h_k, non_blocking=True)
-            v_new.copy_(h_v, non_blocking=True)
-            q.copy_(h_q, non_blocking=True)
-            step()
-            h_o.copy_(out, non_blocking=True)
-            stream.synchronize()
+            e2e_step()
     e2e_s = (time.perf_counter() - w0) / e2e_steps
     (tok_all, e2e_tok), (el_max, e2e_max) = reduce_across_ranks(
         [T * args.steps, T * e2e_steps], [el, e2e_s * e2e_steps], dev)
@@ -857,7 +877,7 @@ def run_prefill(args):
                                         "tokens": T, "algorithmic_bytes": T * H * D * 2 * 4}},
             "e2e": {"value": e2e_tok / e2e_max, "unit": PREFILL_UNIT,
                     "h2d_bytes_per_step": 3 * T * H * D * 2, "d2h_bytes_per_step": T * H * D * 2,
-                    "steps": e2e_steps, "timing": "wall clock, stream synchronised every step"},
+                    "steps": e2e_steps, "timing": "wall clock, stream synchronised every step, after 3 untimed steps"},
             "clocks": clk,
         }
         if not args.no_cpu_baseline:
