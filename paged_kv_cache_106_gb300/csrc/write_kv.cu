@@ -4,11 +4,12 @@
 // [n_tokens][H][D] to their slot in the block-structured cache
 // [num_blocks][H][B][D], one launch for the whole batch.
 //
-// One thread moves one 16-byte vector (8 halves) of a key row and the same
-// vector of the value row: reads are fully coalesced, writes are contiguous
-// runs of D*2 bytes per (token, head).  This kernel moves
-// 2 * n_tokens * H * D * 2 bytes each way (~2.6 MB for 256 OPT-13B tokens),
-// microseconds next to the attention it feeds.
+// Token-major: a CTA takes a token (grid-stride), reads its slot once and
+// its threads move the token's H * D / 8 16-byte vectors of the key row and
+// the same vectors of the value row: reads are fully coalesced, writes are
+// contiguous runs of D*2 bytes per (token, head), and the index arithmetic
+// is shifts (D / 8 and B are powers of two).  This kernel moves
+// 2 * n_tokens * H * D * 2 bytes each way (~2.6 MB for 256 OPT-13B tokens).
 #include <cuda_runtime.h>
 
 #include "pa_device.cuh"
@@ -18,28 +19,33 @@ namespace pagedkv {
 
 namespace {
 
-__global__ void __launch_bounds__(256)
+constexpr int kWriteThreads = 128;
+
+__global__ void __launch_bounds__(kWriteThreads)
 write_kv_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
-                const int64_t *__restrict__ slot_mapping, int64_t n_vec, int vec_per_tok,
-                int vec_per_row, int H, int B, int64_t num_slots, uint4 *__restrict__ k_cache,
+                const int64_t *__restrict__ slot_mapping, int32_t n_tokens, int vec_per_tok,
+                int row_shift, int bshift, int H, int64_t num_slots, uint4 *__restrict__ k_cache,
                 uint4 *__restrict__ v_cache, int32_t *status) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_vec;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = i / vec_per_tok;
-        const int rem = (int)(i - t * vec_per_tok);
-        const int h = rem / vec_per_row;
-        const int c = rem - h * vec_per_row;
+    const int row_mask = (1 << row_shift) - 1;   // vectors per (token, head) row - 1
+    for (int32_t t = blockIdx.x; t < n_tokens; t += gridDim.x) {
         const int64_t slot = slot_mapping[t];
         if (slot < 0) continue;                 // token not stored
         if (slot >= num_slots) {
-            report(status, PA_ERR_BAD_BLOCK);
+            if (threadIdx.x == 0) report(status, PA_ERR_BAD_BLOCK);
             continue;
         }
-        const int64_t blk = slot / B;
-        const int off = (int)(slot - blk * B);
-        const int64_t dst = ((blk * H + h) * B + off) * vec_per_row + c;
-        k_cache[dst] = k[i];
-        v_cache[dst] = v[i];
+        const int64_t blk = slot >> bshift;
+        const int off = (int)(slot & ((1 << bshift) - 1));
+        const uint4 *ks = k + (int64_t)t * vec_per_tok, *vs = v + (int64_t)t * vec_per_tok;
+        // run of head h in the cache: ((blk * H + h) * B + off) rows of D / 8 vectors
+        const int64_t base = ((blk * H) << bshift) + off;
+#pragma unroll 4
+        for (int j = threadIdx.x; j < vec_per_tok; j += kWriteThreads) {
+            const int h = j >> row_shift, c = j & row_mask;
+            const int64_t dst = ((base + ((int64_t)h << bshift)) << row_shift) + c;
+            k_cache[dst] = ks[j];
+            v_cache[dst] = vs[j];
+        }
     }
 }
 
@@ -60,19 +66,22 @@ int launch_write_kv(const void *k, const void *v, const int64_t *slot_mapping, i
         (reinterpret_cast<uintptr_t>(slot_mapping) & 7))
         return fail(PA_ERR_INVALID_ARG, "pa_write_kv: misaligned pointer");
     const int vec_per_row = d->head_dim / 8;
+    int row_shift = 0, bshift = 0;
+    while ((1 << row_shift) < vec_per_row) ++row_shift;
+    while ((1 << bshift) < d->block_size) ++bshift;
+    if ((1 << row_shift) != vec_per_row || (1 << bshift) != d->block_size)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv: head_dim / 8 and block_size must be powers of two");
     const int vec_per_tok = d->num_heads * vec_per_row;
-    const int64_t n_vec = (int64_t)n_tokens * vec_per_tok;
     int sms = 152;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess)
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t want = (n_vec + 255) / 256;
-    const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-    write_kv_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, n_vec,
-        vec_per_tok, vec_per_row, d->num_heads, d->block_size,
-        (int64_t)d->num_blocks * d->block_size, static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), status);
+    // resident CTAs: 16 per SM of 128 threads; a CTA per token up to that
+    const int grid = n_tokens < sms * 16 ? n_tokens : sms * 16;
+    write_kv_kernel<<<grid, kWriteThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, n_tokens,
+        vec_per_tok, row_shift, bshift, d->num_heads, (int64_t)d->num_blocks * d->block_size,
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "pa_write_kv: launch: %s", cudaGetErrorString(e));
     return PA_OK;
