@@ -57,16 +57,26 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _code_sha256(path: str) -> str:
+    """sha256 of a C/CUDA source with its comments and whitespace removed, so
+    that a profile taken on a kernel stays attached to it across comment
+    edits (any change to the code itself changes the hash)."""
+    import hashlib
+    import re
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()
+
+
 def _kernel_traffic(kernel_src: str, name: str = "decode_attention_traffic.json"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel (else None)."""
-    import hashlib
+    on the current code of the kernel (else None)."""
     p = os.path.join(ROOT, "profiles", name)
     try:
         with open(p) as f:
             d = json.load(f)
-        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
-        if d.get("kernel_sha256") == h:
+        if d.get("code_sha256") == _code_sha256(kernel_src):
             return d
     except Exception:
         pass

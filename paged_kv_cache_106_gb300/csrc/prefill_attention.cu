@@ -177,8 +177,8 @@ struct Unit {
 // Tensor maps: K and V cache runs (D = 128 with B >= 8: a 4-D view
 // [row / 8][panel][row % 8][64] with one box per (block, head) run; otherwise
 // rows of D values, box 64 x B, one copy per panel), cache rows for the
-// partial V block (boxes 64 x 8 .. 64 x 1), query rows and output rows as 3-D
-// [rows][H][D] tensors (q: one box of 128 rows; out: boxes of 128 .. 1 rows).
+// partial V block (boxes 64 x 8 .. 64 x 1), and query rows as a 3-D
+// [rows][H][D] tensor with one box of 128 rows.
 struct TcMaps {
     CUtensorMap k, v, v_part[kVPartMaps], q;
 };

@@ -47,3 +47,19 @@ def test_two_gloo_ranks_sum_work_and_max_time():
 def test_single_process_reduction_is_identity():
     import bench
     assert bench.reduce_across_ranks([3, 4], [1.5], "cpu") == ([3.0, 4.0], [1.5])
+
+
+def test_code_hash_ignores_comments_and_whitespace_only(tmp_path):
+    """A profile summary stays attached to its kernel across comment edits:
+    the hash that bench.py compares drops comments and whitespace, and any
+    change to the code itself changes it."""
+    import bench
+
+    a = tmp_path / "a.cu"
+    a.write_text("// header\n__global__ void k(int *p) {\n  p[0] = 1;  /* one */\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// a different header\n\n__global__ void k(int *p)\n{ p[0] = 1; }\n")
+    c = tmp_path / "c.cu"
+    c.write_text("// header\n__global__ void k(int *p) {\n  p[0] = 2;  /* one */\n}\n")
+    assert bench._code_sha256(str(a)) == bench._code_sha256(str(b))
+    assert bench._code_sha256(str(a)) != bench._code_sha256(str(c))
