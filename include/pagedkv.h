@@ -392,6 +392,18 @@ int pa_decode_attention_noalloc(void *out, const void *q, const void *k_cache, c
                                 int32_t n_seqs, int32_t max_blocks, float scale,
                                 int32_t *status, const pa_pool_desc *desc, void *stream);
 
+/* Diagnostic for the bounded waits that every kernel of this library uses
+ * (no counterpart on the pages).  Launches one thread on `stream` that
+ * waits, through the library's bounded wait, for an mbarrier phase that
+ * nothing completes; the wait gives up after its limit (200 ms) and the
+ * thread writes PA_ERR_TIMEOUT into *status, as a kernel whose producer
+ * never arrives would.  Nothing faults and the context stays usable.
+ *   status  device int32, caller-owned; reads PA_ERR_TIMEOUT once the
+ *           stream has completed the call.
+ * Errors: PA_ERR_INVALID_ARG for a NULL status (nothing launched);
+ * PA_ERR_CUDA if the launch fails. */
+int pa_selftest_bounded_wait(int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -98,6 +98,7 @@ def _load():
                                               vp, P(pa_pool_desc), vp]),
         "pa_prefill_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                        ctypes.c_float, vp, P(pa_pool_desc), vp]),
+        "pa_selftest_bounded_wait": (i32, [vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -379,6 +380,13 @@ def pa_prefill_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, q_sta
                                      _dev(block_tables), _dev(ctx_lens), _dev(q_starts), n, mb,
                                      int(max_q_len), rows, ctypes.c_float(scale), _dev(status),
                                      desc.ref, _stream(stream)))
+
+
+def pa_selftest_bounded_wait(status, stream=None) -> None:
+    """One thread waits, with the kernels' bounded wait, for an mbarrier phase
+    that nothing completes; after the limit it writes PA_ERR_TIMEOUT into
+    status (device int32)."""
+    _check(_lib.pa_selftest_bounded_wait(_dev(status), _stream(stream)))
 
 
 def pa_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, ctx_lens, scale: float,

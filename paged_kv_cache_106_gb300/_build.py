@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libpagedkv.so")
 OBJ = os.path.join(PKG, "_build")
 HEADERS = [os.path.join(ROOT, "include", "pagedkv.h")]
 SOURCES = ["pool.cpp", "api.cpp", "write_kv.cu", "copy_blocks.cu", "decode_attention.cu",
-           "prefill_attention.cu"]
+           "prefill_attention.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -66,6 +66,10 @@ extern "C" {
 
 const char *pa_last_error_string(void) { return last_error(); }
 
+int pa_selftest_bounded_wait(int32_t *status, void *stream) {
+    return launch_selftest_bounded_wait(status, stream);
+}
+
 int pa_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32_t n_tokens,
                 void *k_cache, void *v_cache, const pa_pool_desc *desc, int32_t *status,
                 void *stream) {

@@ -22,6 +22,7 @@ bool device_geometry_ok(const pa_pool_desc *d, std::string *why);
 int partition_tokens_of(const pa_pool_desc *d);
 
 // Kernel launchers (device code lives in the .cu files).
+int launch_selftest_bounded_wait(int32_t *status, void *stream);
 int launch_write_kv(const void *k, const void *v, const int64_t *slot_mapping, int32_t n_tokens,
                     void *k_cache, void *v_cache, const pa_pool_desc *d, int32_t *status,
                     void *stream);
