@@ -199,6 +199,18 @@ struct TcBars {
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void zero_smem(uint32_t addr, uint32_t bytes, int lane) {
     for (uint32_t o = (uint32_t)lane * 16u; o < bytes; o += 32u * 16u)
         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr + o), "r"(0) : "memory");
@@ -490,6 +502,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (ok) ok = mbar_wait_bounded(b, par, p.status, true);
                 return ok;
             };
+            // the same, polling: for a slot's P, on the critical path, a polled
+            // wait sees the softmax's arrival sooner than a suspended one
+            // (measured: 0.940 -> 0.925 ms on the 256-prompt batch)
+            auto spin = [&](uint32_t b, uint32_t par) {
+                if (!ok || mbar_test(b, par)) return ok;
+                const uint64_t t0 = globaltimer_ns();
+                for (uint32_t n = 1; !mbar_test(b, par); ++n)
+                    if ((n & 1023) == 0 && (globaltimer_ns() - t0 > kWaitLimitNs ||
+                                            *(volatile const int32_t *)p.status == PA_ERR_TIMEOUT))
+                        return ok = false;
+                return true;
+            };
             // S_x = Q_x K^T for the key tile in K ring stage st
             auto issue_s = [&](int x, int st) {
                 const uint32_t qb = sQ + x * L::TILE, kb = sK + st * L::TILE;
@@ -524,7 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     bool k_next = false;   // key tile j + 1 waited for
                     for (int x = 0; x < 2; ++x) {
                         if (j >= u.nt[x]) continue;
-                        if (!wait(bar(bars.p_full, x), pc[x] & 1)) break;
+                        if (!spin(bar(bars.p_full, x), pc[x] & 1)) break;
                         ++pc[x];
                         // a job's first P V overwrites O: the epilogue must have read
                         // the slot's previous job
