@@ -73,6 +73,15 @@ class AbiAdapter:
         return pk.pa_pool_free_queue(self.p, self.nb).tolist()
 
 
+def test_bounded_wait_selftest_refuses_a_null_status_before_any_launch():
+    """Argument checks of a device call run on the host: a NULL status is
+    refused with PA_ERR_INVALID_ARG and nothing is launched (no GPU needed)."""
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_selftest_bounded_wait(None, stream=0)
+    assert e.value.code == pk.PA_ERR_INVALID_ARG
+    assert "status is NULL" in pk.pa_last_error_string()
+
+
 @pytest.mark.parametrize("name", GOLDEN)
 def test_golden_examples_through_abi(golden_dir, name):
     doc = load(golden_dir, name)

@@ -45,8 +45,3 @@ def test_wait_that_never_completes_reports_timeout_and_leaves_the_context_usable
     oc.write_kv(ref_k, ref_v, k, v, slots)
     assert np.array_equal(kc.cpu().numpy().view(np.uint16), ref_k.view(np.uint16))
     assert np.array_equal(vc.cpu().numpy().view(np.uint16), ref_v.view(np.uint16))
-
-
-def test_selftest_refuses_a_null_status():
-    with pytest.raises(Exception):
-        pk.pa_selftest_bounded_wait(None)
