@@ -228,7 +228,7 @@ def full_40l(pool_bytes: int, seed: int = 110, beam: bool = False,
     )
 
 
-CONFIGS = {
+WORKLOADS = {
     "tiny": tiny,
     "opt13b_b64": opt13b_b64,
     "parallel_sampling": parallel_sampling,

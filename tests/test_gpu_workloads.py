@@ -152,7 +152,7 @@ def _sample_rows(ctx, rng, n_random=8):
 
 @pytest.mark.parametrize("name", ["opt13b_b64", "mixed_b256"])
 def test_full_size_workloads_sampled(name):
-    w = wl.CONFIGS[name]()
+    w = wl.WORKLOADS[name]()
     b = Both(w)
     b.check_cache()
     out, q, tables, ctx = b.decode_step()

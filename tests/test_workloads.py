@@ -30,7 +30,7 @@ def test_kv_bytes_per_token_matches_the_notes_closed_form():
 
 
 def test_structures_are_valid_and_deterministic():
-    for make in wl.CONFIGS.values():
+    for make in wl.WORKLOADS.values():
         a, b = make(), make()
         assert sorted(a.free_order.tolist()) == list(range(a.num_blocks))
         assert a.free_order.tolist() == b.free_order.tolist()
