@@ -164,7 +164,7 @@ class SteadyBatch:
         self.replaced = 0
 
     def admit(self, ids):
-        from paged_kv_cache_106_gb300.workloads import draw_mixed_sequence
+        from workloads import draw_mixed_sequence
         for i in np.nonzero(self.held >= self.target)[0]:
             self.pk.pa_seq_free(self.pool, int(ids[i]))
             prompt, target = draw_mixed_sequence(self.rng)
@@ -183,7 +183,7 @@ def run_ours(args):
     import torch.distributed as dist
 
     import paged_kv_cache_106_gb300 as pk
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
     from paged_kv_cache_106_gb300.step import DecodeStepRunner
 
     ws, rank, local = _dist_env()
@@ -507,7 +507,7 @@ def run_full40(args):
     import torch
 
     import paged_kv_cache_106_gb300 as pk
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
     from paged_kv_cache_106_gb300.step import DecodeStepRunner, admit_workload
 
     ws, rank, local = _dist_env()
@@ -644,7 +644,7 @@ def run_beam_churn(args):
     import torch
 
     import paged_kv_cache_106_gb300 as pk
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
     from paged_kv_cache_106_gb300.step import BeamGroups, DecodeStepRunner
 
     _, _, local = _dist_env()
@@ -747,7 +747,7 @@ def prefill_flops(lens_ctx, lens_q, num_heads, head_dim):
 def _prefill_cpu_baseline(seconds: float):
     """The oracle on a bounded sample of the prefill batch: its first 8 prompts."""
     from oracle import attention as oa
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
     from oracle.alloc import BlockManager
 
     w = wl.prefill_b256()
@@ -788,7 +788,7 @@ def run_prefill(args):
     import torch
 
     import paged_kv_cache_106_gb300 as pk
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
 
     ws, rank, local = _dist_env()
     torch.cuda.set_device(local)
@@ -953,7 +953,7 @@ def run_prefill(args):
 def _oracle_sample(n_seqs):
     """Host data for the first n_seqs sequences of the same workload, laid
     out by the oracle's own block manager."""
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
     from oracle.alloc import BlockManager
 
     w = wl.mixed_b256(steady_state=True)
@@ -1037,7 +1037,7 @@ def run_prefix_cache(args):
     import torch
 
     import paged_kv_cache_106_gb300 as pk
-    from paged_kv_cache_106_gb300 import workloads as wl
+    import workloads as wl
 
     _, _, local = _dist_env()
     torch.cuda.set_device(local)

@@ -132,7 +132,10 @@ int pa_seq_add(pa_pool *pool, int32_t seq_id, int32_t n_tokens, int64_t *slots_o
  * keys are cached (checked against the stored tokens, parent key and extra
  * key) are touched instead of allocated: their reference count goes up and a
  * cached block that was free leaves the free queue, no copy.  The scan stops
- * at the first block that is not cached.  The remaining blocks come from the
+ * at the first block that is not cached, and never reuses the block holding
+ * the last prompt token (a prompt that is all cached still gets that block
+ * new, so at least its last token is computed and nothing writes into a
+ * shared block).  The remaining blocks come from the
  * free queue, and the new full blocks are cached.  A cached block keeps its
  * key while its count is 0 -- freed blocks join the tail of the free queue,
  * so they are evicted (dropped from the cache) last, least recently freed
@@ -344,8 +347,9 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
  *   q_rows        rows of q and out (0: nothing to do)
  *   scale         finite and > 0 (1/sqrt(head_dim) in the pages)
  * head_dim 64 or 128, block_size 4..32.  Tensor cores: fp16 products, fp32
- * accumulation; the probabilities enter the second product as the sum of two
- * fp16 terms, so the fp16 rounding of the output dominates the error.
+ * accumulation; the probabilities (at most 2^8 after a lazy rescale of the
+ * running maximum) enter the second product as fp16, whose rounding stays
+ * below the fp16 rounding of the output.
  * Device-side problems go to *status and leave that sequence's rows
  * unwritten: PA_ERR_INVALID_ARG for q_len < 0, q_len > ctx,
  * q_len > max_q_len or rows outside [0, q_rows); PA_ERR_BAD_BLOCK for ctx > max_blocks * B or a table
@@ -373,12 +377,15 @@ int pa_prefill_attention(void *out, const void *q, const void *k_cache, const vo
  * (no cudaMalloc / cudaFree or allocating library routine); it clears the
  * scratch's scheduling word on the stream itself.
  *
- *   - A batch whose pa_decode_workspace_bytes(n_seqs, max_blocks, desc)
- *     exceeds PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_INVALID_ARG
- *     before any device work.
+ *   - Every argument is checked before any CUDA call; a batch whose
+ *     pa_decode_workspace_bytes(n_seqs, max_blocks, desc) exceeds
+ *     PA_NOALLOC_SCRATCH_BYTES is rejected with PA_ERR_INVALID_ARG.
  *   - The first call on a device looks up the scratch's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with that device current, which may load the
+ *     library's device code); make that first call before any stream
+ *     capture on the device.  A first call whose stream is being captured
+ *     is refused with PA_ERR_INVALID_ARG before the lookup; a lookup that
+ *     fails (PA_ERR_CUDA) is tried again by the next call.
  *   - All calls share the one scratch area, which keeps the last call's
  *     contents: calls whose work overlaps on the GPU (different streams,
  *     threads or processes sharing the context, without ordering between

@@ -154,7 +154,9 @@ class BlockManager:
         total, full = -(-n // B), n // B
         hits = []
         if self.prefix_caching:
-            for j in range(full):
+            # the block holding the last prompt token is never reused: that
+            # token's query must be computed, so its K/V is written afresh
+            for j in range((n - 1) // B if n else 0):
                 b = self.cache.get((extra_key, tuple(tokens[:(j + 1) * B])))
                 if b is None:
                     break

@@ -16,8 +16,8 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-# PAGEDKV_LIB may name another build of the same library (e.g. a tuning build)
-_LIB_PATH = os.environ.get("PAGEDKV_LIB") or os.path.join(_PKG, "libpagedkv.so")
+# always the library that the package's own build step writes next to it
+_LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 
 PA_OK = 0
 PA_ERR_INVALID_ARG = 1

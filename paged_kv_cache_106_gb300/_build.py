@@ -45,19 +45,17 @@ def _stale(out, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: bool = False) -> str:
-    """Compile and link the library; returns its path.  ``extra_flags`` go to
-    every nvcc compile (e.g. ``-DPA_TUNE_WARPS=4``); with ``out`` the library
-    is written elsewhere (objects go to a directory next to it)."""
-    out = out or LIB
-    objdir = OBJ if out == LIB else out + ".objs"
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link the library (only if a source is newer than it);
+    returns its path."""
+    out, objdir = LIB, OBJ
     srcs, deps = _inputs()
-    if not force and not extra_flags and not _stale(out, deps + [os.path.abspath(__file__)]):
+    if not force and not _stale(out, deps + [os.path.abspath(__file__)]):
         return out
     os.makedirs(objdir, exist_ok=True)
     nvcc = nvcc_path()
     common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=default",
-              "--expt-relaxed-constexpr", *ARCH, *extra_flags]
+              "--expt-relaxed-constexpr", *ARCH]
 
     def compile_one(src):
         obj = os.path.join(objdir, os.path.basename(src) + ".o")

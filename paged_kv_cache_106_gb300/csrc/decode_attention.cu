@@ -944,35 +944,15 @@ int sm_count() {
 template <int D, int B>
 struct PersistCfg {
     static constexpr int CHUNK = Geo<D, B>::CHUNK;
-#ifdef PA_TUNE_GH
-    static constexpr int GH = PA_TUNE_GH;
-#else
     // heads per unit: at least 8 KB of contiguous key (and value) rows per copy
     static constexpr int GH0 = 8192 / CHUNK;
     static constexpr int GH = GH0 < 1 ? 1 : (GH0 > 4 ? 4 : GH0);
-#endif
     static constexpr int STAGE = 2 * GH * CHUNK;
-#ifdef PA_TUNE_C
-    static constexpr int C = PA_TUNE_C;
-#else
     static constexpr int C = STAGE <= 8192 ? 4 : (STAGE <= 16384 ? 3 : 2);   // consumer warps
-#endif
-#ifdef PA_TUNE_SPC
-    static constexpr int SPC = PA_TUNE_SPC;
-#else
     static constexpr int SPC0 = (96 * 1024) / (C * STAGE);
-    static constexpr int SPC = SPC0 < 2 ? 2 : (SPC0 > 8 ? 8 : SPC0);
-#endif
-#ifdef PA_TUNE_R
-    static constexpr int R = PA_TUNE_R;
-#else
+    static constexpr int SPC = SPC0 < 2 ? 2 : (SPC0 > 8 ? 8 : SPC0);         // stages per consumer
     static constexpr int R = 3;       // unit slots (open units per CTA)
-#endif
-#ifdef PA_TUNE_PF
-    static constexpr int PF = PA_TUNE_PF;
-#else
     static constexpr int PF = 0;      // L2 prefetch distance, blocks (0: none)
-#endif
 };
 
 template <int D, int B, bool Persistent>
@@ -1015,11 +995,7 @@ int launch_db(const DecodeParams &prm_in, int part_tokens, cudaStream_t stream) 
         max_seqs[dev] = lo;
         per_sm_full[dev] = base;
     });
-#ifdef PA_TUNE_FORCE_GRID
-    if (false) {
-#else
     if (prm.n_seqs <= max_seqs[dev]) {
-#endif
         auto kern = pkern;
         const int use_smem = (int)L::bytes(prm.n_seqs);
         const int per_sm = per_sm_full[dev];
@@ -1161,13 +1137,56 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
 // array instead.  Every device that loads the library holds it until exit.
 // Host code cannot use the array's name as an address (on the host it is only
 // a stand-in for the symbol): the device address is looked up with
-// cudaGetSymbolAddress, once per device, with that device current, on the
-// first call there.  All calls share the array; concurrent calls race.
+// cudaGetSymbolAddress, with that device current, on the first call there
+// that gets past the argument checks.  A failed lookup is not remembered (the
+// next call tries again), and a first call made while its stream is being
+// captured is refused before the lookup.  All calls share the array;
+// concurrent calls race.
 namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
-std::once_flag g_noalloc_once[64];
-void *g_noalloc_ptr[64];
-cudaError_t g_noalloc_err[64];
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];   // guarded by g_noalloc_mu; null until a lookup succeeds
+
+// The scratch's device address on the current device (looked up once).
+int noalloc_scratch(cudaStream_t stream, void **out) {
+    using namespace pagedkv;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaGetDevice: %s",
+                    cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: device %d is beyond the %d "
+                    "devices this library tracks", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev]) {
+        *out = g_noalloc_ptr[dev];
+        return PA_OK;
+    }
+    // The lookup may load the module; it must not run inside a stream capture.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) {
+        cudaGetLastError();   // not sticky: keep it out of later launch checks
+        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaStreamIsCapturing: %s",
+                    cudaGetErrorString(e));
+    }
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_attention_noalloc: the first call on device "
+                    "%d was made while its stream is being captured; make one call before any "
+                    "capture (it looks up the scratch address)", dev);
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaGetSymbolAddress: %s",
+                    cudaGetErrorString(e));
+    }
+    g_noalloc_ptr[dev] = ptr;
+    *out = ptr;
+    return PA_OK;
+}
 }  // namespace
 
 extern "C" int pa_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
@@ -1176,27 +1195,33 @@ extern "C" int pa_decode_attention_noalloc(void *out, const void *q, const void 
                                            int32_t max_blocks, float scale, int32_t *status,
                                            const pa_pool_desc *desc, void *stream) {
     using namespace pagedkv;
+    // every argument error is reported before any CUDA call
+    std::string why;
     if (!desc) return fail(PA_ERR_INVALID_ARG, "pa_decode_attention_noalloc: NULL desc");
+    if (!device_geometry_ok(desc, &why))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_attention_noalloc: %s", why.c_str());
+    if (n_seqs < 0 || n_seqs > 65535 || max_blocks < 0 || desc->num_heads > 65535)
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_noalloc: n_seqs=%d (<= 65535), max_blocks=%d, "
+                    "num_heads=%d", n_seqs, max_blocks, desc->num_heads);
+    if (n_seqs == 0) return PA_OK;
     const size_t need = decode_workspace_bytes(n_seqs, max_blocks, desc);
     if (need > PA_NOALLOC_SCRATCH_BYTES)
         return fail(PA_ERR_INVALID_ARG,
                     "pa_decode_attention_noalloc: the batch needs %zu bytes of scratch, the "
                     "fixed scratch holds %zu (use pa_decode_attention with a workspace)",
                     need, (size_t)PA_NOALLOC_SCRATCH_BYTES);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64)
-        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaGetDevice: %s",
-                    cudaGetErrorString(e));
-    std::call_once(g_noalloc_once[dev], [&] {
-        void *ptr = nullptr;
-        g_noalloc_err[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        g_noalloc_ptr[dev] = ptr;
-    });
-    if (g_noalloc_err[dev] != cudaSuccess || !g_noalloc_ptr[dev])
-        return fail(PA_ERR_CUDA, "pa_decode_attention_noalloc: cudaGetSymbolAddress: %s",
-                    cudaGetErrorString(g_noalloc_err[dev]));
+    if (!out || !q || !k_cache || !v_cache || !ctx_lens || (max_blocks > 0 && !block_tables))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_attention_noalloc: NULL pointer");
+    if (((uintptr_t)out | (uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_attention_noalloc: out/q/caches must be 16-byte aligned");
+    if (!std::isfinite(scale))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_attention_noalloc: scale is not finite");
+    void *scratch = nullptr;
+    const int rc = noalloc_scratch(static_cast<cudaStream_t>(stream), &scratch);
+    if (rc != PA_OK) return rc;
     return launch_decode_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, n_seqs,
-                                   max_blocks, scale, g_noalloc_ptr[dev],
-                                   (size_t)PA_NOALLOC_SCRATCH_BYTES, status, desc, stream);
+                                   max_blocks, scale, scratch, (size_t)PA_NOALLOC_SCRATCH_BYTES,
+                                   status, desc, stream);
 }

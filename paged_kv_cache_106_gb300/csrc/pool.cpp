@@ -214,7 +214,10 @@ int pa_seq_add_tokens(pa_pool *pool, int32_t seq_id, int32_t n_tokens, const int
     const int32_t B = pool->block_size;
     const int32_t total = (int32_t)(((int64_t)n_tokens + B - 1) / B);
     const int32_t full = n_tokens / B;
-    // 1. the longest run of leading full blocks already in the cache
+    // 1. the longest run of leading full blocks already in the cache, short
+    // of the block holding the last prompt token: that token's query must be
+    // computed, so its block is always new and written by the caller
+    const int32_t reusable = n_tokens > 0 ? (n_tokens - 1) / B : 0;
     std::vector<int32_t> hit;
     std::vector<uint64_t> keys((size_t)full);
     uint64_t parent = kRootKey;
@@ -222,6 +225,7 @@ int pa_seq_add_tokens(pa_pool *pool, int32_t seq_id, int32_t n_tokens, const int
     for (int32_t j = 0; j < full; ++j) {
         const int32_t *tok = token_ids + (int64_t)j * B;
         keys[(size_t)j] = block_key(parent, tok, B, extra_key);
+        if (chain && j >= reusable) chain = false;
         if (chain) {
             auto it = pool->cache.find(keys[(size_t)j]);
             const int32_t b = it == pool->cache.end() ? -1 : it->second;

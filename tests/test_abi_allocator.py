@@ -212,6 +212,28 @@ def test_device_calls_reject_bad_geometry_before_any_cuda_work():
         pk.PA_ERR_INVALID_ARG
 
 
+def test_noalloc_rejects_every_bad_argument_before_any_cuda_call():
+    """The workspace-free decode call checks its arguments first: with no GPU
+    in the process, a CUDA call would fail with PA_ERR_CUDA instead."""
+    noalloc = lambda desc, n, mb, ptrs=None: pk._lib.pa_decode_attention_noalloc(
+        *(ptrs or (None,) * 6), n, mb, pk.ctypes.c_float(1.0), None, desc, None)
+    bad = pk.PoolDesc(4, 5, num_heads=2, head_dim=8)
+    assert noalloc(bad.ref, 1, 4) == pk.PA_ERR_INVALID_ARG
+    assert "block_size" in pk.pa_last_error_string()
+    assert noalloc(None, 1, 4) == pk.PA_ERR_INVALID_ARG
+    d = pk.PoolDesc(4, 16, num_heads=40, head_dim=128)
+    assert noalloc(d.ref, -1, 4) == pk.PA_ERR_INVALID_ARG
+    assert noalloc(d.ref, 1, -4) == pk.PA_ERR_INVALID_ARG
+    assert noalloc(d.ref, 0, 4) == pk.PA_OK                   # empty batch: nothing to do
+    assert noalloc(d.ref, 2048, 128) == pk.PA_ERR_INVALID_ARG  # workspace beyond the scratch
+    assert "scratch" in pk.pa_last_error_string()
+    assert noalloc(d.ref, 2, 4) == pk.PA_ERR_INVALID_ARG       # NULL pointers
+    assert "NULL" in pk.pa_last_error_string()
+    odd = (8, 16, 16, 16, 16, 16)                              # out not 16-byte aligned
+    assert noalloc(d.ref, 2, 4, odd) == pk.PA_ERR_INVALID_ARG
+    assert "aligned" in pk.pa_last_error_string()
+
+
 @pytest.mark.parametrize("seed", range(25))
 def test_multi_token_append_lockstep(seed):
     """pa_alloc_slots_n against repeated single appends in the oracle."""

@@ -8,7 +8,7 @@ import pytest
 
 import paged_kv_cache_106_gb300 as pk
 from oracle.alloc import BlockManager
-from paged_kv_cache_106_gb300 import workloads as wl
+import workloads as wl
 from paged_kv_cache_106_gb300.step import BeamGroups
 
 

@@ -22,7 +22,7 @@ import torch
 import paged_kv_cache_106_gb300 as pk
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from paged_kv_cache_106_gb300 import workloads as wl
+import workloads as wl
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-3

@@ -12,7 +12,7 @@ import paged_kv_cache_106_gb300 as pk
 from oracle import attention as oa
 from oracle import cache_ops as oc
 from oracle.alloc import BlockManager, move_group
-from paged_kv_cache_106_gb300 import workloads as wl
+import workloads as wl
 
 pytestmark = pytest.mark.gpu
 H, D, B = 8, 128, 16

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import paged_kv_cache_106_gb300 as pk
-from paged_kv_cache_106_gb300 import workloads as wl
+import workloads as wl
 from paged_kv_cache_106_gb300.step import DecodeStepRunner
 from oracle import attention as oa
 from oracle import cache_ops as oc

@@ -66,6 +66,24 @@ def test_same_system_prompt_is_touched_not_allocated():
     x.check()
 
 
+def test_all_cached_prompt_recomputes_its_last_block():
+    """A prompt whose every block is cached (its length a multiple of B) does
+    not reuse the block of its last token: the prefill needs that token's
+    query, so the block is taken new and its B tokens are reported uncached
+    (the pages do not cover this case; no write lands in a shared block)."""
+    x = Both(16)
+    prompt = list(range(200, 212))                 # three full blocks
+    assert x.add(0, prompt) == 0
+    assert x.add(1, prompt) == 8                   # blocks 0 and 1 reused, block 2 new
+    t0, t1 = x.m.block_table(0), x.m.block_table(1)
+    assert t0[:2] == t1[:2] and t0[2] != t1[2]
+    assert [x.m.ref[b] for b in t1] == [2, 2, 1]
+    x.check()
+    assert x.add(2, prompt[:4]) == 0               # one full block, the last token's: new
+    assert x.m.block_table(2)[0] != t0[0]
+    x.check()
+
+
 def test_extra_key_and_divergence_break_sharing():
     x = Both(32)
     p = list(range(12))

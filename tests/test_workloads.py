@@ -14,7 +14,7 @@ import os
 
 import numpy as np
 
-from paged_kv_cache_106_gb300 import workloads as wl
+import workloads as wl
 from tests.conftest import GOLDEN
 
 
