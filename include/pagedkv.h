@@ -196,6 +196,23 @@ int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
                    int64_t *slot_mapping_out, int32_t *copies_out, int32_t copies_cap,
                    int32_t *n_copies_out);
 
+/* One decode step's host work for a batch, in one call: pa_alloc_slots
+ * for seq_ids (one new token each, copy-on-write pairs to copies_out), then
+ * the batch's block tables and context lengths as pa_get_block_tables
+ * exports them, after the append ([review] §4.3 decoding: the block manager
+ * maps each new token to a slot; §4.6: the scheduler hands the block tables
+ * to the workers).  Written for a serving loop that stages these arrays in
+ * page-locked host memory and uploads them with one copy:
+ *   slot_mapping_out (host, n_seqs int64), ctx_lens_out (host, n_seqs int32),
+ *   tables_out (host, n_seqs x max_blocks int32, padded with -1),
+ *   copies_out (host, copies_cap x 2 int32), *n_copies_out.
+ * All-or-nothing: also fails with no change when a table would grow beyond
+ * max_blocks (PA_ERR_INVALID_ARG).  Errors: as pa_alloc_slots. */
+int pa_decode_step_prepare(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                           int32_t max_blocks, int64_t *slot_mapping_out, int32_t *ctx_lens_out,
+                           int32_t *tables_out, int32_t *copies_out, int32_t copies_cap,
+                           int32_t *n_copies_out);
+
 /* Swapping ([review] §4.5 (1) swapping; [notes] §3.5 Swapping, CPU block
  * manager): a preempted group of sequences moves, all its blocks at once,
  * from the GPU pool to a second pool that manages swap space in host memory,

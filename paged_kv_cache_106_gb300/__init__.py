@@ -85,6 +85,7 @@ def _load():
         "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
         "pa_alloc_slots_n": (i32, [vp, i32, vp, vp, vp, vp, i32, P(i32)]),
         "pa_get_block_tables": (i32, [vp, i32, vp, i32, vp, vp]),
+        "pa_decode_step_prepare": (i32, [vp, i32, vp, i32, vp, vp, vp, vp, i32, P(i32)]),
         "pa_seq_info": (i32, [vp, i32, P(i32), P(i32)]),
         "pa_pool_num_free": (i32, [vp, P(i32)]),
         "pa_pool_free_queue": (i32, [vp, vp, i32, P(i32)]),
@@ -305,6 +306,26 @@ def pa_get_block_tables(pool, seq_ids, max_blocks: int, tables_out=None, ctx_out
     _check(_lib.pa_get_block_tables(pool, n, ids.ctypes.data, int(max_blocks),
                                     tables.ctypes.data, ctx.ctypes.data))
     return tables, ctx
+
+
+def pa_decode_step_prepare(pool, seq_ids, max_blocks: int, slot_out=None, ctx_out=None,
+                           tables_out=None, copies_out=None, copies_cap: int | None = None):
+    """One token appended to every sequence, then the batch's tables.
+    Returns (slot_mapping int64[n], ctx_lens int32[n], tables int32[n, max_blocks],
+    copies int32[n_copies, 2]); the *_out arrays (e.g. views of a pinned
+    staging buffer) are written in place when given."""
+    ids = _host_i32(seq_ids)
+    n = ids.shape[0]
+    cap = n if copies_cap is None else int(copies_cap)
+    slots = np.empty(n, np.int64) if slot_out is None else slot_out
+    ctx = np.empty(n, np.int32) if ctx_out is None else ctx_out
+    tables = np.empty((n, max_blocks), np.int32) if tables_out is None else tables_out
+    copies = np.empty((max(cap, 1), 2), np.int32) if copies_out is None else copies_out
+    nc = ctypes.c_int32(0)
+    _check(_lib.pa_decode_step_prepare(pool, n, ids.ctypes.data, int(max_blocks),
+                                       slots.ctypes.data, ctx.ctypes.data, tables.ctypes.data,
+                                       copies.ctypes.data, cap, ctypes.byref(nc)))
+    return slots, ctx, tables, copies[: nc.value]
 
 
 def pa_seq_info(pool, seq_id: int):

@@ -37,6 +37,7 @@ namespace {
 struct Seq {
     std::vector<int32_t> table;
     int32_t num_tokens = 0;
+    uint64_t stamp = 0;   // the batched call that last listed it (duplicate check)
 };
 
 }  // namespace
@@ -55,6 +56,14 @@ struct pa_pool {
     int64_t count = 0;
     std::vector<int32_t> ref;
     std::unordered_map<int32_t, Seq> seqs;
+    // Scratch of the batched appends, kept between calls so that a call
+    // allocates nothing: a call number for the duplicate check, reference
+    // decrements planned per block (zero between calls) and the blocks they
+    // touched, the sequences of the call.
+    uint64_t epoch = 0;
+    std::vector<int32_t> plan_dec;
+    std::vector<int32_t> plan_touched;
+    std::vector<Seq *> plan_seqs;
     // Prefix cache: full prompt blocks keyed by a hash chain over
     // (parent key, the block's token ids, extra key).  Per block: its key,
     // its parent's key, the extra key and its token ids, to verify a hit.
@@ -148,6 +157,7 @@ int pa_pool_create(const pa_pool_desc *desc, pa_pool **out) {
     p->prv.assign(nb, -1);
     p->in_queue.assign(nb, 0);
     p->ref.assign(nb, 0);
+    p->plan_dec.assign(nb, 0);
     p->caching = (desc->flags & PA_POOL_PREFIX_CACHING) != 0;
     if (p->caching) {
         p->cached.assign(nb, 0);
@@ -404,61 +414,79 @@ int pa_seq_free(pa_pool *pool, int32_t seq_id) {
     return PA_OK;
 }
 
-int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
-                   int64_t *slot_mapping_out, int32_t *copies_out, int32_t copies_cap,
-                   int32_t *n_copies_out) {
-    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: NULL pool");
-    if (n_seqs < 0 || (n_seqs > 0 && (!seq_ids || !slot_mapping_out)) || copies_cap < 0 ||
-        (copies_cap > 0 && !copies_out))
-        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: bad arguments");
+}  // extern "C"
+
+namespace {
+
+// Dry run of one appended token for each of seq_ids (pa_alloc_slots): looks
+// the sequences up into pool->plan_seqs and counts the new blocks and the
+// copies.  Only the reference counts of shared last blocks change between
+// the sequences of one call (each sequence appears once, new blocks belong
+// to one sequence), so tracking those decrements reproduces the real pass
+// exactly.  With max_blocks >= 0, a table that would grow beyond it fails
+// the call.  Changes no state but the scratch.
+int plan_append(pa_pool *pool, const char *who, int32_t n_seqs, const int32_t *seq_ids,
+                int32_t max_blocks, int64_t *need_out, int32_t *n_copies_out) {
     const int32_t B = pool->block_size;
-    // Dry run: the blocks and copies this call needs.  Only the reference
-    // counts of shared last blocks change between the sequences of one call
-    // (each sequence appears once, new blocks belong to one sequence), so
-    // tracking those decrements reproduces the real pass exactly.
-    std::vector<Seq *> seq(static_cast<size_t>(n_seqs));
-    std::unordered_set<int32_t> ids;
-    std::unordered_map<int32_t, int32_t> dec;
-    ids.reserve((size_t)n_seqs * 2);
+    const uint64_t epoch = ++pool->epoch;
+    pool->plan_seqs.resize((size_t)n_seqs);
+    pool->plan_touched.clear();
     int64_t need = 0;
     int32_t n_copies = 0;
+    int rc = PA_OK;
     for (int32_t i = 0; i < n_seqs; ++i) {
         auto it = pool->seqs.find(seq_ids[i]);
-        if (it == pool->seqs.end())
-            return fail(PA_ERR_NO_SEQ, "pa_alloc_slots: no sequence %d", seq_ids[i]);
-        if (!ids.insert(seq_ids[i]).second)
-            return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: sequence %d listed twice",
-                        seq_ids[i]);
+        if (it == pool->seqs.end()) {
+            rc = fail(PA_ERR_NO_SEQ, "%s: no sequence %d", who, seq_ids[i]);
+            break;
+        }
         Seq &s = it->second;
-        seq[(size_t)i] = &s;
+        if (s.stamp == epoch) {
+            rc = fail(PA_ERR_INVALID_ARG, "%s: sequence %d listed twice", who, seq_ids[i]);
+            break;
+        }
+        s.stamp = epoch;
+        pool->plan_seqs[(size_t)i] = &s;
+        size_t blocks_after = s.table.size();
         if (s.table.empty() || pool->last_filled(s) == B) {
             ++need;
+            ++blocks_after;
         } else {
-            int32_t last = s.table.back();
-            int32_t &d = dec[last];
+            const int32_t last = s.table.back();
+            int32_t &d = pool->plan_dec[(size_t)last];
             if (pool->ref[(size_t)last] - d > 1) {
+                if (d == 0) pool->plan_touched.push_back(last);
                 ++need;
                 ++n_copies;
                 ++d;
             }
         }
+        if (max_blocks >= 0 && (int64_t)blocks_after > max_blocks) {
+            rc = fail(PA_ERR_INVALID_ARG, "%s: sequence %d would have %zu blocks > max_blocks %d",
+                      who, seq_ids[i], blocks_after, max_blocks);
+            break;
+        }
     }
-    if (need > pool->count)
-        return fail(PA_ERR_OUT_OF_BLOCKS, "pa_alloc_slots: need %lld blocks, %lld free",
-                    (long long)need, (long long)pool->count);
-    if (n_copies > copies_cap)
-        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: %d copies needed, copies_cap is %d",
-                    n_copies, copies_cap);
-    // Real pass.
+    for (int32_t b : pool->plan_touched) pool->plan_dec[(size_t)b] = 0;
+    pool->plan_touched.clear();
+    *need_out = need;
+    *n_copies_out = n_copies;
+    return rc;
+}
+
+// The real pass over pool->plan_seqs, after a successful plan_append.
+int32_t commit_append(pa_pool *pool, int32_t n_seqs, int64_t *slot_mapping_out,
+                      int32_t *copies_out) {
+    const int32_t B = pool->block_size;
     int32_t c = 0;
     for (int32_t i = 0; i < n_seqs; ++i) {
-        Seq &s = *seq[(size_t)i];
+        Seq &s = *pool->plan_seqs[(size_t)i];
         if (s.table.empty() || pool->last_filled(s) == B) {
             s.table.push_back(pool->pop_free());
         } else {
-            int32_t last = s.table.back();
+            const int32_t last = s.table.back();
             if (pool->ref[(size_t)last] > 1) {
-                int32_t nb = pool->pop_free();
+                const int32_t nb = pool->pop_free();
                 copies_out[2 * c] = last;
                 copies_out[2 * c + 1] = nb;
                 ++c;
@@ -466,9 +494,67 @@ int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
                 s.table.back() = nb;
             }
         }
-        int32_t off = s.num_tokens - (int32_t)(s.table.size() - 1) * B;
+        const int32_t off = s.num_tokens - (int32_t)(s.table.size() - 1) * B;
         slot_mapping_out[i] = (int64_t)s.table.back() * B + off;
         ++s.num_tokens;
+    }
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_alloc_slots(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                   int64_t *slot_mapping_out, int32_t *copies_out, int32_t copies_cap,
+                   int32_t *n_copies_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: NULL pool");
+    if (n_seqs < 0 || (n_seqs > 0 && (!seq_ids || !slot_mapping_out)) || copies_cap < 0 ||
+        (copies_cap > 0 && !copies_out))
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: bad arguments");
+    int64_t need = 0;
+    int32_t n_copies = 0;
+    int rc = plan_append(pool, "pa_alloc_slots", n_seqs, seq_ids, -1, &need, &n_copies);
+    if (rc != PA_OK) return rc;
+    if (need > pool->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "pa_alloc_slots: need %lld blocks, %lld free",
+                    (long long)need, (long long)pool->count);
+    if (n_copies > copies_cap)
+        return fail(PA_ERR_INVALID_ARG, "pa_alloc_slots: %d copies needed, copies_cap is %d",
+                    n_copies, copies_cap);
+    const int32_t c = commit_append(pool, n_seqs, slot_mapping_out, copies_out);
+    if (n_copies_out) *n_copies_out = c;
+    return PA_OK;
+}
+
+int pa_decode_step_prepare(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                           int32_t max_blocks, int64_t *slot_mapping_out, int32_t *ctx_lens_out,
+                           int32_t *tables_out, int32_t *copies_out, int32_t copies_cap,
+                           int32_t *n_copies_out) {
+    const char *who = "pa_decode_step_prepare";
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "%s: NULL pool", who);
+    if (n_seqs < 0 || max_blocks < 0 || copies_cap < 0 || (copies_cap > 0 && !copies_out) ||
+        (n_seqs > 0 && (!seq_ids || !slot_mapping_out || !ctx_lens_out ||
+                        (max_blocks > 0 && !tables_out))))
+        return fail(PA_ERR_INVALID_ARG, "%s: bad arguments", who);
+    int64_t need = 0;
+    int32_t n_copies = 0;
+    int rc = plan_append(pool, who, n_seqs, seq_ids, max_blocks, &need, &n_copies);
+    if (rc != PA_OK) return rc;
+    if (need > pool->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "%s: need %lld blocks, %lld free", who,
+                    (long long)need, (long long)pool->count);
+    if (n_copies > copies_cap)
+        return fail(PA_ERR_INVALID_ARG, "%s: %d copies needed, copies_cap is %d", who, n_copies,
+                    copies_cap);
+    const int32_t c = commit_append(pool, n_seqs, slot_mapping_out, copies_out);
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        const Seq &s = *pool->plan_seqs[(size_t)i];
+        int32_t *row = tables_out + (int64_t)i * max_blocks;
+        const size_t n = s.table.size();   // >= 1: the call appended a token
+        std::memcpy(row, s.table.data(), n * sizeof(int32_t));
+        for (int32_t j = (int32_t)n; j < max_blocks; ++j) row[j] = -1;
+        ctx_lens_out[i] = s.num_tokens;
     }
     if (n_copies_out) *n_copies_out = c;
     return PA_OK;

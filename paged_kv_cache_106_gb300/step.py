@@ -3,14 +3,15 @@
 Per step (vLLM paper review, mz-moonzoo.tistory.com/116, §4.3 global
 execution loop; §4.6: the scheduler hands block tables to the worker):
 
-1. ``pa_alloc_slots``      host block manager: one slot per sequence, plus
-                           the copy-on-write pairs;
-2. ``pa_get_block_tables`` host: tables and context lengths for the batch;
-3. one pinned host -> device copy carrying slot mapping, context lengths,
+1. ``pa_decode_step_prepare`` host block manager, one call: one slot per
+                           sequence, the copy-on-write pairs, then the
+                           batch's tables and context lengths, written
+                           straight into the pinned staging buffer;
+2. one pinned host -> device copy carrying slot mapping, context lengths,
    block tables and copy pairs (double-buffered staging, so the host can
    prepare step t+1 while the GPU still runs step t);
-4. ``pa_copy_blocks``      copy-on-write copies, every layer (only if any);
-5. per layer ``pa_write_kv`` then ``pa_decode_attention``.
+3. ``pa_copy_blocks``      copy-on-write copies, every layer (only if any);
+4. per layer ``pa_write_kv`` then ``pa_decode_attention``.
 
 Everything is enqueued on one stream.  This module only sequences library
 calls and owns the staging buffers; the work runs in libpagedkv.so.
@@ -22,8 +23,8 @@ import time
 import numpy as np
 import torch
 
-from . import (PoolDesc, pa_alloc_slots, pa_copy_blocks, pa_decode_attention,
-               pa_decode_workspace_bytes, pa_get_block_tables, pa_write_kv)
+from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_prepare,
+               pa_decode_workspace_bytes, pa_write_kv)
 
 
 def _align(x, a=256):
@@ -80,9 +81,9 @@ class DecodeStepRunner:
             self.events[k].synchronize()     # staging buffer k no longer in flight
         t0 = time.perf_counter()
         slots, ctx, tables, copies = self._views(self.host[k])
-        _, cp = pa_alloc_slots(self.pool, self.ids, copies_cap=self.S, slot_out=slots,
-                               copies_out=copies)
-        pa_get_block_tables(self.pool, self.ids, self.max_blocks, tables_out=tables, ctx_out=ctx)
+        _, _, _, cp = pa_decode_step_prepare(self.pool, self.ids, self.max_blocks, slot_out=slots,
+                                             ctx_out=ctx, tables_out=tables, copies_out=copies,
+                                             copies_cap=self.S)
         self.host_seconds = time.perf_counter() - t0   # block manager work of this step
         self._pending = (k, int(cp.shape[0]), ctx)
 

@@ -2,6 +2,7 @@
 against the pages' worked examples and, operation by operation, against the
 oracle's block manager: slots, copy pairs, block tables, token counts,
 reference counts and the free queue must be identical (bit-exact indexing)."""
+import copy
 import random
 import re
 import subprocess
@@ -146,6 +147,100 @@ def test_lockstep_with_oracle(seed):
                 got = abi.alloc_slots(seqs)
                 assert got[0] == exp[0]
                 assert [tuple(c) for c in got[1]] == exp[1]
+        _compare(abi, m, live)
+
+
+class FusedStepAdapter(AbiAdapter):
+    """The same block manager, appending through pa_decode_step_prepare."""
+
+    def alloc_slots(self, seqs):
+        nb = max([pk.pa_seq_info(self.p, s)[1] for s in seqs] + [0]) + 1
+        slots, ctx, tables, copies = pk.pa_decode_step_prepare(self.p, seqs, nb)
+        for i, s in enumerate(seqs):
+            nt, n = pk.pa_seq_info(self.p, s)
+            assert ctx[i] == nt
+            assert tables[i, n:].tolist() == [-1] * (nb - n)
+        return slots.tolist(), copies.tolist()
+
+
+@pytest.mark.parametrize("name", GOLDEN)
+def test_golden_examples_through_the_fused_step_call(golden_dir, name):
+    doc = load(golden_dir, name)
+    replay(doc, FusedStepAdapter(doc))
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_fused_step_call_lockstep_with_oracle(seed):
+    """pa_decode_step_prepare = pa_alloc_slots followed by the table export:
+    slots, copies, padded tables and token counts against the oracle, and
+    the same all-or-nothing failures (out of blocks, a table that would
+    outgrow max_blocks, a sequence listed twice, an unknown sequence)."""
+    rng = random.Random(5000 + seed)
+    B = rng.choice([1, 2, 4, 16])
+    nb = rng.randint(0, 48)
+    order = list(range(nb))
+    rng.shuffle(order)
+    abi = AbiAdapter({"num_blocks": nb, "block_size": B, "free_order": order})
+    m = BlockManager(nb, B, order)
+    live, nxt = set(), 0
+    for _ in range(300):
+        r = rng.random()
+        if r < 0.2 or not live:
+            n = rng.randint(0, 3 * B)
+            try:
+                exp = m.add(nxt, n)
+            except OutOfBlocks:
+                with pytest.raises(pk.OutOfBlocks):
+                    abi.add(nxt, n)
+            else:
+                assert abi.add(nxt, n) == exp
+                live.add(nxt)
+            nxt += 1
+        elif r < 0.35:
+            p = rng.choice(sorted(live))
+            m.fork(p, nxt)
+            abi.fork(p, nxt)
+            live.add(nxt)
+            nxt += 1
+        elif r < 0.45:
+            s = rng.choice(sorted(live))
+            m.free(s)
+            abi.free(s)
+            live.discard(s)
+        else:
+            seqs = rng.sample(sorted(live), rng.randint(1, len(live)))
+            longest = max(len(m.block_table(s)) for s in seqs)
+            mb = longest + rng.choice([0, 1, 1, 2])      # 0: may be one short after the append
+            probe = rng.random()
+            if probe < 0.1:                              # a sequence listed twice
+                with pytest.raises(pk.PagedKVError) as e:
+                    pk.pa_decode_step_prepare(abi.p, seqs + seqs[:1], mb + 1)
+                assert e.value.code == pk.PA_ERR_INVALID_ARG
+            elif probe < 0.15:                           # an unknown sequence
+                with pytest.raises(pk.PagedKVError) as e:
+                    pk.pa_decode_step_prepare(abi.p, seqs + [10 ** 6], mb + 1)
+                assert e.value.code == pk.PA_ERR_NO_SEQ
+            else:
+                saved = copy.deepcopy(m)
+                try:
+                    exp_slots, exp_copies = m.alloc_slots(seqs)
+                except OutOfBlocks:
+                    # either failure may be the one reported when both apply
+                    with pytest.raises(pk.PagedKVError) as e:
+                        pk.pa_decode_step_prepare(abi.p, seqs, mb)
+                    assert e.value.code in (pk.PA_ERR_OUT_OF_BLOCKS, pk.PA_ERR_INVALID_ARG)
+                else:
+                    if max(len(m.block_table(s)) for s in seqs) > mb:
+                        m = saved                        # the call must change nothing
+                        with pytest.raises(pk.PagedKVError) as e:
+                            pk.pa_decode_step_prepare(abi.p, seqs, mb)
+                        assert e.value.code == pk.PA_ERR_INVALID_ARG
+                    else:
+                        slots, ctx, tables, copies = pk.pa_decode_step_prepare(abi.p, seqs, mb)
+                        assert slots.tolist() == exp_slots
+                        assert [tuple(c) for c in copies.tolist()] == exp_copies
+                        assert tables.tolist() == m.padded_tables(seqs, mb)
+                        assert ctx.tolist() == [m.num_tokens(s) for s in seqs]
         _compare(abi, m, live)
 
 
