@@ -11,14 +11,18 @@ and replaced by a newly drawn one, so the length mix stays stationary over
 thousands of steps.  (A newcomer's prompt K/V is not written -- prefill is
 another kernel -- its blocks keep the finite values of earlier occupants.)
 
-One step = the whole hot path: host block manager (pa_alloc_slots, table
-export), one packed metadata upload, copy-on-write copies (none in this
-workload), the slot write of the new K/V, and decode attention (split +
-merge).  ``value`` is K/V token positions attended per second
+One step = the whole hot path: host block manager (pa_decode_step_prepare:
+append and table export), one packed metadata upload, copy-on-write copies
+(none in this workload), the slot write of the new K/V, and decode attention
+(split + merge).  ``value`` is K/V token positions attended per second
 (sum of context lengths / step time), inputs resident in HBM (the K/V
-working set, ~2.8 GB, is far larger than L2, so no L2 flush is needed).
+working set, ~3.5 GB, is far larger than L2, so no L2 flush is needed).
 ``e2e`` repeats the step with q / k / v uploaded from pinned host memory and
-the output read back to host every step, wall-clock timed.
+the output read back to host every step, wall-clock timed.  After the timed
+region, ``kernels`` adds the 64-sequence batch (context uniform in
+[128, 2048]) against the HBM roof, parallel sampling with copy-on-write
+(L2-resident, GB/s only) and causal prefill of the mixed batch's prompts
+against its binding roof.
 """
 from __future__ import annotations
 
@@ -376,6 +380,24 @@ def run_ours(args):
     (tokens_all, e2e_tokens_all), (elapsed_max, e2e_max) = reduce_across_ranks(
         [stats["tokens"], e2e_tokens], [elapsed, e2e_time], dev)
 
+    # ---- the other measured rows, on rank 0, after the timed region: the
+    # 64-sequence batch, parallel sampling with copy-on-write, and causal
+    # prefill of the mixed batch's prompts against its binding roof
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra["decode_opt13b_b64"] = decode_b64_stats(dev)
+        extra["parallel_sampling"] = parallel_sampling_stats(dev)
+        pb = PrefillBatch(dev)
+        _, pf_ms, pf_wkv_ms = pb.time_steps(20, 3)
+        pf = pb.roofline(pf_ms)
+        pf.update({"workload": f"causal prefill of {len(pb.lens)} whole prompts (lognormal, "
+                               f"median 200, cap 1536; {pb.T} tokens), OPT-13B layer 40x128, "
+                               "block 16", "launches": 20,
+                   "prompt_tokens_per_s": pb.T / (pf_ms / 1e3),
+                   "slot_write_us_for_the_prompts": pf_wkv_ms * 1e3})
+        extra["pa_prefill_attention"] = pf
+        pb.close()
+
     if rank == 0:
         peak, peak_kind = _peaks()
         attn_avg_s = sum(attn_ms) / len(attn_ms) / 1e3
@@ -432,12 +454,14 @@ def run_ours(args):
                     "GB/s": (2 * 2 * S * H * D * 2 + 8 * S) / (sum(write_ms) / len(write_ms) / 1e3) / 1e9,
                     "note": "new K/V of the batch read and scattered to their slots (timed in the step loop)",
                 },
+                **extra,
                 "pa_copy_blocks": copy_stats,
                 "pa_swap_blocks": swap_stats,
                 "host_block_manager": {
                     "us_per_step": 1e6 * sum(host_s) / len(host_s),
-                    "note": "host wall clock per step: free/admit finished sequences, pa_alloc_slots "
-                            "and pa_get_block_tables for the batch (waits on the GPU excluded)",
+                    "note": "host wall clock per step: free/admit finished sequences, then "
+                            "pa_decode_step_prepare (one token per sequence, tables and lengths "
+                            "into the pinned staging buffer); waits on the GPU excluded",
                 },
             },
             "e2e": {
@@ -637,6 +661,143 @@ def time_swap_blocks(pk, desc, w, kc, vc, stream, n_pairs=256, reps=20):
     return res
 
 
+def decode_b64_stats(dev, steps: int = 200, warmup: int = 5) -> dict:
+    """The 64-sequence OPT-13B batch (context uniform in [128, 2048], pool
+    1.25x the blocks needed, shuffled free queue): decode steps through the
+    runner, attention per launch timed with CUDA events on its stream, its
+    algorithmic bytes from the step's contexts (K/V of every attended token,
+    tables, lengths, q read, o written)."""
+    import torch
+
+    import paged_kv_cache_106_gb300 as pk
+    import workloads as wl
+    from paged_kv_cache_106_gb300.step import DecodeStepRunner
+
+    w = wl.opt13b_b64()
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    desc, pool = _pool_setup(pk, w)
+    S = len(w.prompt_lens)
+    ids = np.arange(S, dtype=np.int32)
+    max_blocks = -(-(max(w.prompt_lens) + warmup + steps + 1) // B)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed)
+    kc = torch.empty((w.num_blocks, H, B, D), dtype=torch.float16, device=dev).normal_(generator=gen)
+    vc = torch.empty_like(kc).normal_(generator=gen)
+    q, k_new, v_new = (torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+                       for _ in range(3))
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream(device=dev)
+    runner = DecodeStepRunner(pool, desc, ids, max_blocks, device=dev, stream=stream)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
+    nbytes, tokens = 0, 0
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            runner.prepare()
+            ctx = runner.ctx_host.astype(np.int64)
+            runner.copy_blocks([kc], [vc])
+            runner.write_kv(k_new, v_new, kc, vc)
+            j = i - warmup
+            if j >= 0:
+                evs[j][0].record(stream)
+            runner.attention(out, q, kc, vc, w.scale)
+            if j >= 0:
+                evs[j][1].record(stream)
+                tokens += int(ctx.sum())
+                nbytes += int(ctx.sum()) * H * D * 4 + int(((ctx + B - 1) // B).sum()) * 4 \
+                    + S * 4 + S * H * D * 4
+    torch.cuda.synchronize()
+    assert runner.status.item() == 0, runner.status.item()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    peak, kind = _peaks()
+    achieved = nbytes / steps / (ms / 1e3) / 1e9
+    pk.pa_pool_destroy(pool)
+    return {"workload": "64 sequences, OPT-13B layer 40x128, block 16, context uniform in "
+                        "[128, 2048], pool 1.25x the blocks needed, shuffled free queue",
+            "bound": "hbm", "launches": steps, "mean_ctx": tokens / steps / S,
+            "us_per_launch": ms * 1e3, "algorithmic_bytes_per_launch": nbytes / steps,
+            "achieved": achieved, "peak": peak, "peak_kind": f"{kind} hbm_gbs", "unit": "GB/s",
+            "frac": achieved / peak, "seq_tokens_per_s": tokens / steps / (ms / 1e3),
+            "l2": "K/V working set %.2f GB per launch >> 129 MB L2, no flush" % (nbytes / steps / 1e9)}
+
+
+def parallel_sampling_stats(dev) -> dict:
+    """16 prompts (lognormal, median 160, cap 1024) x 4 samples forked from
+    them, 64 decode steps: copy-on-write of each shared partial last block,
+    slot write, attention.  Per step the GPU time of its kernels (copies,
+    slot write, attention) from CUDA events.  Logical bytes count a shared
+    block once per sequence that reads it; unique bytes once.  The unique
+    working set is a few hundred MB at most and the samples re-read the
+    shared prompt blocks from L2, so the GB/s are not an HBM roofline."""
+    import torch
+
+    import paged_kv_cache_106_gb300 as pk
+    import workloads as wl
+    from paged_kv_cache_106_gb300.step import DecodeStepRunner
+
+    res = None
+    for episode in range(2):              # the first one warms up; the second is timed
+        w = wl.parallel_sampling()
+        H, D, B = w.num_heads, w.head_dim, w.block_size
+        desc, pool = _pool_setup(pk, w)
+        ids = list(range(len(w.prompt_lens)))
+        nxt = len(ids)
+        for root, extra in w.forks:
+            for _ in range(extra):
+                pk.pa_seq_fork(pool, root, nxt)
+                ids.append(nxt)
+                nxt += 1
+        S = len(ids)
+        max_blocks = -(-(max(w.prompt_lens) + w.decode_steps + 1) // B)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed)
+        kc = torch.empty((w.num_blocks, H, B, D), dtype=torch.float16, device=dev).normal_(generator=gen)
+        vc = torch.empty_like(kc).normal_(generator=gen)
+        q, k_new, v_new = (torch.randn((S, H, D), dtype=torch.float16, device=dev, generator=gen)
+                           for _ in range(3))
+        out = torch.empty_like(q)
+        stream = torch.cuda.Stream(device=dev)
+        runner = DecodeStepRunner(pool, desc, ids, max_blocks, device=dev, stream=stream)
+        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+               for _ in range(w.decode_steps)]
+        logical, unique, copies, tokens = 0, 0, 0, 0
+        with torch.cuda.stream(stream):
+            for i in range(w.decode_steps):
+                runner.prepare()
+                ctx = runner.ctx_host.astype(np.int64)
+                tables = runner._views(runner.host[(runner.i - 1) & 1])[2]
+                evs[i][0].record(stream)
+                runner.copy_blocks([kc], [vc])
+                runner.write_kv(k_new, v_new, kc, vc)
+                evs[i][1].record(stream)
+                runner.attention(out, q, kc, vc, w.scale)
+                evs[i][2].record(stream)
+                copies += runner.n_copies
+                tokens += int(ctx.sum())
+                logical += int(ctx.sum()) * H * D * 4
+                blocks = np.unique(tables[tables >= 0])
+                unique += len(blocks) * B * H * D * 4      # whole blocks, an upper bound
+        torch.cuda.synchronize()
+        assert runner.status.item() == 0, runner.status.item()
+        n = w.decode_steps
+        step_ms = sum(a.elapsed_time(c) for a, _, c in evs) / n
+        attn_ms = sum(b.elapsed_time(c) for _, b, c in evs) / n
+        res = {"workload": "16 prompts lognormal (median 160, cap 1024) x 4 samples sharing the "
+                           "prompt blocks, 64 decode steps, OPT-13B layer 40x128, block 16",
+               "sequences": S, "steps": n, "cow_copies": copies,
+               "us_per_step": step_ms * 1e3, "attention_us_per_step": attn_ms * 1e3,
+               "seq_tokens_per_s": tokens / n / (attn_ms / 1e3),
+               "logical_GB/s": logical / n / (attn_ms / 1e3) / 1e9,
+               "unique_GB/s": unique / n / (attn_ms / 1e3) / 1e9,
+               "unique_bytes_per_step": unique / n,
+               "l2_resident": True,
+               "note": "GPU time of the step's kernels (copy-on-write copies, slot write, "
+                       "attention); logical bytes count shared blocks once per reading "
+                       "sequence, unique bytes once (whole blocks); the samples' re-reads of "
+                       "shared blocks hit L2, so this is not an HBM roofline"}
+        pk.pa_pool_destroy(pool)
+    return res
+
+
 def run_beam_churn(args):
     """Beam-search churn: 64 requests x 4 beams (OPT-13B layer shapes), every
     step = prune (fork repeated survivors, free the rest), host block
@@ -781,74 +942,138 @@ def _prefill_cpu_baseline(seconds: float):
                       f"{dt:.1f} s, fp64 C + OpenMP"}
 
 
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return (float(json.load(f)["bf16_tflops"]),
+                    "measured bf16 burst (MEASURED_PEAKS.json; fp16 has the same nominal rate)")
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+class PrefillBatch:
+    """The prompt phase of the mixed batch on one GPU: 256 whole prompts
+    admitted through the block manager, their new K/V, queries and output."""
+
+    def __init__(self, dev, seed: int = 112, prompts: int = 0):
+        import torch
+
+        import paged_kv_cache_106_gb300 as pk
+        import workloads as wl
+
+        self.pk = pk
+        w = wl.prefill_b256(seed=seed)
+        if prompts:
+            w.prompt_lens = w.prompt_lens[:prompts]
+        self.w = w
+        H, D, B = w.num_heads, w.head_dim, w.block_size
+        lens = np.array(w.prompt_lens, np.int64)
+        self.lens = lens
+        self.desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
+        self.pool = pk.pa_pool_create(self.desc)
+        slots = np.concatenate([pk.pa_seq_add(self.pool, i, int(n)) for i, n in enumerate(lens)])
+        mb = -(-int(lens.max()) // B)
+        tables, ctx = pk.pa_get_block_tables(self.pool, list(range(len(lens))), mb)
+        self.T = T = int(lens.sum())
+        qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(w.seed)
+        self.kc = torch.empty((w.num_blocks, H, B, D), dtype=torch.float16, device=dev).normal_(generator=gen)
+        self.vc = torch.empty_like(self.kc).normal_(generator=gen)
+        self.q = torch.randn((T, H, D), dtype=torch.float16, device=dev, generator=gen)
+        self.k_new, self.v_new = torch.randn_like(self.q), torch.randn_like(self.q)
+        self.out = torch.empty_like(self.q)
+        self.d_slots = torch.from_numpy(slots).to(dev)
+        self.d_tables, self.d_ctx, self.d_qs = (torch.from_numpy(x).to(dev) for x in (tables, ctx, qs))
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.mql = int(lens.max())
+        self.flops = prefill_flops(ctx.tolist(), lens.tolist(), H, D)
+        # bytes the attention must move at least: K and V of every prompt
+        # token read, q read, o written, tables and lengths read
+        self.unique_bytes = 4 * T * H * D * 2 + int(((lens + B - 1) // B).sum()) * 4 + 12 * len(lens)
+
+    def write(self, k=None, v=None):
+        self.pk.pa_write_kv(self.k_new if k is None else k, self.v_new if v is None else v,
+                            self.d_slots, self.kc, self.vc, self.desc, status=self.status,
+                            stream=self.stream)
+
+    def attend(self, q=None, out=None):
+        self.pk.pa_prefill_attention(self.out if out is None else out, self.q if q is None else q,
+                                     self.kc, self.vc, self.d_tables, self.d_ctx, self.d_qs,
+                                     self.w.scale, self.desc, max_q_len=self.mql,
+                                     status=self.status, stream=self.stream)
+
+    def time_steps(self, steps: int, warmup: int):
+        """Slot write + attention per step; returns (elapsed s, attention ms per
+        launch, slot-write ms per launch) from CUDA events on the stream."""
+        import torch
+
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                self.write()
+                self.attend()
+        torch.cuda.synchronize()
+        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(self.stream)
+        for i in range(steps):
+            evs[i][2].record(self.stream)
+            self.write()
+            evs[i][0].record(self.stream)
+            self.attend()
+            evs[i][1].record(self.stream)
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        assert self.status.item() == 0, self.status.item()
+        attn_ms = sum(a.elapsed_time(b) for a, b, _ in evs) / steps
+        wkv_ms = sum(c.elapsed_time(a) for a, _, c in evs) / steps
+        return t0.elapsed_time(t1) / 1e3, attn_ms, wkv_ms
+
+    def roofline(self, attn_ms: float) -> dict:
+        """The binding roof of the attention call: the larger of the HBM time
+        of its unique bytes and the tensor time of its causal flops."""
+        hbm, hbm_kind = _peaks()
+        tf, tf_kind = _tensor_peak()
+        t_hbm = self.unique_bytes / (hbm * 1e9) * 1e3
+        t_tc = self.flops / (tf * 1e12) * 1e3
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        if bound == "hbm":
+            achieved, peak, unit = self.unique_bytes / (attn_ms / 1e3) / 1e9, hbm, "GB/s"
+            kind = f"{hbm_kind} hbm_gbs"
+        else:
+            achieved, peak, unit = self.flops / (attn_ms / 1e3) / 1e12, tf, "TFLOP/s"
+            kind = tf_kind
+        return {"bound": bound, "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": unit,
+                "frac": achieved / peak, "ms_per_launch": attn_ms,
+                "unique_bytes_per_launch": self.unique_bytes, "hbm_floor_ms": t_hbm,
+                "algorithmic_flops_per_launch": self.flops, "tensor_floor_ms": t_tc,
+                "tflops": self.flops / (attn_ms / 1e3) / 1e12,
+                "GB/s": self.unique_bytes / (attn_ms / 1e3) / 1e9}
+
+    def close(self):
+        self.pk.pa_pool_destroy(self.pool)
+
+
 def run_prefill(args):
     """Prompt phase of the mixed batch: every step writes the K/V of all 256
     prompts into the pool (pa_write_kv, one slot per prompt token) and runs
     causal paged prefill attention over them (one OPT-13B layer)."""
     import torch
 
-    import paged_kv_cache_106_gb300 as pk
-    import workloads as wl
-
     ws, rank, local = _dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = wl.prefill_b256(seed=112 + rank)
-    if args.prompts:
-        w.prompt_lens = w.prompt_lens[:args.prompts]
-    H, D, B = w.num_heads, w.head_dim, w.block_size
-    lens = np.array(w.prompt_lens, np.int64)
-    desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
-    pool = pk.pa_pool_create(desc)
-    slots = np.concatenate([pk.pa_seq_add(pool, i, int(n)) for i, n in enumerate(lens)])
-    mb = -(-int(lens.max()) // B)
-    tables, ctx = pk.pa_get_block_tables(pool, list(range(len(lens))), mb)
-    T = int(lens.sum())
-    qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(w.seed)
-    kc = torch.empty((w.num_blocks, H, B, D), dtype=torch.float16, device=dev).normal_(generator=gen)
-    vc = torch.empty_like(kc).normal_(generator=gen)
-    q = torch.randn((T, H, D), dtype=torch.float16, device=dev, generator=gen)
-    k_new, v_new = torch.randn_like(q), torch.randn_like(q)
-    out = torch.empty_like(q)
-    d_slots = torch.from_numpy(slots).to(dev)
-    d_tables, d_ctx, d_qs = (torch.from_numpy(x).to(dev) for x in (tables, ctx, qs))
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    mql = int(lens.max())
-    flops = prefill_flops(ctx.tolist(), lens.tolist(), H, D)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[2].record(stream)
-        pk.pa_write_kv(k_new, v_new, d_slots, kc, vc, desc, status=status, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        pk.pa_prefill_attention(out, q, kc, vc, d_tables, d_ctx, d_qs, w.scale, desc,
-                                max_q_len=mql, status=status, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            step()
-    torch.cuda.synchronize()
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    pb = PrefillBatch(dev, seed=112 + rank, prompts=args.prompts)
+    w, lens, T = pb.w, pb.lens, pb.T
+    H, D = w.num_heads, w.head_dim
+    q, k_new, v_new, out = pb.q, pb.k_new, pb.v_new, pb.out
+    stream, status = pb.stream, pb.status
     clocks = ClockSampler(local)
     clocks.start()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
+    el, attn_ms, wkv_ms = pb.time_steps(args.steps, args.warmup)
     clk = clocks.stop()
-    assert status.item() == 0, status.item()
-    el = t0.elapsed_time(t1) / 1e3
-    attn_s = sum(a.elapsed_time(b) for a, b, _ in evs) / len(evs) / 1e3
-    wkv_s = sum(c.elapsed_time(a) for a, _, c in evs) / len(evs) / 1e3
     # end to end through the same calls: the step's new K/V and queries come
     # from pinned host memory, the output goes back to it
     h_k, h_v, h_q = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
@@ -880,9 +1105,8 @@ def run_prefill(args):
         stream.wait_event(ev["in"][s])
         if used[s]:
             stream.wait_event(ev["out"][s])    # step i - 2's output has left this set
-        pk.pa_write_kv(kn, vn, d_slots, kc, vc, desc, status=status, stream=stream)
-        pk.pa_prefill_attention(oo, qq, kc, vc, d_tables, d_ctx, d_qs, w.scale, desc,
-                                max_q_len=mql, status=status, stream=stream)
+        pb.write(kn, vn)
+        pb.attend(qq, oo)
         ev["comp"][s].record(stream)
         s_out.wait_event(ev["comp"][s])
         with torch.cuda.stream(s_out):
@@ -908,18 +1132,13 @@ def run_prefill(args):
     (tok_all, e2e_tok), (el_max, e2e_max) = reduce_across_ranks(
         [T * args.steps, T * e2e_steps], [el, e2e_s * e2e_steps], dev)
     if rank == 0:
-        peak = None
-        try:
-            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-                peak, kind = float(json.load(f)["bf16_tflops"]), "measured bf16 burst (fp16 nominal rate = bf16)"
-        except Exception:
-            peak, kind = 1900.0, "fallback"
-        achieved = flops / attn_s / 1e12
+        roof = pb.roofline(attn_ms)
         traffic = _kernel_traffic(os.path.join(ROOT, "paged_kv_cache_106_gb300", "csrc",
                                                "prefill_attention.cu"),
                                   "prefill_attention_traffic.json")
-        if args.prompts:
-            traffic = None   # the committed capture is of the full batch
+        roof["kernel"] = "paged_prefill_tc<128> (pa_prefill_attention)"
+        roof["traffic"] = None if traffic is None else \
+            traffic["dram_bytes_per_unique_byte"] * pb.unique_bytes
         line = {
             "metric": PREFILL_METRIC, "value": tok_all / el_max, "unit": PREFILL_UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -930,13 +1149,8 @@ def run_prefill(args):
                        "prompt_tokens": T, "pool_blocks": w.num_blocks,
                        "l2": "K/V written and read back per step ~1.7 GB >> 129 MB L2, no flush"},
             "gpu_launches": 2 * args.steps,
-            "roofline": {"bound": "tensor", "kernel": "paged_prefill_tc<128> (pa_prefill_attention)",
-                         "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": "TFLOP/s",
-                         "frac": achieved / peak,
-                         "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
-                         "algorithmic_flops_per_launch": flops,
-                         "attn_ms_per_launch": attn_s * 1e3},
-            "kernels": {"pa_write_kv": {"us_per_launch": wkv_s * 1e6,
+            "roofline": roof,
+            "kernels": {"pa_write_kv": {"us_per_launch": wkv_ms * 1e3,
                                         "tokens": T, "algorithmic_bytes": T * H * D * 2 * 4}},
             "e2e": {"value": e2e_tok / e2e_max, "unit": PREFILL_UNIT,
                     "h2d_bytes_per_step": 3 * T * H * D * 2, "d2h_bytes_per_step": T * H * D * 2,
@@ -947,7 +1161,7 @@ def run_prefill(args):
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = _prefill_cpu_baseline(args.cpu_seconds)
         print(json.dumps(line), flush=True)
-    pk.pa_pool_destroy(pool)
+    pb.close()
 
 
 def _oracle_sample(n_seqs):
@@ -1137,6 +1351,9 @@ def main():
     ap.add_argument("--batch", type=int, default=256)
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="default workload: skip the 64-sequence, parallel-sampling and "
+                         "prefill measurements that follow the timed region")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)

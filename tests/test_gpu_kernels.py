@@ -166,9 +166,11 @@ def test_attention_bad_block_id_is_reported_not_dereferenced():
     assert st.item() == pk.PA_ERR_BAD_BLOCK
 
 
-def test_write_kv_is_bit_exact():
-    rng = np.random.default_rng(17)
-    NB, H, B, D, T = 37, 40, 16, 128, 300
+@pytest.mark.parametrize("T,H,NB", [(300, 40, 37), (5000, 8, 400)])
+def test_write_kv_is_bit_exact(T, H, NB):
+    # 300 tokens: a thread per vector; 5000: the token-major grid-stride launch
+    rng = np.random.default_rng(17 + T)
+    B, D = 16, 128
     kc = _f16(rng, (NB, H, B, D))
     vc = _f16(rng, (NB, H, B, D))
     slots = rng.choice(NB * B, size=T, replace=False).astype(np.int64)
