@@ -158,7 +158,10 @@ def _pool_setup(pk, w):
 
 
 class SteadyBatch:
-    """Host side of the continuous batch: replaces finished sequences."""
+    """Host side of the continuous batch: replaces finished sequences.
+    Newcomers' (prompt, target) lengths are seeded inputs, drawn in blocks."""
+
+    DRAW_BLOCK = 4096
 
     def __init__(self, pk, pool, w, rng):
         self.pk, self.pool, self.rng = pk, pool, rng
@@ -166,12 +169,21 @@ class SteadyBatch:
         self.target = np.array(w.targets, np.int64)
         self.next_id = len(w.prompt_lens)
         self.replaced = 0
+        self._draws, self._next_draw = None, self.DRAW_BLOCK
+
+    def _draw(self):
+        if self._next_draw == self.DRAW_BLOCK:
+            from workloads import draw_mixed_sequences
+            p, t = draw_mixed_sequences(self.rng, self.DRAW_BLOCK)
+            self._draws, self._next_draw = (p.tolist(), t.tolist()), 0
+        i = self._next_draw
+        self._next_draw += 1
+        return self._draws[0][i], self._draws[1][i]
 
     def admit(self, ids):
-        from workloads import draw_mixed_sequence
-        for i in np.nonzero(self.held >= self.target)[0]:
+        for i in np.flatnonzero(self.held >= self.target).tolist():
             self.pk.pa_seq_free(self.pool, int(ids[i]))
-            prompt, target = draw_mixed_sequence(self.rng)
+            prompt, target = self._draw()
             self.pk.pa_seq_add(self.pool, self.next_id, prompt, want_slots=False)
             ids[i] = self.next_id
             self.next_id += 1
@@ -231,7 +243,7 @@ def run_ours(args):
         h_admit = time.perf_counter() - h0
         n_cp = runner.prepare()
         if stats is not None:
-            host_s.append(h_admit + runner.host_seconds)
+            host_s.append((h_admit, runner.host_seconds))
         batch.appended()
         ctx = runner.ctx_host.astype(np.int64)
         if dump is not None:
@@ -288,6 +300,16 @@ def run_ours(args):
     attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
     write_ms = [e[2].elapsed_time(e[0]) for e in evs]
     copy_stats = time_copy_blocks(pk, pool, desc, w, kc, vc, stream) if rank == 0 else None
+    # the step's slot write alone, 50 launches back to back between two events
+    # (inside the step loop each launch also carries its own events)
+    with torch.cuda.stream(stream):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(50):
+            runner.write_kv(k_new, v_new, kc, vc)
+        b.record(stream)
+    torch.cuda.synchronize()
+    write_b2b_us = a.elapsed_time(b) * 1e3 / 50
     swap_stats = time_swap_blocks(pk, desc, w, kc, vc, stream) if rank == 0 else None
     assert runner.status.item() == 0, f"device status {runner.status.item()}"
 
@@ -450,6 +472,7 @@ def run_ours(args):
             "kernels": {
                 "pa_write_kv": {
                     "us_per_launch": 1e3 * sum(write_ms) / len(write_ms),
+                    "us_per_launch_back_to_back": write_b2b_us,
                     "algorithmic_bytes": 2 * 2 * S * H * D * 2 + 8 * S,
                     "GB/s": (2 * 2 * S * H * D * 2 + 8 * S) / (sum(write_ms) / len(write_ms) / 1e3) / 1e9,
                     "note": "new K/V of the batch read and scattered to their slots (timed in the step loop)",
@@ -458,7 +481,9 @@ def run_ours(args):
                 "pa_copy_blocks": copy_stats,
                 "pa_swap_blocks": swap_stats,
                 "host_block_manager": {
-                    "us_per_step": 1e6 * sum(host_s) / len(host_s),
+                    "us_per_step": 1e6 * sum(a + b for a, b in host_s) / len(host_s),
+                    "admission_us_per_step": 1e6 * sum(a for a, _ in host_s) / len(host_s),
+                    "step_prepare_us_per_step": 1e6 * sum(b for _, b in host_s) / len(host_s),
                     "note": "host wall clock per step: free/admit finished sequences, then "
                             "pa_decode_step_prepare (one token per sequence, tables and lengths "
                             "into the pinned staging buffer); waits on the GPU excluded",

@@ -328,6 +328,17 @@ def pa_decode_step_prepare(pool, seq_ids, max_blocks: int, slot_out=None, ctx_ou
     return slots, ctx, tables, copies[: nc.value]
 
 
+def pa_decode_step_prepare_into(pool, n_seqs: int, ids_addr: int, max_blocks: int,
+                                slots_addr: int, ctx_addr: int, tables_addr: int,
+                                copies_addr: int, copies_cap: int, n_copies) -> int:
+    """pa_decode_step_prepare on raw host addresses (a serving loop's
+    preallocated staging buffers); ``n_copies`` is a ctypes.c_int32 that
+    receives the copy count.  Returns it."""
+    _check(_lib.pa_decode_step_prepare(pool, n_seqs, ids_addr, max_blocks, slots_addr, ctx_addr,
+                                       tables_addr, copies_addr, copies_cap, ctypes.byref(n_copies)))
+    return n_copies.value
+
+
 def pa_seq_info(pool, seq_id: int):
     nt, nb = ctypes.c_int32(), ctypes.c_int32()
     _check(_lib.pa_seq_info(pool, int(seq_id), ctypes.byref(nt), ctypes.byref(nb)))

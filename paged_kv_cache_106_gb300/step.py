@@ -18,12 +18,13 @@ calls and owns the staging buffers; the work runs in libpagedkv.so.
 """
 from __future__ import annotations
 
+import ctypes
 import time
 
 import numpy as np
 import torch
 
-from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_prepare,
+from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_prepare_into,
                pa_decode_workspace_bytes, pa_write_kv)
 
 
@@ -49,6 +50,9 @@ class DecodeStepRunner:
         self.off_cp = self.off_tab + _align(4 * S * MB)
         self.nbytes = self.off_cp + _align(8 * S)
         self.host = [torch.empty(self.nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        self.host_addr = [h.data_ptr() for h in self.host]
+        self.host_ctx = [self._views(h)[1] for h in self.host]
+        self._n_copies = ctypes.c_int32(0)
         self.events = [None, None]
         self.dev = torch.empty(self.nbytes, dtype=torch.uint8, device=self.device)
         self.d_slots = self.dev[self.off_slots:self.off_slots + 8 * S].view(torch.int64)
@@ -80,12 +84,15 @@ class DecodeStepRunner:
         if self.events[k] is not None:
             self.events[k].synchronize()     # staging buffer k no longer in flight
         t0 = time.perf_counter()
-        slots, ctx, tables, copies = self._views(self.host[k])
-        _, _, _, cp = pa_decode_step_prepare(self.pool, self.ids, self.max_blocks, slot_out=slots,
-                                             ctx_out=ctx, tables_out=tables, copies_out=copies,
-                                             copies_cap=self.S)
+        if self.ids.dtype != np.int32 or not self.ids.flags.c_contiguous or \
+                self.ids.shape[0] != self.S:
+            raise ValueError("ids must be a contiguous int32 array of the batch size")
+        base = self.host_addr[k]
+        n_cp = pa_decode_step_prepare_into(
+            self.pool, self.S, self.ids.ctypes.data, self.max_blocks, base + self.off_slots,
+            base + self.off_ctx, base + self.off_tab, base + self.off_cp, self.S, self._n_copies)
         self.host_seconds = time.perf_counter() - t0   # block manager work of this step
-        self._pending = (k, int(cp.shape[0]), ctx)
+        self._pending = (k, n_cp, self.host_ctx[k])
 
     def upload(self) -> int:
         """Enqueue the prepared step's metadata upload on the stream."""

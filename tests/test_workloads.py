@@ -57,10 +57,13 @@ def test_steady_state_batch_does_not_drift():
     held = np.array(w.prompt_lens, np.int64)
     target = np.array(w.targets, np.int64)
     rng = np.random.default_rng(3)
+    prompts, targets = wl.draw_mixed_sequences(rng, 20000)
+    nxt = 0
     means = []
     for _ in range(1500):
         for i in np.nonzero(held >= target)[0]:
-            held[i], target[i] = wl.draw_mixed_sequence(rng)
+            held[i], target[i] = prompts[nxt], targets[nxt]
+            nxt += 1
         held += 1
         means.append(held.mean())
     first, last = np.mean(means[:300]), np.mean(means[-300:])

@@ -180,11 +180,12 @@ def mixed_b256(seed: int = 109, batch: int = 256, growth_steps: int = 64,
     )
 
 
-def draw_mixed_sequence(rng: np.random.Generator):
-    """A newly admitted sequence of the mixed batch: (prompt length, target length)."""
-    prompt = int(_lognormal_lengths(rng, 1, 200, 1536)[0])
-    output = int(_lognormal_lengths(rng, 1, 250, 1 << 30)[0])
-    return prompt, min(prompt + output, CTX_CAP)
+def draw_mixed_sequences(rng: np.random.Generator, n: int):
+    """``n`` newly admitted sequences of the mixed batch at once:
+    (prompt lengths, target lengths), int64 arrays."""
+    prompt = _lognormal_lengths(rng, n, 200, 1536)
+    output = _lognormal_lengths(rng, n, 250, 1 << 30)
+    return prompt, np.minimum(prompt + output, CTX_CAP)
 
 
 def full_40l(pool_bytes: int, seed: int = 110, beam: bool = False,
