@@ -74,8 +74,9 @@ def _code_sha256(path: str) -> str:
 
 
 def _kernel_traffic(kernel_src: str, name: str = "decode_attention_traffic.json"):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current code of the kernel (else None)."""
+    """The committed ncu traffic summary of a kernel (DRAM bytes of one
+    captured launch of a small case over that launch's algorithmic bytes), if
+    it was taken on the current code of the kernel (else None)."""
     p = os.path.join(ROOT, "profiles", name)
     try:
         with open(p) as f:
@@ -461,7 +462,11 @@ def run_ours(args):
                 "unit": "GB/s",
                 "frac": achieved / peak,
                 "frac_of_nominal_7900": achieved / 7900.0,
-                "traffic": None if traffic is None else traffic["dram_bytes_per_launch"],
+                # DRAM bytes of the small-case capture per algorithmic byte, times
+                # this launch's algorithmic bytes
+                "traffic": None if traffic is None else
+                traffic["traffic_over_algorithmic"] * stats["attn_bytes"] / args.steps,
+                "traffic_from": None if traffic is None else traffic["capture"],
                 "traffic_over_algorithmic": None if traffic is None
                 else traffic["traffic_over_algorithmic"],
                 "algorithmic_bytes_per_launch": stats["attn_bytes"] / args.steps,
@@ -1162,8 +1167,9 @@ def run_prefill(args):
                                                "prefill_attention.cu"),
                                   "prefill_attention_traffic.json")
         roof["kernel"] = "paged_prefill_tc<128> (pa_prefill_attention)"
-        roof["traffic"] = None if traffic is None else \
-            traffic["dram_bytes_per_unique_byte"] * pb.unique_bytes
+        roof["traffic"] = None if traffic is None or args.prompts else \
+            traffic["traffic_over_algorithmic"] * pb.unique_bytes
+        roof["traffic_from"] = None if traffic is None else traffic["capture"]
         line = {
             "metric": PREFILL_METRIC, "value": tok_all / el_max, "unit": PREFILL_UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
