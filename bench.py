@@ -195,6 +195,42 @@ class SteadyBatch:
         self.held += 1
 
 
+def other_rows(args) -> dict:
+    """Short runs of the other measured rows for the default bench line:
+    the 40-layer pool-filling step, beam-search churn and prefix caching,
+    each summarised from its own mode's line."""
+    import copy
+
+    import torch
+
+    out = {}
+    a = copy.copy(args)
+    a.warmup, a.steps, a.beam, a.prompts = 3, 10, False, 0
+    f = run_full40(a, quiet=True)
+    out["full_40l_step"] = {
+        "workload": f["config"]["workload"], "sequences": f["config"]["sequences"],
+        "pool_bytes": f["config"]["pool_bytes"], "steps": a.steps,
+        "seq_tokens_per_s": f["value"], "ms_per_step": f["ms_per_step"],
+        "attention_GB/s": f["roofline"]["achieved"], "frac": f["roofline"]["frac"],
+        "peak": f["roofline"]["peak"], "bound": "hbm",
+        "algorithmic_bytes_per_step": f["roofline"]["algorithmic_bytes_per_step"]}
+    torch.cuda.empty_cache()
+    a.warmup, a.steps = 3, 20
+    b = run_beam_churn(a, quiet=True)
+    out["beam_churn"] = {"workload": b["config"]["workload"], "steps": a.steps,
+                         "ms_per_step": b["ms_per_step"], "seq_tokens_per_s": b["value"],
+                         "per_step": b["per_step"], "host_us_per_step": b["host_us_per_step"],
+                         "logical_attention_GB/s": b["logical_attention_GB/s"]}
+    torch.cuda.empty_cache()
+    a.warmup, a.steps = 2, 5
+    c = run_prefix_cache(a, quiet=True)
+    out["prefix_cache"] = {"workload": c["config"]["workload"], "steps": a.steps,
+                           "speedup": c["speedup"], "cached": c["cached"],
+                           "uncached": c["uncached"]}
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -420,6 +456,9 @@ def run_ours(args):
                    "slot_write_us_for_the_prompts": pf_wkv_ms * 1e3})
         extra["pa_prefill_attention"] = pf
         pb.close()
+        del pb
+        torch.cuda.empty_cache()
+        extra.update(other_rows(args))
 
     if rank == 0:
         peak, peak_kind = _peaks()
@@ -548,7 +587,7 @@ def time_copy_blocks(pk, pool, desc, w, kc, vc, stream, n_pairs=256, reps=50):
             "note": "blocks of live sequences copied into free blocks, K and V (read + write)"}
 
 
-def run_full40(args):
+def run_full40(args, quiet: bool = False):
     """The 40-layer decode step over a pool-filling cache (one GPU).
 
     The K/V pool takes min(120 GB, half the free device memory); sequences
@@ -634,7 +673,7 @@ def run_full40(args):
     attn_s = sum(a.elapsed_time(b) for layer in evs for a, b in layer) / 1e3
     peak, peak_kind = _peaks()
     achieved = stats["attn_bytes"] / attn_s / 1e9
-    print(json.dumps({
+    line = {
         "metric": METRIC, "value": stats["tokens"] / elapsed, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -653,8 +692,11 @@ def run_full40(args):
                      "note": "K/V counted once per referencing sequence (shared blocks once "
                              "per beam): logical bytes"},
         "clocks": clocks,
-    }), flush=True)
+    }
+    if not quiet:
+        print(json.dumps(line), flush=True)
     pk.pa_pool_destroy(pool)
+    return line
 
 
 def time_swap_blocks(pk, desc, w, kc, vc, stream, n_pairs=256, reps=20):
@@ -828,7 +870,7 @@ def parallel_sampling_stats(dev) -> dict:
     return res
 
 
-def run_beam_churn(args):
+def run_beam_churn(args, quiet: bool = False):
     """Beam-search churn: 64 requests x 4 beams (OPT-13B layer shapes), every
     step = prune (fork repeated survivors, free the rest), host block
     manager, copy-on-write copies, slot write, decode attention."""
@@ -904,7 +946,7 @@ def run_beam_churn(args):
     torch.cuda.synchronize()
     assert runner.status.item() == 0
     el = t0.elapsed_time(t1) / 1e3
-    print(json.dumps({
+    line = {
         "metric": METRIC, "value": stats["tokens"] / el, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "data": "synthetic",
@@ -916,8 +958,11 @@ def run_beam_churn(args):
         "logical_attention_GB/s": stats["bytes"] / el / 1e9,
         "note": "logical bytes count shared blocks once per beam; host time = pruning + "
                 "block manager + Python launch path (the wait on the GPU excluded)",
-    }), flush=True)
+    }
+    if not quiet:
+        print(json.dumps(line), flush=True)
     pk.pa_pool_destroy(pool)
+    return line
 
 
 PREFILL_METRIC = "paged prefill-attn prompt-tokens/s (1 GB300) + achieved TFLOP/s"
@@ -1268,7 +1313,7 @@ def run_reference(args):
     }), flush=True)
 
 
-def run_prefix_cache(args):
+def run_prefix_cache(args, quiet: bool = False):
     """Prefix caching: 256 prompts = one shared 512-token system prompt + a
     suffix of their own (lognormal, median 200, cap 1024), OPT-13B layer
     shapes.  One step admits every prompt through the hash-chained block
@@ -1358,7 +1403,7 @@ def run_prefix_cache(args):
                      "host_us_per_admission": admit_s / args.steps / n_p * 1e6}
         pk.pa_pool_destroy(pool)
     c, u = res["cached"], res["uncached"]
-    print(json.dumps({
+    line = {
         "metric": "prefix-cached prefill prompt-tokens/s (1 GB300)", "value": c["prompt_tokens_per_s"],
         "unit": "prompt-tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": c["gpu_ms_per_step"], "higher_is_better": True, "data": "synthetic",
@@ -1370,7 +1415,10 @@ def run_prefix_cache(args):
         "cached": c, "uncached": u, "speedup": c["prompt_tokens_per_s"] / u["prompt_tokens_per_s"],
         "timing": "GPU: CUDA events around the slot write + prefill of a step; host: wall clock of "
                   "the admissions (Python calls into the C block manager) and the table read",
-    }), flush=True)
+    }
+    if not quiet:
+        print(json.dumps(line), flush=True)
+    return line
 
 
 def main():
@@ -1383,8 +1431,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="default workload: skip the 64-sequence, parallel-sampling and "
-                         "prefill measurements that follow the timed region")
+                    help="default workload: skip the other rows measured after the timed "
+                         "region (64 sequences, parallel sampling, prefill, 40 layers, beam "
+                         "churn, prefix cache)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-seqs", type=int, default=32)
     ap.add_argument("--ref-seqs", type=int, default=16)
