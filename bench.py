@@ -903,15 +903,21 @@ def run_beam_churn(args, quiet: bool = False):
     mb = -(-(max(churn.prompt_lens) + total) // B) + 1
     runner = DecodeStepRunner(pool, desc, bg.ids(), mb, device=dev, stream=stream)
     rng = np.random.default_rng(churn.seed + 1)
-    # the seeded survivor draws are inputs: drawn before any timing
-    draws = iter([churn.survivors(rng) for _ in range(total)])
+    # the seeded survivor draws are inputs: drawn before any timing, as counts
+    # of each beam among its group's survivors
+    def counts_of(surv):
+        c = np.zeros((churn.groups, churn.width), np.int32)
+        for g, keep in enumerate(surv):
+            c[g] = np.bincount(keep, minlength=churn.width)
+        return c
+    draws = iter([counts_of(churn.survivors(rng)) for _ in range(total)])
     host, stats = [], {"copies": 0, "forks": 0, "frees": 0, "tokens": 0, "bytes": 0}
 
     split = {"prepare_wait": 0.0, "block_manager": 0.0, "launches": 0.0, "prune": 0.0}
 
     def step(record):
         h0 = time.perf_counter()
-        runner.ids = np.array(bg.ids(), np.int32)
+        runner.ids = bg.id_array()
         runner.prepare()
         h1 = time.perf_counter()
         ctx = runner.ctx_host.astype(np.int64)

@@ -176,6 +176,22 @@ int pa_seq_free(pa_pool *pool, int32_t seq_id);
 int pa_seq_fork_batch(pa_pool *pool, int32_t n, const int32_t *parents, const int32_t *children);
 int pa_seq_free_batch(pa_pool *pool, int32_t n, const int32_t *seq_ids);
 
+/* One pruning step of beam search for n_groups groups of `width` beams
+ * ([notes] §3.4.2: beams fork where a candidate is kept several times and
+ * pruned beams drop their references; [review] §4.4 (2)).  beams (host,
+ * n_groups x width int32, in/out) holds each group's beam sequence ids;
+ * counts (host, n_groups x width int32) how many of the group's `width`
+ * survivors each beam is (each row sums to width).  Per group, in order:
+ * every surviving beam keeps its id and is forked count - 1 times into new
+ * ids *next_id, *next_id + 1, ... (pa_seq_fork), placed right after it;
+ * beams with count 0 are freed, in beam order (pa_seq_free).  The group's
+ * new ids are written back into its row of beams and *next_id advances.
+ * Everything is checked before anything changes.  Errors: PA_ERR_NO_SEQ (a
+ * beam does not exist or a new id is in use), PA_ERR_INVALID_ARG (a row
+ * that does not sum to width, a beam listed twice, a negative count). */
+int pa_beam_prune(pa_pool *pool, int32_t n_groups, int32_t width, int32_t *beams,
+                  const int32_t *counts, int32_t *next_id);
+
 /* append, for a batch: one new token for each of seq_ids[0..n_seqs), handled
  * in the order given ([review] §4.3 steps 1-2; [tutorial] Fig. 3, Fig. 6):
  *   - no block yet, or the last block is full (shared or not): take a new

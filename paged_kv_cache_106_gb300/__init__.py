@@ -82,6 +82,7 @@ def _load():
         "pa_seq_fork_batch": (i32, [vp, i32, vp, vp]),
         "pa_seq_free_batch": (i32, [vp, i32, vp]),
         "pa_seq_free": (i32, [vp, i32]),
+        "pa_beam_prune": (i32, [vp, i32, i32, vp, vp, P(i32)]),
         "pa_alloc_slots": (i32, [vp, i32, vp, vp, vp, i32, P(i32)]),
         "pa_alloc_slots_n": (i32, [vp, i32, vp, vp, vp, vp, i32, P(i32)]),
         "pa_get_block_tables": (i32, [vp, i32, vp, i32, vp, vp]),
@@ -263,6 +264,20 @@ def pa_seq_fork_batch(pool, parents, children) -> None:
 def pa_seq_free_batch(pool, seq_ids) -> None:
     ids = _host_i32(seq_ids)
     _check(_lib.pa_seq_free_batch(pool, ids.shape[0], ids.ctypes.data))
+
+
+def pa_beam_prune(pool, beams, counts, next_id: int) -> int:
+    """beams: int32 [groups, width] (contiguous, updated in place); counts:
+    int32 [groups, width], each row summing to width.  Returns the new next_id."""
+    if beams.dtype != np.int32 or not beams.flags.c_contiguous or beams.ndim != 2:
+        raise ValueError("beams must be a contiguous int32 [groups, width] array")
+    cnt = _host_i32(counts)
+    if cnt.shape != beams.shape:
+        raise ValueError("counts and beams differ in shape")
+    nid = ctypes.c_int32(int(next_id))
+    _check(_lib.pa_beam_prune(pool, beams.shape[0], beams.shape[1], beams.ctypes.data,
+                              cnt.ctypes.data, ctypes.byref(nid)))
+    return nid.value
 
 
 def pa_seq_free(pool, seq_id: int) -> None:

@@ -24,6 +24,7 @@
 // A sequence's #filled is kept as its token count: every table entry but
 // the last holds B tokens, the last holds num_tokens - (entries - 1) * B.
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <new>
 #include <unordered_map>
@@ -64,6 +65,7 @@ struct pa_pool {
     std::vector<int32_t> plan_dec;
     std::vector<int32_t> plan_touched;
     std::vector<Seq *> plan_seqs;
+    std::vector<int32_t> beam_row;   // pa_beam_prune: a group's new beams
     // Prefix cache: full prompt blocks keyed by a hash chain over
     // (parent key, the block's token ids, extra key).  Per block: its key,
     // its parent's key, the extra key and its token ids, to verify a hit.
@@ -401,6 +403,64 @@ int pa_seq_free_batch(pa_pool *pool, int32_t n, const int32_t *seq_ids) {
                         seq_ids[i]);
     }
     for (int32_t i = 0; i < n; ++i) pa_seq_free(pool, seq_ids[i]);
+    return PA_OK;
+}
+
+int pa_beam_prune(pa_pool *pool, int32_t n_groups, int32_t width, int32_t *beams,
+                  const int32_t *counts, int32_t *next_id) {
+    const char *who = "pa_beam_prune";
+    if (!pool || n_groups < 0 || width < 1 || !next_id ||
+        (n_groups > 0 && (!beams || !counts)))
+        return fail(PA_ERR_INVALID_ARG, "%s: bad arguments", who);
+    // check everything first: every beam exists once, each group keeps
+    // `width` survivors, the new ids are unused
+    const uint64_t epoch = ++pool->epoch;
+    int64_t forks = 0;
+    for (int32_t g = 0; g < n_groups; ++g) {
+        int64_t kept = 0;
+        for (int32_t i = 0; i < width; ++i) {
+            const int32_t c = counts[(int64_t)g * width + i], id = beams[(int64_t)g * width + i];
+            if (c < 0) return fail(PA_ERR_INVALID_ARG, "%s: negative count", who);
+            auto it = pool->seqs.find(id);
+            if (it == pool->seqs.end()) return fail(PA_ERR_NO_SEQ, "%s: no sequence %d", who, id);
+            if (it->second.stamp == epoch)
+                return fail(PA_ERR_INVALID_ARG, "%s: sequence %d listed twice", who, id);
+            it->second.stamp = epoch;
+            kept += c;
+            if (c > 1) forks += c - 1;
+        }
+        if (kept != width)
+            return fail(PA_ERR_INVALID_ARG, "%s: group %d keeps %lld beams, not %d", who, g,
+                        (long long)kept, width);
+    }
+    if ((int64_t)*next_id + forks > INT32_MAX)
+        return fail(PA_ERR_INVALID_ARG, "%s: sequence ids run out", who);
+    for (int64_t k = 0; k < forks; ++k)
+        if (pool->seqs.count((int32_t)(*next_id + k)))
+            return fail(PA_ERR_NO_SEQ, "%s: sequence %lld already exists", who,
+                        (long long)(*next_id + k));
+    // apply, group by group: the survivors in beam order, each followed by its
+    // forks; then the pruned beams are freed, in beam order
+    std::vector<int32_t> &nb = pool->beam_row;
+    int32_t nid = *next_id;
+    for (int32_t g = 0; g < n_groups; ++g) {
+        int32_t *row = beams + (int64_t)g * width;
+        const int32_t *cnt = counts + (int64_t)g * width;
+        nb.clear();
+        for (int32_t i = 0; i < width; ++i) {
+            if (cnt[i] == 0) continue;
+            nb.push_back(row[i]);
+            for (int32_t c = 1; c < cnt[i]; ++c) {
+                pa_seq_fork(pool, row[i], nid);
+                nb.push_back(nid++);
+            }
+        }
+        for (int32_t i = 0; i < width; ++i)
+            if (cnt[i] == 0) pa_seq_free(pool, row[i]);
+        std::copy(nb.begin(), nb.end(), row);
+    }
+    nb.clear();
+    *next_id = nid;
     return PA_OK;
 }
 

@@ -172,46 +172,45 @@ def admit_workload(pool, w) -> list:
 
 class BeamGroups:
     """Applies a BeamChurn's survivor draws to a pool through the block
-    manager: forks for repeated survivors, frees for pruned beams.  Keeps the
-    batch (beam sequence ids, group-major) for the next decode step."""
+    manager: forks for repeated survivors, frees for pruned beams, one
+    pa_beam_prune call per step.  Keeps the batch (beam sequence ids,
+    group-major) for the next decode step."""
 
     def __init__(self, pool, churn):
         from . import pa_seq_add, pa_seq_fork
         self.pool, self.churn = pool, churn
+        G, W = len(churn.prompt_lens), churn.width
+        self.beams = np.empty((G, W), np.int32)
         self.next_id = 0
-        self.beams = []
         for g, n in enumerate(churn.prompt_lens):
             root = self.next_id
             pa_seq_add(pool, root, n, want_slots=False)
-            members = [root]
-            for _ in range(churn.width - 1):
-                pa_seq_fork(pool, root, self.next_id + len(members))
-                members.append(self.next_id + len(members))
-            self.next_id += len(members)
-            self.beams.append(members)
+            for j in range(1, W):
+                pa_seq_fork(pool, root, root + j)
+            self.beams[g] = np.arange(root, root + W, dtype=np.int32)
+            self.next_id += W
 
     def ids(self):
-        return [s for members in self.beams for s in members]
+        return self.beams.ravel().tolist()
+
+    def id_array(self):
+        """The batch as an int32 array (a view; valid until the next prune)."""
+        return self.beams.reshape(-1)
 
     def prune(self, survivors):
-        """survivors[g]: beam indices kept by group g (with repeats).  All
-        forks, then all frees, each as one batched library call (a group's
-        forks come before its frees, so the order matches per-beam calls).
-        Returns (forks, frees) performed."""
-        from . import pa_seq_fork_batch, pa_seq_free_batch
-        parents, children, dead = [], [], []
-        for g, keep in enumerate(survivors):
-            members = self.beams[g]
-            new = []
-            for i in sorted(set(keep)):
-                new.append(members[i])
-                for _ in range(keep.count(i) - 1):
-                    parents.append(members[i])
-                    children.append(self.next_id)
-                    new.append(self.next_id)
-                    self.next_id += 1
-            dead.extend(s for i, s in enumerate(members) if i not in keep)
-            self.beams[g] = new
-        pa_seq_fork_batch(self.pool, parents, children)
-        pa_seq_free_batch(self.pool, dead)
-        return len(children), len(dead)
+        """survivors[g]: beam indices kept by group g (with repeats), or an
+        int [groups, width] array of how often each beam is kept.  Returns
+        (forks, frees) performed."""
+        from . import pa_beam_prune
+        W = self.beams.shape[1]
+        if isinstance(survivors, np.ndarray):
+            counts = survivors
+        else:
+            counts = np.zeros(self.beams.shape, np.int32)
+            for g, keep in enumerate(survivors):
+                counts[g] = np.bincount(keep, minlength=W)
+        frees = int((counts == 0).sum())
+        nid = pa_beam_prune(self.pool, self.beams, counts, self.next_id)
+        forks = nid - self.next_id
+        self.next_id = nid
+        return forks, frees
