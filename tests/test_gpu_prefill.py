@@ -220,12 +220,11 @@ def test_prefill_writes_land_where_the_oracle_byte_model_puts_them():
         pk.pa_pool_destroy(pool)
 
 
-def test_prefill_full_size_batch_sampled():
-    """The bench's prefill batch (256 prompts, 40 heads x 128, block 16) in the
-    launch configuration the bench times; the oracle checks a sample of
-    sequences (the longest, the shortest and random ones)."""
+def test_prefill_full_size_batch_every_row():
+    """The bench's prefill batch (256 prompts, 81 539 tokens, 40 heads x 128,
+    block 16) in the launch configuration the bench times; every output row
+    against the oracle (about 1.1 G query-key pairs in fp64 on the host)."""
     w = wl.prefill_b256()
-    rng = wl.value_rng(w)
     H, D, B = w.num_heads, w.head_dim, w.block_size
     lens = np.array(w.prompt_lens)
     desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
@@ -248,20 +247,10 @@ def test_prefill_full_size_batch_sampled():
                             max_q_len=int(lens.max()), status=st)
     torch.cuda.synchronize()
     assert st.item() == 0
-    sample = sorted({int(lens.argmax()), int(lens.argmin())} |
-                    set(rng.choice(len(lens), 6, replace=False).tolist()))
-    used = np.unique(tables[sample][tables[sample] >= 0])
-    remap = np.full(w.num_blocks, -1, np.int32)
-    remap[used] = np.arange(used.size, dtype=np.int32)
-    kcs = kc[torch.from_numpy(used).cuda()].cpu().numpy()
-    vcs = vc[torch.from_numpy(used).cuda()].cpu().numpy()
-    ts = np.where(tables[sample] >= 0, remap[np.maximum(tables[sample], 0)], -1).astype(np.int32)
-    rows = np.concatenate([np.arange(qs[i], qs[i + 1]) for i in sample])
-    qsub = q[torch.from_numpy(rows).cuda()].cpu().numpy()
-    qss = np.concatenate([[0], np.cumsum(lens[sample])]).astype(np.int32)
-    ref = oa.paged_prefill(qsub, kcs, vcs, ts, ctx[sample], qss, w.scale)
-    got = out[torch.from_numpy(rows).cuda()].cpu().numpy()
-    _check(got, ref)
+    assert slots.shape == (T,)
+    ref = oa.paged_prefill(q.cpu().numpy(), kc.cpu().numpy(), vc.cpu().numpy(), tables, ctx, qs,
+                           w.scale)
+    _check(out.cpu().numpy(), ref)
 
 
 def test_prefill_is_bitwise_repeatable():
