@@ -69,3 +69,21 @@ def test_steady_state_batch_does_not_drift():
     first, last = np.mean(means[:300]), np.mean(means[-300:])
     assert abs(last - first) / first < 0.12
     assert held.max() <= wl.CTX_CAP
+
+
+def test_generators_and_oracle_load_without_the_product_library():
+    """The seeded generators and the oracle import nothing from the product
+    package: a process that uses only them (the oracle's timed runs) maps no
+    libpagedkv.so."""
+    import subprocess
+    import sys
+
+    from tests.conftest import ROOT
+    code = ("import sys; sys.path.insert(0, %r)\n"
+            "import workloads, oracle.alloc, oracle.cache_ops\n"
+            "from oracle import attention\n"
+            "attention.max_threads()\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "print('libpagedkv' in maps, 'liboracle_attention' in maps)\n" % ROOT)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True)
+    assert out.stdout.split() == ["False", "True"], out.stdout + out.stderr
