@@ -99,6 +99,26 @@ def test_prefill_matches_oracle(D, B):
     _check(got, ref)
 
 
+@pytest.mark.parametrize("factor", [4.0, 0.25])
+def test_prefill_scores_that_jump_on_a_later_tile(factor):
+    """Keys at positions 256-383 scaled by `factor`: with 4, the rows that
+    reach them see their maximum jump far past the running one on a later,
+    unmasked key tile (the lazy rescale of O and of the probabilities of that
+    tile must take place); with 1/4, the maximum stays where it was."""
+    rng = np.random.default_rng(77)
+    H, D, B = 2, 128, 16
+    ctx = [520, 400]
+    q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ctx, H, D, B)
+    for s in range(len(ctx)):
+        for p in range(256, min(384, ctx[s])):
+            kc[tables[s][p // B], :, p % B, :] = (kc[tables[s][p // B], :, p % B, :].astype(np.float32)
+                                                 * factor).astype(np.float16)
+    scale = float(np.float32(1 / math.sqrt(D)))
+    got = _gpu_prefill(q, kc, vc, tables, ctxa, qs, scale, B)
+    ref = oa.paged_prefill(q, kc, vc, tables, ctxa, qs, scale)
+    _check(got, ref)
+
+
 def test_prefill_block_placement_is_bitwise_irrelevant():
     rng = np.random.default_rng(7)
     H, D, B = 2, 128, 16
