@@ -197,8 +197,9 @@ class SteadyBatch:
 
 def other_rows(args) -> dict:
     """Short runs of the other measured rows for the default bench line:
-    the 40-layer pool-filling step, beam-search churn and prefix caching,
-    each summarised from its own mode's line."""
+    the 40-layer pool-filling step (plain and with beam groups sharing
+    blocks), beam-search churn and prefix caching, each summarised from its
+    own mode's line."""
     import copy
 
     import torch
@@ -214,6 +215,19 @@ def other_rows(args) -> dict:
         "attention_GB/s": f["roofline"]["achieved"], "frac": f["roofline"]["frac"],
         "peak": f["roofline"]["peak"], "bound": "hbm",
         "algorithmic_bytes_per_step": f["roofline"]["algorithmic_bytes_per_step"]}
+    torch.cuda.empty_cache()
+    a.beam = True
+    f = run_full40(a, quiet=True)
+    out["full_40l_beam_step"] = {
+        "workload": f["config"]["workload"], "sequences": f["config"]["sequences"],
+        "pool_bytes": f["config"]["pool_bytes"], "steps": a.steps,
+        "logical_over_unique_blocks": f["config"]["logical_over_unique_blocks"],
+        "copies_per_step": f["config"]["copies_per_step"],
+        "seq_tokens_per_s": f["value"], "ms_per_step": f["ms_per_step"],
+        "logical_attention_GB/s": f["roofline"]["achieved"],
+        "note": "logical bytes count blocks shared by a group's beams once per beam; the "
+                "beams of a group re-read them from L2, so this is not an HBM roofline"}
+    a.beam = False
     torch.cuda.empty_cache()
     a.warmup, a.steps = 3, 20
     b = run_beam_churn(a, quiet=True)
