@@ -514,16 +514,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         return ok = false;
                 return true;
             };
-            // S_x = Q_x K^T for the key tile in K ring stage st
+            // S_x = Q_x K^T for the key tile in K ring stage st.  A descriptor's
+            // start address is its low field (address / 16; shared memory is far
+            // below the field's range), so the descriptors of successive slices
+            // are one base plus a constant.
             auto issue_s = [&](int x, int st) {
-                const uint32_t qb = sQ + x * L::TILE, kb = sK + st * L::TILE;
+                const uint64_t dq = tc::smem_desc(sQ + x * L::TILE, 16, 1024);
+                const uint64_t dk = tc::smem_desc(sK + st * L::TILE, 16, 1024u * NP);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // Q: [panel][128 rows]; K: 8-row groups of NP panels
                     const uint32_t col = (kk & 3) * 32;
-                    tc::mma_ss(tmem + x * 128, tc::smem_desc(qb + (kk >> 2) * kPanel + col, 16, 1024),
-                               tc::smem_desc(kb + (kk >> 2) * 1024u + col, 16, 1024u * NP), idS,
-                               kk > 0 ? 1u : 0u);
+                    tc::mma_ss(tmem + x * 128, dq + (((kk >> 2) * kPanel + col) >> 4),
+                               dk + (((kk >> 2) * 1024u + col) >> 4), idS, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(bar(bars.s_full, x));
             };
@@ -554,13 +557,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // the slot's previous job
                         if (j == 0 && job[x] > 0 && !spin(bar(bars.o_free, x), (job[x] - 1) & 1)) break;
                         tc::fence_after();
-                        const uint32_t vb = sV + (gj % NSV) * L::TILE;
+                        const uint64_t dv0 = tc::smem_desc(sV + (gj % NSV) * L::TILE, 1024, 1024u * NP);
 #pragma unroll
                         for (int kk = 0; kk < TBN / 16; ++kk) {
                             // V: 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart.
                             // P of keys 16 kk .. 16 kk + 15: column half (kk / 4) * 64, then
                             // 16 columns per 32 keys, 8 columns (16 fp16) per slice
-                            const uint64_t dv = tc::smem_desc(vb + kk * 2048u * NP, 1024, 1024u * NP);
+                            const uint64_t dv = dv0 + ((kk * 2048u * NP) >> 4);
                             const uint32_t pa =
                                 tmem + x * 128 + (kk >> 2) * 64 + ((kk >> 1) & 1) * 16 + (kk & 1) * 8;
                             tc::mma_ts(tmem + kOCol + x * 128, pa, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
