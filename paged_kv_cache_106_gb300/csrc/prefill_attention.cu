@@ -122,6 +122,36 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return pol;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Two fp32 values as one packed pair, and back.
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// Packed fp32 pairs: a * b + c and a + b, element by element, one instruction
+// each (round to nearest, as fmaf and + on each element).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Two probabilities as one fp16 pair (lower column in the low half).
 __device__ __forceinline__ uint32_t pack_pair(float p0, float p1) {
     const __half2 h = __floats2half2_rn(p0, p1);
@@ -686,11 +716,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (need_mask) {
                             const int lim = pos - (n0 + cc * 32);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                m4[i & 3] = fmaxf(m4[i & 3], i > lim ? -INFINITY : __uint_as_float(r[i]));
+                            for (int i = 0; i < 16; ++i)
+                                m4[i & 3] = max3f(m4[i & 3], 2 * i > lim ? -INFINITY : __uint_as_float(r[2 * i]),
+                                                  2 * i + 1 > lim ? -INFINITY : __uint_as_float(r[2 * i + 1]));
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(r[i]));
+                            for (int i = 0; i < 16; ++i)
+                                m4[i & 3] = max3f(m4[i & 3], __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
                         }
                     }
                     mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * qs;   // scale > 0
@@ -712,7 +744,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     m_run = mt;
                     l_run *= corr;
                 }
-                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                // x = s * qs - m_run and the running sum, two columns per instruction
+                const uint64_t qs2 = pack_f32x2(qs, qs), negm2 = pack_f32x2(-m_run, -m_run);
+                uint64_t ls2[2] = {0ull, 0ull};
 #pragma unroll 1
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t r[32], w[16];
@@ -728,27 +762,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int lim = pos - (n0 + cc * 32);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float p0 =
-                                2 * i > lim ? 0.f : ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
-                            const float p1 = 2 * i + 1 > lim
-                                                 ? 0.f
-                                                 : ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
-                            ls[i & 3] += p0 + p1;
+                            float x0, x1;
+                            unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(r[2 * i]),
+                                                              __uint_as_float(r[2 * i + 1])),
+                                                   qs2, negm2),
+                                         x0, x1);
+                            const float p0 = 2 * i > lim ? 0.f : ex2(x0);
+                            const float p1 = 2 * i + 1 > lim ? 0.f : ex2(x1);
+                            ls2[i & 1] = add_f32x2(ls2[i & 1], pack_f32x2(p0, p1));
                             w[i] = pack_pair(p0, p1);
                         }
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), qs, -m_run));
-                            const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qs, -m_run));
-                            ls[i & 3] += p0 + p1;
+                            float x0, x1;
+                            unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(r[2 * i]),
+                                                              __uint_as_float(r[2 * i + 1])),
+                                                   qs2, negm2),
+                                         x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            ls2[i & 1] = add_f32x2(ls2[i & 1], pack_f32x2(p0, p1));
                             w[i] = pack_pair(p0, p1);
                         }
                     }
                     // P of these 32 keys as 16 fp16 pairs, over S columns already read
                     tc::st16(sb + cc * 16, w);
                 }
-                l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                {
+                    float a0, a1, b0, b1;
+                    unpack_f32x2(ls2[0], a0, a1);
+                    unpack_f32x2(ls2[1], b0, b1);
+                    l_run += (a0 + b0) + (a1 + b1);
+                }
                 tc::wait_st();
                 if (__any_sync(0xffffffffu, resc && t > 0)) {
                     // O holds the job's tiles < t, complete (S of tile t was committed
