@@ -645,6 +645,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // a meeting, so that the partner's sum is in red_l
         auto epi_read = [&](uint32_t (&hv)[4 * NCH]) {
             const float inv = 1.f / (pend_l + bars.red_l[x][half ^ 1][row]);
+            const uint64_t inv2 = pack_f32x2(inv, inv), zero2 = 0ull;
             tc::fence_after();
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
@@ -652,9 +653,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc::ld32(ob + cc * 32, r);
                 tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    hv[cc * 16 + i] = pack_pair(__uint_as_float(r[2 * i]) * inv,
-                                                __uint_as_float(r[2 * i + 1]) * inv);
+                for (int i = 0; i < 16; ++i) {
+                    float o0, o1;
+                    unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(r[2 * i]),
+                                                      __uint_as_float(r[2 * i + 1])),
+                                           inv2, zero2),
+                                 o0, o1);
+                    hv[cc * 16 + i] = pack_pair(o0, o1);
+                }
             }
         };
         // write it: chunks exchanged within groups of NCH lanes (an NCH x NCH
