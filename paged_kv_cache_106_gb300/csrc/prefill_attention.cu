@@ -703,12 +703,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // the last position among this warp's rows: key chunks after it are
             // masked for every row of the warp
             const int pos_w = u.pos0 + min(q0 + quarter * 32 + 31, u.ql - 1);
+            // the position of this warp's first row: a chunk whose last key is at
+            // or before it needs no mask for any real row of the warp (padded
+            // rows past the queries are never stored)
+            const int pos_f = u.pos0 + q0 + quarter * 32;
             float m_run = -INFINITY, l_run = 0.f;
             for (int t = 0; t < u.nt[x]; ++t, ++sc) {
                 ok = ok && warp_all(mbar_wait_bounded(bar(bars.s_full, x), sc & 1, p.status, true));
                 const int n0 = t * TBN + half * 64;   // first key of this warp's columns
                 // keys past a row's position are masked: key n0 + 32 cc + i with i > lim
-                const bool need_mask = n0 + 63 > u.pos0 + q0;
                 float mt = -INFINITY;
                 if (ok) {
                     tc::fence_after();
@@ -719,7 +722,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         uint32_t r[32];
                         tc::ld32(sb + cc * 32, r);
                         tc::wait_ld();
-                        if (need_mask) {
+                        if (n0 + cc * 32 + 31 > pos_f) {
                             const int lim = pos - (n0 + cc * 32);
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
@@ -764,7 +767,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc::ld32(sb + cc * 32, r);
                     tc::wait_ld();
-                    if (need_mask) {
+                    if (n0 + cc * 32 + 31 > pos_f) {
                         const int lim = pos - (n0 + cc * 32);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
