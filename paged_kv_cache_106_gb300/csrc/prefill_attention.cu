@@ -58,6 +58,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -69,6 +70,20 @@
 namespace pagedkv {
 namespace {
 
+// Work counters of the prefill launches.  A launch takes its units one at a
+// time from `next`; each block adds one to `done` when it takes no more, and
+// the last one sets both back to zero, so that the next launch (on the same
+// stream, or a replay of the same graph) finds zeros.  Launches pick counter
+// (call number % kUnitCounters): calls on different streams stay apart while
+// fewer than kUnitCounters of them are in flight at once.
+struct UnitCounter {
+    unsigned long long next;
+    unsigned int done;
+    unsigned int pad;
+};
+constexpr int kUnitCounters = 64;
+__device__ UnitCounter g_unit_ctr[kUnitCounters];
+
 struct PrefillParams {
     __half *out;
     const __half *q;
@@ -77,10 +92,12 @@ struct PrefillParams {
     const int32_t *tables;
     const int32_t *ctx_lens;
     const int32_t *q_starts;
-    int32_t num_heads, num_blocks, max_blocks, max_q_len, q_rows, q_pairs, bshift;
+    int32_t num_heads, num_blocks, max_blocks, max_q_len, q_rows, bshift;
     float qscale;  // scale * log2(e): softmax evaluated with exp2
     int32_t *status;
+    UnitCounter *units;             // this launch's unit counter
 };
+
 
 // 2^x by the PTX approximation instruction (relative error about 2^-22;
 // -inf gives +0).
@@ -163,6 +180,7 @@ constexpr int TBN = 128;          // key positions per key tile
 constexpr int NSK = 2;            // K ring stages
 constexpr int NSV = 2;            // V ring stages
 constexpr int NU = 4;             // unit descriptors in flight
+constexpr int kLookahead = 2;     // units a block takes before its readers have fetched them all
 // warps 0-7: softmax and epilogue of slot 0, 8-15: of slot 1
 constexpr int kMmaWarp = 16, kKWarp = 17, kVWarp = 18, kSchedWarp = 19;
 constexpr int kTcThreads = 640;   // 20 warps
@@ -291,9 +309,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bar(bars.q_full, x), 1);
             mbar_init(bar(bars.q_empty, x), 1);   // the job's last Q K^T is done
             mbar_init(bar(bars.s_full, x), 1);
-            mbar_init(bar(bars.p_full, x), 256);  // the slot's softmax threads
+            mbar_init(bar(bars.p_full, x), 8);    // the slot's softmax warps
             mbar_init(bar(bars.o_full, x), 1);
-            mbar_init(bar(bars.o_free, x), 256);  // the slot's softmax threads
+            mbar_init(bar(bars.o_free, x), 8);    // the slot's softmax warps
         }
         for (int i = 0; i < NSK; ++i) {
             mbar_init(bar(bars.k_full, i), 1);
@@ -315,7 +333,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = bars.tmem;
-    const int q_pairs = p.q_pairs;
 
     // Reads unit k of this CTA from the ring (bounded wait); n_tiles < 0 on timeout.
     auto get_unit = [&](int k, Unit &u) {
@@ -329,68 +346,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
 
     if (warp == kSchedWarp) {
-        // ---- scheduler: lanes test 32 candidate units at a time, the valid ones
-        // are published in order; a unit with one query tile takes the slots in
-        // turn, so that consecutive such units overlap
-        const long long V = (long long)n_seqs * H * q_pairs;
+        // ---- scheduler: the launch's units in the order (sequence, pair of
+        // query tiles from the last, head) are taken one at a time from the
+        // launch's counter, so that blocks that finish early take more (with a
+        // fixed share per block, the 256-prompt batch gave the heaviest block
+        // about 5 % more work than the mean).  A unit
+        // index is mapped to its sequence by a cursor that walks the sequences
+        // 32 at a time, summing their units; the indices a block takes only
+        // grow, so its cursor only moves forward.  A unit is taken only once
+        // every reader has fetched the unit two before it: a block holds few
+        // units it has not started.  A unit with one query tile takes the slots
+        // in turn, so that consecutive such units overlap.
         int k = 0, singles = 0;
         bool ok = true;
-        for (long long base_v = blockIdx.x; ok && base_v < V; base_v += 32ll * gridDim.x) {
-            const long long v = base_v + (long long)lane * gridDim.x;
+        int w0 = -32;                      // first sequence of the cursor's window
+        unsigned long long before = 0;     // units of the sequences before the window
+        unsigned long long incl = 0;       // units of the window's sequences up to this lane's
+        unsigned long long win = 0;        // units of the window
+        unsigned long long own = 0;        // units of this lane's sequence
+        for (;;) {
+            if (k >= kLookahead)
+                ok = warp_all(mbar_wait_bounded(bar(bars.unit_empty, (k - kLookahead) % NU),
+                                                ((k - kLookahead) / NU) & 1, p.status, true));
+            if (!ok) break;
+            unsigned long long d = 0;
+            if (lane == 0) d = atomicAdd(&p.units->next, 1ull);
+            d = __shfl_sync(0xffffffffu, d, 0);
+            while (d >= before + win && w0 + 32 < n_seqs) {
+                before += win;
+                w0 += 32;
+                const int s = w0 + lane;
+                unsigned long long n = 0;
+                if (s < n_seqs) {
+                    const int q_beg = p.q_starts[s], ql = p.q_starts[s + 1] - q_beg, ctx = p.ctx_lens[s];
+                    const bool bad_len = ql < 0 || ql > ctx || ql > p.max_q_len || q_beg < 0 ||
+                                         (int64_t)q_beg + ql > p.q_rows;
+                    const bool bad_ctx = (int64_t)ctx > ((int64_t)p.max_blocks << p.bshift);
+                    // every block's cursor passes every sequence; one reports
+                    if ((bad_len || bad_ctx) && blockIdx.x == 0)
+                        report(p.status, bad_len ? PA_ERR_INVALID_ARG : PA_ERR_BAD_BLOCK);
+                    if (!bad_len && !bad_ctx)
+                        n = (unsigned long long)H * (unsigned long long)(((ql + TBM - 1) / TBM + 1) / 2);
+                }
+                own = n;
+                incl = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                win = __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (d >= before + win) break;   // past the last unit
+            const int src = __ffs(__ballot_sync(0xffffffffu, incl > d - before)) - 1;
+            const unsigned long long excl = __shfl_sync(0xffffffffu, incl - own, src);
             Unit u{};
-            bool valid = false;
-            if (v < V) {
-                // v -> (sequence, pair of query tiles from the last, head)
-                u.s = (int)(v / ((long long)H * q_pairs));
-                const int r = (int)(v - (long long)u.s * H * q_pairs);
-                const int pr = r / H;
-                u.h = r - pr * H;
-                u.q_beg = p.q_starts[u.s];
-                u.ql = p.q_starts[u.s + 1] - u.q_beg;
-                const int ctx = p.ctx_lens[u.s];
-                const bool bad_len = u.ql < 0 || u.ql > ctx || u.ql > p.max_q_len ||
-                                     u.q_beg < 0 || (int64_t)u.q_beg + u.ql > p.q_rows;
-                const bool bad_ctx = (int64_t)ctx > ((int64_t)p.max_blocks << p.bshift);
-                if ((bad_len || bad_ctx) && pr == 0 && u.h == 0)
-                    report(p.status, bad_len ? PA_ERR_INVALID_ARG : PA_ERR_BAD_BLOCK);
-                const int xa = (u.ql + TBM - 1) / TBM - 1 - 2 * pr;   // the pair's later query tile
-                valid = !bad_len && !bad_ctx && xa >= 0;
-                if (valid) {
-                    u.pos0 = ctx - u.ql;
-                    for (int x = 0; x < 2; ++x) {
-                        const int qt = xa - x;
-                        u.q0[x] = qt * TBM;
-                        const int end = u.pos0 + u.q0[x] + min(TBM, u.ql - u.q0[x]);
-                        u.nt[x] = qt >= 0 ? (end + TBN - 1) / TBN : 0;
-                    }
-                    u.n_end = u.pos0 + u.q0[0] + min(TBM, u.ql - u.q0[0]);
-                    u.n_tiles = u.nt[0];
-                }
+            u.s = w0 + src;
+            const unsigned long long r = d - before - excl;   // unit within the sequence
+            const int pr = (int)(r / (unsigned)H);
+            u.h = (int)(r - (unsigned long long)pr * H);
+            u.q_beg = p.q_starts[u.s];
+            u.ql = p.q_starts[u.s + 1] - u.q_beg;
+            const int ctx = p.ctx_lens[u.s];
+            const int xa = (u.ql + TBM - 1) / TBM - 1 - 2 * pr;   // the pair's later query tile
+            u.pos0 = ctx - u.ql;
+            for (int x = 0; x < 2; ++x) {
+                const int qt = xa - x;
+                u.q0[x] = qt * TBM;
+                const int end = u.pos0 + u.q0[x] + min(TBM, u.ql - u.q0[x]);
+                u.nt[x] = qt >= 0 ? (end + TBN - 1) / TBN : 0;
             }
-            uint32_t mask = __ballot_sync(0xffffffffu, valid);
-            while (mask) {
-                const int src = __ffs(mask) - 1;
-                mask &= mask - 1;
-                const bool single = __shfl_sync(0xffffffffu, u.nt[1] == 0, src);
-                if (k >= NU)
-                    ok = warp_all(mbar_wait_bounded(bar(bars.unit_empty, k % NU),
-                                                    ((k / NU) - 1) & 1, p.status, true));
-                if (!ok) break;
-                if (lane == src) {
-                    if (single && (singles & 1)) {   // the lone tile goes to slot 1
-                        u.q0[1] = u.q0[0];
-                        u.nt[1] = u.nt[0];
-                        u.nt[0] = 0;
-                    }
-                    bars.unit[k % NU] = u;
-                    mbar_arrive(bar(bars.unit_full, k % NU));
+            u.n_end = u.pos0 + u.q0[0] + min(TBM, u.ql - u.q0[0]);
+            u.n_tiles = u.nt[0];
+            const bool single = u.nt[1] == 0;
+            if (lane == 0) {
+                if (single && (singles & 1)) {   // the lone tile goes to slot 1
+                    u.q0[1] = u.q0[0];
+                    u.nt[1] = u.nt[0];
+                    u.nt[0] = 0;
                 }
-                singles += single ? 1 : 0;
-                __syncwarp();
-                ++k;
+                bars.unit[k % NU] = u;
+                mbar_arrive(bar(bars.unit_full, k % NU));
             }
+            singles += single ? 1 : 0;
+            __syncwarp();
+            ++k;
         }
-        // end marker
+        // this block takes no more units; the last block resets the counter
+        if (lane == 0 && atomicAdd(&p.units->done, 1u) == gridDim.x - 1) {
+            p.units->next = 0;
+            p.units->done = 0;
+        }
+        // end marker, once its ring slot is free
         if (ok && k >= NU)
             ok = warp_all(mbar_wait_bounded(bar(bars.unit_empty, k % NU), ((k / NU) - 1) & 1,
                                             p.status, true));
@@ -818,8 +865,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc::wait_st();
                 }
+                // one arrival per warp, once every lane's stores are done
                 tc::fence_before();
-                mbar_arrive(bar(bars.p_full, x));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bars.p_full, x));
                 if (t == 0 && pend) {
                     // the previous job's O (complete: this tile's S was committed after
                     // its last P V) is read, then released to this job's first P V;
@@ -827,7 +876,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint32_t hv[4 * NCH];
                     epi_read(hv);
                     tc::fence_before();
-                    mbar_arrive(bar(bars.o_free, x));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bars.o_free, x));
                     epi_store(hv);
                 }
             }
@@ -888,6 +938,20 @@ int sm_count_of_current_device() {
             n[dev] = 0;
     });
     return n[dev];
+}
+
+// The device address of the unit counters, per device, looked up once.
+UnitCounter *unit_counters_of_current_device() {
+    static std::once_flag once[64];
+    static UnitCounter *ptr[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::call_once(once[dev], [&] {
+        void *a = nullptr;
+        ptr[dev] = cudaGetSymbolAddress(&a, g_unit_ctr) == cudaSuccess
+                       ? static_cast<UnitCounter *>(a) : nullptr;
+    });
+    return ptr[dev];
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime
@@ -974,7 +1038,10 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
         rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 8 >> m);
     if (rc == PA_OK) rc = encode_map(&maps.q, p.q, 3, (uint64_t)p.q_rows, H, D, TBM);
     if (rc != PA_OK) return rc;
-    p.q_pairs = ((p.max_q_len + TBM - 1) / TBM + 1) / 2;
+    static std::atomic<uint32_t> calls{0};
+    UnitCounter *ctrs = unit_counters_of_current_device();
+    if (!ctrs) return fail(PA_ERR_CUDA, "prefill: cannot find the unit counters");
+    p.units = ctrs + calls.fetch_add(1) % kUnitCounters;
     paged_prefill_tc<D><<<sms, kTcThreads, TcLayout<D>::BYTES, st>>>(p, maps, n_seqs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -1021,7 +1088,7 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     p.max_blocks = max_blocks;
     p.max_q_len = max_q_len;
     p.q_rows = q_rows;
-    p.q_pairs = 0;   // set by the launcher from its tile height
+    p.units = nullptr;   // set by the launcher
     p.bshift = bshift;
     p.qscale = scale * 1.4426950408889634f;
     p.status = status;

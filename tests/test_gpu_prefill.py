@@ -313,6 +313,69 @@ def test_prefill_is_bitwise_repeatable():
             assert torch.equal(out.view(torch.int16), first.view(torch.int16))
 
 
+def test_prefill_replayed_from_a_graph_repeated_and_on_two_streams():
+    """A launch takes its (sequence, query-tile pair, head) units one at a
+    time from a counter that the launch sets back to zero when it ends, one of
+    64 counters picked per call.  A launch captured in a CUDA graph and
+    replayed five times, 70 launches in a row (more calls than counters) and
+    two launches in flight at once on two streams each give bitwise the
+    output of a single launch, which matches the oracle."""
+    rng = np.random.default_rng(31)
+    H, D, B = 4, 128, 16
+    ctx = [300, 129, 1, 520, 77, 256]
+    q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ctx, H, D, B)
+    scale = 1.0 / math.sqrt(D)
+    desc = pk.PoolDesc(kc.shape[0], B, num_heads=H, head_dim=D)
+    dq, dk, dv, dt, dc, dqs = (_dev(a) for a in (q, kc, vc, tables, ctxa, qs))
+    mql = max(ctx)
+    st = _status()
+
+    def launch(out, stream=None):
+        pk.pa_prefill_attention(out, dq, dk, dv, dt, dc, dqs, scale, desc, max_q_len=mql,
+                                status=st, stream=stream)
+
+    ref = torch.full_like(dq, float("nan"))
+    launch(ref)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _check(ref.cpu().numpy(), oa.paged_prefill(q, kc, vc, tables, ctxa, qs, scale))
+    bits = ref.view(torch.int16)
+
+    s = torch.cuda.Stream()
+    out_g = torch.full_like(dq, float("nan"))
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        launch(out_g, s)   # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        launch(out_g, s)
+    for _ in range(5):
+        out_g.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g.view(torch.int16), bits)
+
+    outs = [torch.full_like(dq, float("nan")) for _ in range(70)]
+    for o in outs:
+        launch(o)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), bits)
+
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    o1, o2 = torch.full_like(dq, float("nan")), torch.full_like(dq, float("nan"))
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s1):
+        launch(o1, s1)
+    with torch.cuda.stream(s2):
+        launch(o2, s2)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(o1.view(torch.int16), bits) and torch.equal(o2.view(torch.int16), bits)
+
+
 def test_prefill_status_reports_bad_lengths_and_blocks():
     rng = np.random.default_rng(13)
     H, D, B = 2, 64, 4
