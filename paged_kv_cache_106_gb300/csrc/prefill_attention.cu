@@ -23,8 +23,9 @@
 //                  then the same for slot 1, so one slot's products run on
 //                  the tensor pipe while the other slot's softmax works;
 //       warp 17    Q tiles and K tiles by TMA, warp 18 V tiles by TMA;
-//       warp 19    scheduler: publishes this CTA's non-empty units through a
-//                  4-slot descriptor ring.
+//       warp 19    scheduler: takes units one at a time from the launch's
+//                  counter (CTAs that finish early take more) and publishes
+//                  them through a 4-slot descriptor ring.
 //     A job's output is written by its softmax warps at the slot's next job:
 //     after writing that job's first P they read the old O (complete: the
 //     new S was committed after its last P V), release it to the first P V,
