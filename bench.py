@@ -1148,7 +1148,21 @@ class PrefillBatch:
                 "unique_bytes_per_launch": self.unique_bytes, "hbm_floor_ms": t_hbm,
                 "algorithmic_flops_per_launch": self.flops, "tensor_floor_ms": t_tc,
                 "tflops": self.flops / (attn_ms / 1e3) / 1e12,
-                "GB/s": self.unique_bytes / (attn_ms / 1e3) / 1e9}
+                "GB/s": self.unique_bytes / (attn_ms / 1e3) / 1e9,
+                **self.traffic()}
+
+    def traffic(self) -> dict:
+        """DRAM bytes per launch from the committed ncu capture of the full
+        256-prompt batch (its DRAM bytes over unique bytes, times this batch's
+        unique bytes), if it was taken on the current kernel code and this is
+        that batch (the ratio does not carry over to a subset of prompts)."""
+        t = _kernel_traffic(os.path.join(ROOT, "paged_kv_cache_106_gb300", "csrc", "prefill_attention.cu"),
+                            "prefill_attention_traffic.json")
+        full = t is not None and t.get("prompt_tokens") == self.T
+        return {"kernel": "paged_prefill_tc<128> (pa_prefill_attention)",
+                "traffic": t["traffic_over_algorithmic"] * self.unique_bytes if full else None,
+                "traffic_over_algorithmic": t["traffic_over_algorithmic"] if full else None,
+                "traffic_from": t["capture"] if full else None}
 
     def close(self):
         self.pk.pa_pool_destroy(self.pool)
@@ -1231,13 +1245,6 @@ def run_prefill(args):
         [T * args.steps, T * e2e_steps], [el, e2e_s * e2e_steps], dev)
     if rank == 0:
         roof = pb.roofline(attn_ms)
-        traffic = _kernel_traffic(os.path.join(ROOT, "paged_kv_cache_106_gb300", "csrc",
-                                               "prefill_attention.cu"),
-                                  "prefill_attention_traffic.json")
-        roof["kernel"] = "paged_prefill_tc<128> (pa_prefill_attention)"
-        roof["traffic"] = None if traffic is None or args.prompts else \
-            traffic["traffic_over_algorithmic"] * pb.unique_bytes
-        roof["traffic_from"] = None if traffic is None else traffic["capture"]
         line = {
             "metric": PREFILL_METRIC, "value": tok_all / el_max, "unit": PREFILL_UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
