@@ -160,17 +160,36 @@ def _pool_setup(pk, w):
 
 class SteadyBatch:
     """Host side of the continuous batch: replaces finished sequences.
-    Newcomers' (prompt, target) lengths are seeded inputs, drawn in blocks."""
+    Newcomers' (prompt, target) lengths are seeded inputs, drawn in blocks.
+    A sequence is replaced at the first step whose admission sees it hold at
+    least its target length; that step is known when it is admitted, so
+    each step looks up only its own list (in ascending batch index)."""
 
     DRAW_BLOCK = 4096
 
     def __init__(self, pk, pool, w, rng):
         self.pk, self.pool, self.rng = pk, pool, rng
-        self.held = np.array(w.prompt_lens, np.int64)
+        self.prompt = np.array(w.prompt_lens, np.int64)   # tokens held when admitted
         self.target = np.array(w.targets, np.int64)
+        self.since = np.zeros(len(self.prompt), np.int64)  # step of admission
+        self.step = 0
+        self.due = {}
+        for i in range(len(self.prompt)):
+            self._schedule(i, 0)
         self.next_id = len(w.prompt_lens)
         self.replaced = 0
         self._draws, self._next_draw = None, self.DRAW_BLOCK
+
+    @property
+    def held(self):
+        """Tokens each sequence of the batch holds now."""
+        return self.prompt + (self.step - self.since)
+
+    def _schedule(self, i, first):
+        # held at step self.step + j is prompt + j; replaced at the first
+        # j >= first with prompt + j >= target
+        j = max(first, int(self.target[i] - self.prompt[i]))
+        self.due.setdefault(self.step + j, []).append(i)
 
     def _draw(self):
         if self._next_draw == self.DRAW_BLOCK:
@@ -182,17 +201,21 @@ class SteadyBatch:
         return self._draws[0][i], self._draws[1][i]
 
     def admit(self, ids):
-        for i in np.flatnonzero(self.held >= self.target).tolist():
+        due = self.due.pop(self.step, None)
+        if not due:
+            return
+        for i in sorted(due):
             self.pk.pa_seq_free(self.pool, int(ids[i]))
             prompt, target = self._draw()
             self.pk.pa_seq_add(self.pool, self.next_id, prompt, want_slots=False)
             ids[i] = self.next_id
             self.next_id += 1
-            self.held[i], self.target[i] = prompt, target
+            self.prompt[i], self.target[i], self.since[i] = prompt, target, self.step
+            self._schedule(i, 1)
             self.replaced += 1
 
     def appended(self):
-        self.held += 1
+        self.step += 1
 
 
 def other_rows(args) -> dict:

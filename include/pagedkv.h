@@ -229,6 +229,25 @@ int pa_decode_step_prepare(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids
                            int32_t *tables_out, int32_t *copies_out, int32_t copies_cap,
                            int32_t *n_copies_out);
 
+/* pa_decode_step_prepare for a staging buffer that a serving loop reuses
+ * step after step: the outputs and their meaning are the same, but row i of
+ * tables_out is written only when sequence seq_ids[i]'s block table changed
+ * since this call last wrote that row.  row_versions (host, n_seqs uint64,
+ * owned by the caller) records what each row holds: zero it before the first
+ * call, and keep one such array per tables_out buffer and max_blocks (reset
+ * it to zero when either changes, or when anything else writes tables_out).
+ * A table changes when its sequence is added, forked, moved between pools,
+ * or takes a new or copied block; in a decode step that is about one
+ * sequence in B, so most rows are left as they are.  Table versions are
+ * unique in the process, so a row never matches another sequence or pool.
+ * Errors: as pa_decode_step_prepare; PA_ERR_INVALID_ARG for a NULL
+ * row_versions when rows are to be written. */
+int pa_decode_step_prepare_rows(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                                int32_t max_blocks, int64_t *slot_mapping_out,
+                                int32_t *ctx_lens_out, int32_t *tables_out,
+                                uint64_t *row_versions, int32_t *copies_out, int32_t copies_cap,
+                                int32_t *n_copies_out);
+
 /* Swapping ([review] §4.5 (1) swapping; [notes] §3.5 Swapping, CPU block
  * manager): a preempted group of sequences moves, all its blocks at once,
  * from the GPU pool to a second pool that manages swap space in host memory,

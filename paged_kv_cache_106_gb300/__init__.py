@@ -87,6 +87,7 @@ def _load():
         "pa_alloc_slots_n": (i32, [vp, i32, vp, vp, vp, vp, i32, P(i32)]),
         "pa_get_block_tables": (i32, [vp, i32, vp, i32, vp, vp]),
         "pa_decode_step_prepare": (i32, [vp, i32, vp, i32, vp, vp, vp, vp, i32, P(i32)]),
+        "pa_decode_step_prepare_rows": (i32, [vp, i32, vp, i32, vp, vp, vp, vp, vp, i32, P(i32)]),
         "pa_seq_info": (i32, [vp, i32, P(i32), P(i32)]),
         "pa_pool_num_free": (i32, [vp, P(i32)]),
         "pa_pool_free_queue": (i32, [vp, vp, i32, P(i32)]),
@@ -343,6 +344,32 @@ def pa_decode_step_prepare(pool, seq_ids, max_blocks: int, slot_out=None, ctx_ou
     return slots, ctx, tables, copies[: nc.value]
 
 
+def pa_decode_step_prepare_rows(pool, seq_ids, max_blocks: int, tables, row_versions,
+                                slot_out=None, ctx_out=None, copies_out=None,
+                                copies_cap: int | None = None):
+    """pa_decode_step_prepare into a ``tables`` array (int32[n, max_blocks])
+    that the caller keeps from step to step, with its ``row_versions``
+    (uint64[n], zeros at first): only rows whose sequence's table changed are
+    rewritten.  Returns (slot_mapping, ctx_lens, tables, copies)."""
+    ids = _host_i32(seq_ids)
+    n = ids.shape[0]
+    if tables.dtype != np.int32 or tables.shape != (n, max_blocks) or not tables.flags.c_contiguous:
+        raise ValueError("tables must be a contiguous int32 array of shape (n, max_blocks)")
+    if row_versions.dtype != np.uint64 or row_versions.shape != (n,) or \
+            not row_versions.flags.c_contiguous:
+        raise ValueError("row_versions must be a contiguous uint64 array of length n")
+    cap = n if copies_cap is None else int(copies_cap)
+    slots = np.empty(n, np.int64) if slot_out is None else slot_out
+    ctx = np.empty(n, np.int32) if ctx_out is None else ctx_out
+    copies = np.empty((max(cap, 1), 2), np.int32) if copies_out is None else copies_out
+    nc = ctypes.c_int32(0)
+    _check(_lib.pa_decode_step_prepare_rows(pool, n, ids.ctypes.data, int(max_blocks),
+                                            slots.ctypes.data, ctx.ctypes.data, tables.ctypes.data,
+                                            row_versions.ctypes.data, copies.ctypes.data, cap,
+                                            ctypes.byref(nc)))
+    return slots, ctx, tables, copies[: nc.value]
+
+
 def pa_decode_step_prepare_into(pool, n_seqs: int, ids_addr: int, max_blocks: int,
                                 slots_addr: int, ctx_addr: int, tables_addr: int,
                                 copies_addr: int, copies_cap: int, n_copies) -> int:
@@ -351,6 +378,20 @@ def pa_decode_step_prepare_into(pool, n_seqs: int, ids_addr: int, max_blocks: in
     receives the copy count.  Returns it."""
     _check(_lib.pa_decode_step_prepare(pool, n_seqs, ids_addr, max_blocks, slots_addr, ctx_addr,
                                        tables_addr, copies_addr, copies_cap, ctypes.byref(n_copies)))
+    return n_copies.value
+
+
+def pa_decode_step_prepare_rows_into(pool, n_seqs: int, ids_addr: int, max_blocks: int,
+                                     slots_addr: int, ctx_addr: int, tables_addr: int,
+                                     versions_addr: int, copies_addr: int, copies_cap: int,
+                                     n_copies) -> int:
+    """pa_decode_step_prepare_rows on raw host addresses: table rows whose
+    sequence's table is unchanged since this call last wrote them (per the
+    caller's ``versions_addr`` array, one uint64 per row) are left as they
+    are.  ``n_copies`` is a ctypes.c_int32 that receives the copy count."""
+    _check(_lib.pa_decode_step_prepare_rows(pool, n_seqs, ids_addr, max_blocks, slots_addr,
+                                            ctx_addr, tables_addr, versions_addr, copies_addr,
+                                            copies_cap, ctypes.byref(n_copies)))
     return n_copies.value
 
 

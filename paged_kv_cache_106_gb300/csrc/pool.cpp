@@ -24,6 +24,7 @@
 // A sequence's #filled is kept as its token count: every table entry but
 // the last holds B tokens, the last holds num_tokens - (entries - 1) * B.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstring>
 #include <new>
@@ -39,7 +40,13 @@ struct Seq {
     std::vector<int32_t> table;
     int32_t num_tokens = 0;
     uint64_t stamp = 0;   // the batched call that last listed it (duplicate check)
+    uint64_t tver = 0;    // table version: a new value at every change of the table
 };
+
+// Table versions, unique in the process (a sequence keeps its version when
+// it moves between pools); 0 is never handed out.
+std::atomic<uint64_t> g_table_version{0};
+uint64_t next_table_version() { return ++g_table_version; }
 
 }  // namespace
 
@@ -209,6 +216,7 @@ int pa_seq_add(pa_pool *pool, int32_t seq_id, int32_t n_tokens, int64_t *slots_o
     s.table.reserve((size_t)need);
     for (int64_t i = 0; i < need; ++i) s.table.push_back(pool->pop_free());
     s.num_tokens = n_tokens;
+    s.tver = next_table_version();
     if (slots_out)
         for (int32_t p = 0; p < n_tokens; ++p)
             slots_out[p] = (int64_t)s.table[(size_t)(p / B)] * B + p % B;
@@ -281,6 +289,7 @@ int pa_seq_add_tokens(pa_pool *pool, int32_t seq_id, int32_t n_tokens, const int
         }
     }
     s.num_tokens = n_tokens;
+    s.tver = next_table_version();
     if (slots_out)
         for (int32_t p = 0; p < n_tokens; ++p)
             slots_out[p] = (int64_t)s.table[(size_t)(p / B)] * B + p % B;
@@ -343,6 +352,7 @@ static int move_group(const char *who, pa_pool *from, pa_pool *to, int32_t n_seq
         Seq s = std::move(it->second);
         from->seqs.erase(it);
         for (int32_t &b : s.table) b = moved[b];
+        s.tver = next_table_version();
         to->seqs.emplace(seq_ids[i], std::move(s));
     }
     // the source blocks go back to their free queue, last-used first
@@ -372,6 +382,7 @@ int pa_seq_fork(pa_pool *pool, int32_t parent, int32_t child) {
         return fail(PA_ERR_NO_SEQ, "pa_seq_fork: sequence %d already exists", child);
     Seq c = it->second;
     for (int32_t b : c.table) ++pool->ref[(size_t)b];
+    c.tver = next_table_version();
     pool->seqs.emplace(child, std::move(c));
     return PA_OK;
 }
@@ -543,6 +554,7 @@ int32_t commit_append(pa_pool *pool, int32_t n_seqs, int64_t *slot_mapping_out,
         Seq &s = *pool->plan_seqs[(size_t)i];
         if (s.table.empty() || pool->last_filled(s) == B) {
             s.table.push_back(pool->pop_free());
+            s.tver = next_table_version();
         } else {
             const int32_t last = s.table.back();
             if (pool->ref[(size_t)last] > 1) {
@@ -552,6 +564,7 @@ int32_t commit_append(pa_pool *pool, int32_t n_seqs, int64_t *slot_mapping_out,
                 ++c;
                 --pool->ref[(size_t)last];
                 s.table.back() = nb;
+                s.tver = next_table_version();
             }
         }
         const int32_t off = s.num_tokens - (int32_t)(s.table.size() - 1) * B;
@@ -559,6 +572,46 @@ int32_t commit_append(pa_pool *pool, int32_t n_seqs, int64_t *slot_mapping_out,
         ++s.num_tokens;
     }
     return c;
+}
+
+// The decode step: append one token to each listed sequence (plan, then
+// commit), then its slot, context length and padded table row.  With
+// row_versions, row i is written only when the sequence's table version
+// differs from row_versions[i] (then stored there).
+int decode_step_prepare(pa_pool *pool, const char *who, int32_t n_seqs, const int32_t *seq_ids,
+                        int32_t max_blocks, int64_t *slot_mapping_out, int32_t *ctx_lens_out,
+                        int32_t *tables_out, uint64_t *row_versions, int32_t *copies_out,
+                        int32_t copies_cap, int32_t *n_copies_out) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "%s: NULL pool", who);
+    if (n_seqs < 0 || max_blocks < 0 || copies_cap < 0 || (copies_cap > 0 && !copies_out) ||
+        (n_seqs > 0 && (!seq_ids || !slot_mapping_out || !ctx_lens_out ||
+                        (max_blocks > 0 && !tables_out))))
+        return fail(PA_ERR_INVALID_ARG, "%s: bad arguments", who);
+    int64_t need = 0;
+    int32_t n_copies = 0;
+    int rc = plan_append(pool, who, n_seqs, seq_ids, max_blocks, &need, &n_copies);
+    if (rc != PA_OK) return rc;
+    if (need > pool->count)
+        return fail(PA_ERR_OUT_OF_BLOCKS, "%s: need %lld blocks, %lld free", who,
+                    (long long)need, (long long)pool->count);
+    if (n_copies > copies_cap)
+        return fail(PA_ERR_INVALID_ARG, "%s: %d copies needed, copies_cap is %d", who, n_copies,
+                    copies_cap);
+    const int32_t c = commit_append(pool, n_seqs, slot_mapping_out, copies_out);
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        const Seq &s = *pool->plan_seqs[(size_t)i];
+        ctx_lens_out[i] = s.num_tokens;
+        if (row_versions) {
+            if (row_versions[i] == s.tver) continue;   // the row already holds this table
+            row_versions[i] = s.tver;
+        }
+        int32_t *row = tables_out + (int64_t)i * max_blocks;
+        const size_t n = s.table.size();   // >= 1: the call appended a token
+        std::memcpy(row, s.table.data(), n * sizeof(int32_t));
+        for (int32_t j = (int32_t)n; j < max_blocks; ++j) row[j] = -1;
+    }
+    if (n_copies_out) *n_copies_out = c;
+    return PA_OK;
 }
 
 }  // namespace
@@ -591,33 +644,21 @@ int pa_decode_step_prepare(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids
                            int32_t max_blocks, int64_t *slot_mapping_out, int32_t *ctx_lens_out,
                            int32_t *tables_out, int32_t *copies_out, int32_t copies_cap,
                            int32_t *n_copies_out) {
-    const char *who = "pa_decode_step_prepare";
-    if (!pool) return fail(PA_ERR_INVALID_ARG, "%s: NULL pool", who);
-    if (n_seqs < 0 || max_blocks < 0 || copies_cap < 0 || (copies_cap > 0 && !copies_out) ||
-        (n_seqs > 0 && (!seq_ids || !slot_mapping_out || !ctx_lens_out ||
-                        (max_blocks > 0 && !tables_out))))
-        return fail(PA_ERR_INVALID_ARG, "%s: bad arguments", who);
-    int64_t need = 0;
-    int32_t n_copies = 0;
-    int rc = plan_append(pool, who, n_seqs, seq_ids, max_blocks, &need, &n_copies);
-    if (rc != PA_OK) return rc;
-    if (need > pool->count)
-        return fail(PA_ERR_OUT_OF_BLOCKS, "%s: need %lld blocks, %lld free", who,
-                    (long long)need, (long long)pool->count);
-    if (n_copies > copies_cap)
-        return fail(PA_ERR_INVALID_ARG, "%s: %d copies needed, copies_cap is %d", who, n_copies,
-                    copies_cap);
-    const int32_t c = commit_append(pool, n_seqs, slot_mapping_out, copies_out);
-    for (int32_t i = 0; i < n_seqs; ++i) {
-        const Seq &s = *pool->plan_seqs[(size_t)i];
-        int32_t *row = tables_out + (int64_t)i * max_blocks;
-        const size_t n = s.table.size();   // >= 1: the call appended a token
-        std::memcpy(row, s.table.data(), n * sizeof(int32_t));
-        for (int32_t j = (int32_t)n; j < max_blocks; ++j) row[j] = -1;
-        ctx_lens_out[i] = s.num_tokens;
-    }
-    if (n_copies_out) *n_copies_out = c;
-    return PA_OK;
+    return decode_step_prepare(pool, "pa_decode_step_prepare", n_seqs, seq_ids, max_blocks,
+                               slot_mapping_out, ctx_lens_out, tables_out, nullptr, copies_out,
+                               copies_cap, n_copies_out);
+}
+
+int pa_decode_step_prepare_rows(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
+                                int32_t max_blocks, int64_t *slot_mapping_out,
+                                int32_t *ctx_lens_out, int32_t *tables_out,
+                                uint64_t *row_versions, int32_t *copies_out, int32_t copies_cap,
+                                int32_t *n_copies_out) {
+    if (n_seqs > 0 && max_blocks > 0 && !row_versions)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_step_prepare_rows: NULL row_versions");
+    return decode_step_prepare(pool, "pa_decode_step_prepare_rows", n_seqs, seq_ids, max_blocks,
+                               slot_mapping_out, ctx_lens_out, tables_out, row_versions,
+                               copies_out, copies_cap, n_copies_out);
 }
 
 int pa_alloc_slots_n(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
@@ -675,6 +716,7 @@ int pa_alloc_slots_n(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
         for (int32_t t = 0; t < counts[i]; ++t) {
             if (s.table.empty() || pool->last_filled(s) == B) {
                 s.table.push_back(pool->pop_free());
+                s.tver = next_table_version();
             } else if (t == 0 && pool->ref[(size_t)s.table.back()] > 1) {
                 const int32_t last = s.table.back();
                 const int32_t nb = pool->pop_free();
@@ -683,6 +725,7 @@ int pa_alloc_slots_n(pa_pool *pool, int32_t n_seqs, const int32_t *seq_ids,
                 ++c;
                 --pool->ref[(size_t)last];
                 s.table.back() = nb;
+                s.tver = next_table_version();
             }
             const int32_t off = s.num_tokens - (int32_t)(s.table.size() - 1) * B;
             slot_mapping_out[o++] = (int64_t)s.table.back() * B + off;

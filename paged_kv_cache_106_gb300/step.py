@@ -3,10 +3,11 @@
 Per step (vLLM paper review, mz-moonzoo.tistory.com/116, §4.3 global
 execution loop; §4.6: the scheduler hands block tables to the worker):
 
-1. ``pa_decode_step_prepare`` host block manager, one call: one slot per
-                           sequence, the copy-on-write pairs, then the
-                           batch's tables and context lengths, written
-                           straight into the pinned staging buffer;
+1. ``pa_decode_step_prepare_rows`` host block manager, one call: one slot
+                           per sequence, the copy-on-write pairs, then the
+                           batch's context lengths and the table rows that
+                           changed since that staging buffer last held them,
+                           written straight into the pinned staging buffer;
 2. one pinned host -> device copy carrying slot mapping, context lengths,
    block tables and copy pairs (double-buffered staging, so the host can
    prepare step t+1 while the GPU still runs step t);
@@ -24,7 +25,7 @@ import time
 import numpy as np
 import torch
 
-from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_prepare_into,
+from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_prepare_rows_into,
                pa_decode_workspace_bytes, pa_write_kv)
 
 
@@ -52,6 +53,9 @@ class DecodeStepRunner:
         self.host = [torch.empty(self.nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
         self.host_addr = [h.data_ptr() for h in self.host]
         self.host_ctx = [self._views(h)[1] for h in self.host]
+        # per staging buffer: the table version each of its rows holds (0: none)
+        self.row_versions = [np.zeros(S, np.uint64) for _ in range(2)]
+        self.row_versions_addr = [v.ctypes.data for v in self.row_versions]
         self._n_copies = ctypes.c_int32(0)
         self.events = [None, None]
         self.dev = torch.empty(self.nbytes, dtype=torch.uint8, device=self.device)
@@ -88,9 +92,10 @@ class DecodeStepRunner:
                 self.ids.shape[0] != self.S:
             raise ValueError("ids must be a contiguous int32 array of the batch size")
         base = self.host_addr[k]
-        n_cp = pa_decode_step_prepare_into(
+        n_cp = pa_decode_step_prepare_rows_into(
             self.pool, self.S, self.ids.ctypes.data, self.max_blocks, base + self.off_slots,
-            base + self.off_ctx, base + self.off_tab, base + self.off_cp, self.S, self._n_copies)
+            base + self.off_ctx, base + self.off_tab, self.row_versions_addr[k], base + self.off_cp,
+            self.S, self._n_copies)
         self.host_seconds = time.perf_counter() - t0   # block manager work of this step
         self._pending = (k, n_cp, self.host_ctx[k])
 

@@ -3,6 +3,7 @@ against the pages' worked examples and, operation by operation, against the
 oracle's block manager: slots, copy pairs, block tables, token counts,
 reference counts and the free queue must be identical (bit-exact indexing)."""
 import copy
+import ctypes
 import random
 import re
 import subprocess
@@ -11,7 +12,7 @@ import numpy as np
 import pytest
 
 import paged_kv_cache_106_gb300 as pk
-from oracle.alloc import BlockManager, OutOfBlocks
+from oracle.alloc import BlockManager, OutOfBlocks, move_group
 from tests.allocator_replay import load, replay
 from tests.conftest import ROOT
 
@@ -242,6 +243,103 @@ def test_fused_step_call_lockstep_with_oracle(seed):
                         assert tables.tolist() == m.padded_tables(seqs, mb)
                         assert ctx.tolist() == [m.num_tokens(s) for s in seqs]
         _compare(abi, m, live)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_row_skipping_step_call_keeps_every_row_current(seed):
+    """pa_decode_step_prepare_rows into two staging buffers used in turn, as a
+    serving loop uses them, while the batch's rows are replaced (free + add,
+    sometimes under the freed id again), forked into, and swapped out and back
+    in: after every call every row of the buffer it wrote equals the oracle's
+    padded table (rows it skipped included), and slots, copy pairs and
+    lengths match the oracle's append."""
+    rng = random.Random(7000 + seed)
+    B = rng.choice([1, 2, 4, 16])
+    S = rng.randint(1, 10)
+    MB = 10
+    nb = S * (MB + 4)
+    order = list(range(nb))
+    rng.shuffle(order)
+    gpu = pk.pa_pool_create(pk.PoolDesc(nb, B, free_order=order))
+    cpu = pk.pa_pool_create(pk.PoolDesc(nb, B, free_order=list(range(nb))))
+    m, mc = BlockManager(nb, B, order), BlockManager(nb, B, list(range(nb)))
+    ids = np.arange(S, dtype=np.int32)
+    nxt = S
+    for s in ids.tolist():
+        n = rng.randint(1, 3 * B)
+        m.add(s, n)
+        pk.pa_seq_add(gpu, s, n, want_slots=False)
+    bufs = [np.full((S, MB), -7, np.int32) for _ in range(2)]
+    vers = [np.zeros(S, np.uint64) for _ in range(2)]
+    slots = np.empty(S, np.int64)
+    ctx = np.empty(S, np.int32)
+    copies = np.empty((S, 2), np.int32)
+    ncp = ctypes.c_int32()
+
+    def replace(i, same_id):
+        nonlocal nxt
+        old = int(ids[i])
+        m.free(old)
+        pk.pa_seq_free(gpu, old)
+        new = old if same_id else nxt
+        nxt += 0 if same_id else 1
+        n = rng.randint(1, 3 * B)
+        m.add(new, n)
+        pk.pa_seq_add(gpu, new, n, want_slots=False)
+        ids[i] = new
+
+    for step in range(160):
+        i = rng.randrange(S)
+        r = rng.random()
+        if r < 0.15:
+            replace(i, rng.random() < 0.3)
+        elif r < 0.25 and S > 1:
+            j = rng.randrange(S)
+            if j != i:
+                old = int(ids[i])
+                m.free(old)
+                pk.pa_seq_free(gpu, old)
+                m.fork(int(ids[j]), nxt)
+                pk.pa_seq_fork(gpu, int(ids[j]), nxt)
+                ids[i] = nxt
+                nxt += 1
+        elif r < 0.35:
+            s = int(ids[i])
+            try:
+                exp_out = move_group(m, mc, [s])
+            except ValueError:                       # a block shared outside the row
+                pass
+            else:
+                assert [tuple(p) for p in pk.pa_swap_out(gpu, cpu, [s]).tolist()] == exp_out
+                exp_in = move_group(mc, m, [s])
+                assert [tuple(p) for p in pk.pa_swap_in(cpu, gpu, [s]).tolist()] == exp_in
+        for i2 in range(S):                          # keep every table inside the rows
+            if len(m.block_table(int(ids[i2]))) >= MB:
+                replace(i2, False)
+        k = step & 1
+        exp_slots, exp_copies = m.alloc_slots(ids.tolist())
+        n_cp = pk.pa_decode_step_prepare_rows_into(
+            gpu, S, ids.ctypes.data, MB, slots.ctypes.data, ctx.ctypes.data, bufs[k].ctypes.data,
+            vers[k].ctypes.data, copies.ctypes.data, S, ncp)
+        assert slots.tolist() == exp_slots, step
+        assert [tuple(c) for c in copies[:n_cp].tolist()] == exp_copies, step
+        assert ctx.tolist() == [m.num_tokens(int(s)) for s in ids], step
+        assert bufs[k].tolist() == m.padded_tables(ids.tolist(), MB), step
+    pk.pa_pool_destroy(gpu)
+    pk.pa_pool_destroy(cpu)
+
+
+def test_row_skipping_step_call_refuses_a_null_versions_array():
+    p = pk.pa_pool_create(pk.PoolDesc(8, 4))
+    pk.pa_seq_add(p, 0, 3, want_slots=False)
+    ids = np.zeros(1, np.int32)
+    slots, ctx, tab, cps = np.empty(1, np.int64), np.empty(1, np.int32), np.empty(4, np.int32), np.empty(2, np.int32)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_decode_step_prepare_rows_into(p, 1, ids.ctypes.data, 4, slots.ctypes.data, ctx.ctypes.data,
+                                            tab.ctypes.data, 0, cps.ctypes.data, 1, ctypes.c_int32())
+    assert e.value.code == pk.PA_ERR_INVALID_ARG
+    assert pk.pa_seq_info(p, 0) == (3, 1)                  # nothing appended
+    pk.pa_pool_destroy(p)
 
 
 def test_abi_error_codes_and_no_partial_change():
