@@ -569,8 +569,9 @@ def run_ours(args):
                     "admission_us_per_step": 1e6 * sum(a for a, _ in host_s) / len(host_s),
                     "step_prepare_us_per_step": 1e6 * sum(b for _, b in host_s) / len(host_s),
                     "note": "host wall clock per step: free/admit finished sequences, then "
-                            "pa_decode_step_prepare (one token per sequence, tables and lengths "
-                            "into the pinned staging buffer); waits on the GPU excluded",
+                            "pa_decode_step_prepare_rows (one token per sequence, lengths and "
+                            "the changed table rows into the pinned staging buffer); waits on the "
+                            "GPU excluded",
                 },
             },
             "e2e": {
