@@ -17,7 +17,8 @@
 //       warps 0-7 / 8-15  softmax and epilogue of slot 0 / 1: warps w and
 //                  w + 4 share the query rows of tensor-memory lane quarter
 //                  w % 4, each half of a tile's key columns, and meet once per
-//                  tile (a named barrier per slot) to combine row maxima;
+//                  tile (a named barrier of the two warps) to combine row
+//                  maxima;
 //       warp 16    one thread issues every tcgen05.mma and commit, in the
 //                  order P V (slot 0), Q K^T of the next key tile (slot 0),
 //                  then the same for slot 1, so one slot's products run on
@@ -671,9 +672,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- softmax and epilogue: warps 8x .. 8x + 7 serve slot x.  Warps w and
         // w + 4 of the slot share the query rows of tensor-memory lane quarter
         // w % 4; the first takes key columns 0-63 of each tile, the second
-        // 64-127, and they meet once per tile (a named barrier per slot) to
+        // 64-127, and they meet once per tile (a named barrier of the two) to
         // combine their row maxima.  The slot's warps leave their loops only
-        // together, at a meeting.  A job's output is written at the start of
+        // together, at the vote that starts each unit.  A job's output is written at the start of
         // the slot's next job, when its O is complete (that job's first S was
         // committed after the last P V of the previous one), or after the last.
         const int x = warp >> 3, quarter = warp & 3, half = (warp >> 2) & 1;
@@ -682,8 +683,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t sb = lane_base + x * 128 + half * 64;
         const uint32_t ob = lane_base + kOCol + x * 128 + half * (D / 2);
         const int meet = 1 + x;   // named barrier of the slot (0 is __syncthreads)
+        const int pair = 3 + 4 * x + quarter;   // named barrier of warps w and w + 4
         const float qs = p.qscale;
-        bool ok = true, stop = false;
+        bool ok = true;
         int sc = 0, job = 0;     // S tiles and jobs of this slot so far
         bool pend = false;       // the previous job's output is still in O
         float pend_l = 0.f;
@@ -786,13 +788,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 bars.red[x][sc & 1][half][row] = mt;
                 if (t == 0 && pend) bars.red_l[x][half][row] = pend_l;
-                // the two halves of each row meet: one exit decision for the slot's
-                // warps, the partner's maximum (and, on a job's first tile, the
-                // partner's sum for the pending output)
-                if (!group_all(meet, 256, ok)) {
-                    stop = true;
-                    break;
-                }
+                // the two halves of each row meet (a barrier of the two warps): the
+                // partner's maximum (and, on a job's first tile, the partner's sum
+                // for the pending output).  A failed wait in either makes both
+                // skip the rest of the unit's work, meeting at each tile still;
+                // the slot's warps leave together at the next unit
+                ok = group_all(pair, 64, ok);
+                if (!ok) continue;
                 mt = fmaxf(mt, bars.red[x][sc & 1][half ^ 1][row]);
                 float corr = 1.f;
                 const bool resc = mt > m_run + kRescaleLog2;
@@ -882,7 +884,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     epi_store(hv);
                 }
             }
-            if (stop) break;
             pend = true;
             pend_l = l_run;
             pend_out = qi < u.ql ? reinterpret_cast<unsigned long long>(
@@ -891,7 +892,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ++job;
         }
         // the last job's output, once its last P V is done
-        if (!stop && pend) {
+        if (pend) {
             ok = ok && warp_all(mbar_wait_bounded(bar(bars.o_full, x), (job - 1) & 1, p.status, true));
             bars.red_l[x][half][row] = pend_l;
             if (group_all(meet, 256, ok)) {
