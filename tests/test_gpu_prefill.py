@@ -99,18 +99,26 @@ def test_prefill_matches_oracle(D, B):
     _check(got, ref)
 
 
-@pytest.mark.parametrize("factor", [4.0, 0.25])
-def test_prefill_scores_that_jump_on_a_later_tile(factor):
-    """Keys at positions 256-383 scaled by `factor`: with 4, the rows that
-    reach them see their maximum jump far past the running one on a later,
-    unmasked key tile (the lazy rescale of O and of the probabilities of that
-    tile must take place); with 1/4, the maximum stays where it was."""
+@pytest.mark.parametrize("factor,lo,hi", [(4.0, 256, 384), (0.25, 256, 384), (8.0, 256, 384),
+                                          (8.0, 288, 320), (16.0, 330, 340)])
+def test_prefill_scores_that_jump_on_a_later_tile(factor, lo, hi):
+    """Keys at positions lo..hi-1 (inside the third key tile) scaled by
+    `factor`.  With 4 the rows that reach them see their maximum jump past
+    the running one by about 2^11 on a later, unmasked key tile (the lazy
+    rescale of O); with 1/4 the maximum stays where it was.  With 8 and 16
+    the jump passes 2^15, what fp16 probabilities computed against the
+    running maximum could hold: over the whole tile a chunk's maximum is past
+    it before any of the tile's P is written, and the two halves of a row end
+    with different references; over keys 288-319 only the second 32-key
+    chunk of the first half jumps, after the first chunk's P is written, and
+    the second half must take its partner's higher reference; over keys
+    330-339 the jump is inside one chunk of the second half."""
     rng = np.random.default_rng(77)
     H, D, B = 2, 128, 16
     ctx = [520, 400]
     q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ctx, H, D, B)
     for s in range(len(ctx)):
-        for p in range(256, min(384, ctx[s])):
+        for p in range(lo, min(hi, ctx[s])):
             kc[tables[s][p // B], :, p % B, :] = (kc[tables[s][p // B], :, p % B, :].astype(np.float32)
                                                  * factor).astype(np.float16)
     scale = float(np.float32(1 / math.sqrt(D)))
