@@ -404,9 +404,14 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
  * below the fp16 rounding of the output.
  * Device-side problems go to *status and leave that sequence's rows
  * unwritten: PA_ERR_INVALID_ARG for q_len < 0, q_len > ctx,
- * q_len > max_q_len or rows outside [0, q_rows); PA_ERR_BAD_BLOCK for ctx > max_blocks * B or a table
- * entry outside the pool (that entry is not read and the sequence's output
- * is unspecified).
+ * q_len > max_q_len or rows outside [0, q_rows); PA_ERR_BAD_BLOCK for
+ * ctx > max_blocks * B or a table entry outside the pool (that entry is not
+ * read and the sequence's output is unspecified).
+ * Work is balanced across the GPU through a unit counter in the library's
+ * device memory that each launch sets back to zero when it ends; calls take
+ * the library's 64 counters in turn, so up to 64 calls may be in flight at
+ * once on different streams (a captured call replayed from a CUDA graph
+ * reuses its counter, which its previous replay left at zero).
  * Errors: PA_ERR_INVALID_ARG (geometry, sizes, NULL or misaligned
  * pointers), PA_ERR_CUDA. */
 int pa_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
