@@ -306,6 +306,7 @@ def run_ours(args):
     batch = SteadyBatch(pk, pool, w, np.random.default_rng(w.seed + 7 + rank))
     merge = pk.pa_decode_workspace_bytes(S, max_blocks, desc) > 0
     bytes_fixed = S * H * D * 2 * 2       # q read + o written
+    bytes_new = S * H * D * 2 * 4         # the new tokens' K and V read and stored in the cache
 
     dump = [] if args.dump_steps else None
 
@@ -324,22 +325,20 @@ def run_ours(args):
             nblk_d = (ctx + B - 1) // B
             dump.append({"tokens": int(ctx.sum()),
                          "attn_bytes": int(ctx.sum()) * H * D * 4 + int(nblk_d.sum()) * 4
-                         + S * 4 + bytes_fixed})
+                         + S * 4 + bytes_fixed + bytes_new})
         runner.copy_blocks([kc], [vc])
         if ev_pair is not None:
-            ev_pair[2].record(stream)
-        runner.write_kv(k_new, v_new, kc, vc)
-        if ev_pair is not None:
             ev_pair[0].record(stream)
-        runner.attention(out, q, kc, vc, w.scale)
+        # the new tokens' slot write inside the attention launch
+        runner.step_attention(out, q, k_new, v_new, kc, vc, w.scale)
         if ev_pair is not None:
             ev_pair[1].record(stream)
         if stats is not None:
             stats["tokens"] += int(ctx.sum())
             nblk = (ctx + B - 1) // B
             stats["attn_bytes"] += int(ctx.sum()) * H * D * 2 * 2 + int(nblk.sum()) * 4 + S * 4 \
-                + bytes_fixed
-            stats["launches"] += 2 + (1 if merge else 0) + (1 if n_cp else 0)
+                + bytes_fixed + bytes_new
+            stats["launches"] += 1 + (1 if merge else 0) + (1 if n_cp else 0)
             stats["copies"] += n_cp
 
     with torch.cuda.stream(stream):
@@ -352,7 +351,7 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
     stats = {"tokens": 0, "attn_bytes": 0, "launches": 0, "copies": 0}
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2))
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -372,7 +371,6 @@ def run_ours(args):
             json.dump({"warmup": args.warmup, "steps": dump}, f)
     elapsed = t0.elapsed_time(t1) / 1e3
     attn_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    write_ms = [e[2].elapsed_time(e[0]) for e in evs]
     copy_stats = time_copy_blocks(pk, pool, desc, w, kc, vc, stream) if rank == 0 else None
     # the step's slot write alone, 50 launches back to back between two events
     # (inside the step loop each launch also carries its own events)
@@ -448,8 +446,7 @@ def run_ours(args):
         runner.upload()
         n_tok = int(runner.ctx_host.sum())
         runner.copy_blocks([kc], [vc])
-        runner.write_kv(kk, vv, kc, vc)
-        runner.attention(oo, qq, kc, vc, w.scale)
+        runner.step_attention(oo, qq, kk, vv, kc, vc, w.scale)
         ev["comp"][sidx].record(stream)
         s_out.wait_event(ev["comp"][sidx])
         with torch.cuda.stream(s_out):
@@ -553,13 +550,13 @@ def run_ours(args):
             "kernels": {
                 "pa_write_kv": {
                     "us_per_launch": write_b2b_us,
-                    "us_in_step_loop": 1e3 * sum(write_ms) / len(write_ms),
                     "algorithmic_bytes": 2 * 2 * S * H * D * 2 + 8 * S,
                     "GB/s": (2 * 2 * S * H * D * 2 + 8 * S) / (write_b2b_us / 1e6) / 1e9,
-                    "note": "new K/V of the batch read and scattered to their slots; us_per_launch: 50 "
-                            "launches back to back between two CUDA events (launch gaps included); "
-                            "us_in_step_loop: between the events around the launch inside the timed "
-                            "step loop, which also holds the events' own cost and any wait for the host",
+                    "in_step": "none: the timed decode step stores its new tokens inside the "
+                               "attention launch (pa_decode_step_attention)",
+                    "note": "the separate slot write of the batch's new K/V (what a caller of "
+                            "pa_write_kv runs): 50 launches back to back between two CUDA events, "
+                            "launch gaps included",
                 },
                 **extra,
                 "pa_copy_blocks": copy_stats,
@@ -678,17 +675,16 @@ def run_full40(args, quiet: bool = False):
         ctx = runner.ctx_host.astype(np.int64)
         runner.copy_blocks(kcs, vcs)
         for l in range(L):
-            runner.write_kv(k_new, v_new, kcs[l], vcs[l])
             if evs is not None:
                 evs[l][0].record(stream)
-            runner.attention(out, q, kcs[l], vcs[l], w.scale)
+            runner.step_attention(out, q, k_new, v_new, kcs[l], vcs[l], w.scale)
             if evs is not None:
                 evs[l][1].record(stream)
         if stats is not None:
             nblk = (ctx + B - 1) // B
             stats["tokens"] += int(ctx.sum()) * L
             stats["attn_bytes"] += L * (int(ctx.sum()) * H * D * 4 + int(nblk.sum()) * 4 + S * 4
-                                        + S * H * D * 4)
+                                        + S * H * D * 4 + S * H * D * 8)
             stats["copies"] += runner.n_copies
 
     with torch.cuda.stream(stream):
@@ -808,16 +804,15 @@ def decode_b64_stats(dev, steps: int = 200, warmup: int = 5) -> dict:
             runner.prepare()
             ctx = runner.ctx_host.astype(np.int64)
             runner.copy_blocks([kc], [vc])
-            runner.write_kv(k_new, v_new, kc, vc)
             j = i - warmup
             if j >= 0:
                 evs[j][0].record(stream)
-            runner.attention(out, q, kc, vc, w.scale)
+            runner.step_attention(out, q, k_new, v_new, kc, vc, w.scale)
             if j >= 0:
                 evs[j][1].record(stream)
                 tokens += int(ctx.sum())
                 nbytes += int(ctx.sum()) * H * D * 4 + int(((ctx + B - 1) // B).sum()) * 4 \
-                    + S * 4 + S * H * D * 4
+                    + S * 4 + S * H * D * 4 + S * H * D * 8
     torch.cuda.synchronize()
     assert runner.status.item() == 0, runner.status.item()
     ms = sum(a.elapsed_time(b) for a, b in evs) / steps
@@ -880,9 +875,8 @@ def parallel_sampling_stats(dev) -> dict:
                 tables = runner._views(runner.host[(runner.i - 1) & 1])[2]
                 evs[i][0].record(stream)
                 runner.copy_blocks([kc], [vc])
-                runner.write_kv(k_new, v_new, kc, vc)
                 evs[i][1].record(stream)
-                runner.attention(out, q, kc, vc, w.scale)
+                runner.step_attention(out, q, k_new, v_new, kc, vc, w.scale)
                 evs[i][2].record(stream)
                 copies += runner.n_copies
                 tokens += int(ctx.sum())
@@ -903,8 +897,8 @@ def parallel_sampling_stats(dev) -> dict:
                "unique_GB/s": unique / n / (attn_ms / 1e3) / 1e9,
                "unique_bytes_per_step": unique / n,
                "l2_resident": True,
-               "note": "GPU time of the step's kernels (copy-on-write copies, slot write, "
-                       "attention); logical bytes count shared blocks once per reading "
+               "note": "GPU time of the step's kernels (copy-on-write copies, then the slot "
+                       "write and attention in one call); logical bytes count shared blocks once per reading "
                        "sequence, unique bytes once (whole blocks); the samples' re-reads of "
                        "shared blocks hit L2, so this is not an HBM roofline"}
         pk.pa_pool_destroy(pool)
@@ -963,8 +957,7 @@ def run_beam_churn(args, quiet: bool = False):
         h1 = time.perf_counter()
         ctx = runner.ctx_host.astype(np.int64)
         runner.copy_blocks([kc], [vc])
-        runner.write_kv(k_new, v_new, kc, vc)
-        runner.attention(out, q, kc, vc, 1 / math.sqrt(D))
+        runner.step_attention(out, q, k_new, v_new, kc, vc, 1 / math.sqrt(D))
         h2 = time.perf_counter()
         f, fr = bg.prune(next(draws))
         h3 = time.perf_counter()

@@ -376,6 +376,32 @@ int pa_decode_attention(void *out, const void *q, const void *k_cache, const voi
                         int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
                         int32_t *status, const pa_pool_desc *desc, void *stream);
 
+/* One decode step's slot write and attention in one call ([review] §5.1 (1)
+ * fused reshape and block write; §4.3 decoding): for every sequence s <
+ * n_seqs, the step's new key and value rows k_new[s], v_new[s] (device,
+ * [n_seqs][num_heads][head_dim] fp16, 16-byte aligned) are stored at
+ * slot_mapping[s] (device, n_seqs int64, the slot pa_alloc_slots /
+ * pa_decode_step_prepare returned for the token), exactly as pa_write_kv
+ * with one token per sequence, and then attention runs as
+ * pa_decode_attention (same arguments and workspace), the new token
+ * included.  Where the persistent decode kernel runs (batches whose
+ * per-sequence plan fits its shared memory) the write happens inside it: the
+ * unit that reads a sequence's last context block first stores the new rows
+ * into it, so the step takes one launch fewer; otherwise the slot write runs
+ * as its own launch first, on the same stream.
+ * slot_mapping[s] must be the slot of position ctx_lens[s] - 1 (the token
+ * just appended); the in-kernel write checks it against the block table and
+ * reports PA_ERR_INVALID_ARG in *status (writing nothing) when it is not.  A
+ * negative slot skips the sequence's write, as in pa_write_kv.
+ * Errors: as pa_decode_attention; PA_ERR_INVALID_ARG also for NULL or
+ * misaligned k_new, v_new or slot_mapping. */
+int pa_decode_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                             const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                             const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,
+                             int32_t max_blocks, float scale, void *workspace,
+                             size_t workspace_bytes, int32_t *status, const pa_pool_desc *desc,
+                             void *stream);
+
 /* Causal paged prefill attention ([review] §4.3, the prompt phase: the
  * prompt's tokens are processed together, each attending to the tokens
  * before it and itself; [notes] §3.1 blockwise attention equation, applied

@@ -97,6 +97,8 @@ def _load():
         "pa_decode_workspace_bytes": (sz, [i32, i32, P(pa_pool_desc)]),
         "pa_decode_attention": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float, vp, sz,
                                       vp, P(pa_pool_desc), vp]),
+        "pa_decode_step_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
+                                           ctypes.c_float, vp, sz, vp, P(pa_pool_desc), vp]),
         "pa_decode_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, i32, i32, ctypes.c_float,
                                               vp, P(pa_pool_desc), vp]),
         "pa_prefill_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -452,6 +454,22 @@ def pa_decode_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, scale:
                                     _dev(block_tables), _dev(ctx_lens), n, mb,
                                     ctypes.c_float(scale), _dev(workspace), ws_bytes,
                                     _dev(status), desc.ref, _stream(stream)))
+
+
+def pa_decode_step_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                             ctx_lens, scale: float, desc: PoolDesc, workspace=None, status=None,
+                             stream=None, n_seqs: int | None = None,
+                             max_blocks: int | None = None) -> None:
+    """The step's slot write (one new token per sequence, at slot_mapping[s])
+    and decode attention in one call."""
+    n = int(q.shape[0]) if n_seqs is None else int(n_seqs)
+    mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.pa_decode_step_attention(_dev(out), _dev(q), _dev(k_new), _dev(v_new),
+                                         _dev(slot_mapping), _dev(k_cache), _dev(v_cache),
+                                         _dev(block_tables), _dev(ctx_lens), n, mb,
+                                         ctypes.c_float(scale), _dev(workspace), ws_bytes,
+                                         _dev(status), desc.ref, _stream(stream)))
 
 
 def pa_prefill_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, q_starts,

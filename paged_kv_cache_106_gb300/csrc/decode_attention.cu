@@ -99,6 +99,12 @@ struct DecodeParams {
     int32_t part_blocks;
     int32_t max_parts;
     float qscale;      // scale * log2(e)
+    // optional slot write of the step's new token (persistent kernel): k_new /
+    // v_new rows [n_seqs][H][D], slots[s] the slot of position ctx_lens[s] - 1
+    // (NULL: no write)
+    const __half *k_new;
+    const __half *v_new;
+    const int64_t *slots;
 };
 
 // ---------------------------------------------------------------- block math
@@ -285,6 +291,9 @@ paged_decode_persistent(const DecodeParams p) {
     constexpr int STAGES = L::STAGES, STAGE = L::STAGE, CHUNK = G::CHUNK;
     constexpr int QVEC = GH * D / 8;                  // 16-byte pieces of a unit's q rows
     constexpr int QPL = (QVEC + 31) / 32;             // ... per producer lane
+    // the step's new token is written here when its rows take one vector per
+    // lane (else the launcher runs the slot write first)
+    constexpr bool kWrite = QPL == 1;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -409,6 +418,8 @@ paged_decode_persistent(const DecodeParams p) {
         struct Pending {
             int ticket, s, h0, nh, part, ctx, n_parts, j0, nb, tbl;
             uint4 q[QPL];
+            int64_t wslot;          // the new token's slot (-1: nothing to write)
+            uint4 kw, vw;           // this lane's piece of its key and value rows
         };
         // Decode a ticket (shared memory only) and start the loads of its
         // context length, q rows and first 32 table entries (lane t: entry
@@ -419,8 +430,10 @@ paged_decode_persistent(const DecodeParams p) {
             u.ticket = ticket;
             u.s = u.h0 = u.nh = u.part = u.ctx = u.n_parts = u.j0 = u.nb = 0;
             u.tbl = -1;
+            u.wslot = -1;
 #pragma unroll
             for (int k = 0; k < QPL; ++k) u.q[k] = make_uint4(0, 0, 0, 0);
+            u.kw = u.vw = make_uint4(0, 0, 0, 0);
             if (ticket >= n_units) return u;
             const int gp = ticket / HG;
             const int hg = ticket - gp * HG;
@@ -451,6 +464,17 @@ paged_decode_persistent(const DecodeParams p) {
 #pragma unroll
             for (int k = 0; k < QPL; ++k)
                 if (lane + 32 * k < u.nh * (D / 8)) u.q[k] = qsrc[lane + 32 * k];
+            if (kWrite && p.slots && gp >= n_full) {
+                // a context's last partition holds the step's new token: this
+                // unit writes its heads' key and value rows (loaded now, stored
+                // before the copy of the block that holds them)
+                u.wslot = p.slots[lo];
+                const size_t row = ((size_t)lo * H + u.h0) * (D / 8) + lane;
+                if (lane < u.nh * (D / 8)) {
+                    u.kw = reinterpret_cast<const uint4 *>(p.k_new)[row];
+                    u.vw = reinterpret_cast<const uint4 *>(p.v_new)[row];
+                }
+            }
             return u;
         };
         // blocks of the unit in its partition (needs the context length)
@@ -550,6 +574,26 @@ paged_decode_persistent(const DecodeParams p) {
                         }
                         if (tgt < cur.nb) pf_cur = max(pf_cur, tgt + 1);
                         else if (tn2 < nxt_nb) pf_nxt = max(pf_nxt, tn2 + 1);
+                    }
+                    if (kWrite && b == cur.nb - 1 && cur.wslot >= 0) {
+                        // the new token: its slot must be position ctx - 1, in this
+                        // block; its rows are stored, then fenced against the bulk
+                        // copy below that reads them
+                        const int64_t blk = cur.wslot / B;
+                        const int off = (int)(cur.wslot % B);
+                        if (blk == phys && off == (cur.ctx - 1) % B && phys >= 0 && phys < p.num_blocks) {
+                            __half *kd = const_cast<__half *>(p.k_cache) + ((size_t)phys * H + cur.h0) * B * D + (size_t)off * D;
+                            __half *vd = const_cast<__half *>(p.v_cache) + ((size_t)phys * H + cur.h0) * B * D + (size_t)off * D;
+                            if (lane < cur.nh * (D / 8)) {
+                                const int g = lane / (D / 8), c8 = lane % (D / 8);
+                                reinterpret_cast<uint4 *>(kd + (size_t)g * B * D)[c8] = cur.kw;
+                                reinterpret_cast<uint4 *>(vd + (size_t)g * B * D)[c8] = cur.vw;
+                            }
+                            fence_proxy_async_global();
+                        } else if (lane == 0) {
+                            report(p.status, PA_ERR_INVALID_ARG);
+                        }
+                        __syncwarp();
                     }
                     const int st = i_stage % STAGES;
                     const int use = i_stage / STAGES;
@@ -959,7 +1003,8 @@ template <int D, int B, bool Persistent>
 struct KernelTag {};
 
 template <int D, int B>
-int launch_db(const DecodeParams &prm_in, int part_tokens, cudaStream_t stream) {
+int launch_db(const DecodeParams &prm_in, int part_tokens, const pa_pool_desc *d,
+              cudaStream_t stream) {
     DecodeParams prm = prm_in;
     cudaError_t e;
     using PC = PersistCfg<D, B>;
@@ -995,6 +1040,16 @@ int launch_db(const DecodeParams &prm_in, int part_tokens, cudaStream_t stream) 
         max_seqs[dev] = lo;
         per_sm_full[dev] = base;
     });
+    // the persistent kernel writes the step's new token when a unit's rows
+    // take one vector per producer lane; otherwise the slot write runs first
+    constexpr bool kernel_writes = (PC::GH * D / 8 + 31) / 32 == 1;
+    if (prm.slots && !(kernel_writes && prm.n_seqs <= max_seqs[dev])) {
+        const int rc = launch_write_kv(prm.k_new, prm.v_new, prm.slots, prm.n_seqs,
+                                       const_cast<__half *>(prm.k_cache),
+                                       const_cast<__half *>(prm.v_cache), d, prm.status, stream);
+        if (rc != PA_OK) return rc;
+        prm.slots = nullptr;
+    }
     if (prm.n_seqs <= max_seqs[dev]) {
         auto kern = pkern;
         const int use_smem = (int)L::bytes(prm.n_seqs);
@@ -1032,12 +1087,13 @@ int launch_db(const DecodeParams &prm_in, int part_tokens, cudaStream_t stream) 
 }
 
 template <int D>
-int launch_d(int B, const DecodeParams &prm, int part_tokens, cudaStream_t stream) {
+int launch_d(int B, const DecodeParams &prm, int part_tokens, const pa_pool_desc *d,
+             cudaStream_t stream) {
     switch (B) {
-        case 4: return launch_db<D, 4>(prm, part_tokens, stream);
-        case 8: return launch_db<D, 8>(prm, part_tokens, stream);
-        case 16: return launch_db<D, 16>(prm, part_tokens, stream);
-        case 32: return launch_db<D, 32>(prm, part_tokens, stream);
+        case 4: return launch_db<D, 4>(prm, part_tokens, d, stream);
+        case 8: return launch_db<D, 8>(prm, part_tokens, d, stream);
+        case 16: return launch_db<D, 16>(prm, part_tokens, d, stream);
+        case 32: return launch_db<D, 32>(prm, part_tokens, d, stream);
     }
     return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: unsupported block_size %d", B);
 }
@@ -1062,11 +1118,13 @@ size_t decode_workspace_bytes(int32_t n_seqs, int32_t max_blocks, const pa_pool_
            align256(rows * d->head_dim * sizeof(float));
 }
 
-int launch_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
-                            const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,
-                            int32_t max_blocks, float scale, void *workspace,
-                            size_t workspace_bytes, int32_t *status, const pa_pool_desc *d,
-                            void *stream) {
+namespace {
+
+int launch_decode(void *out, const void *q, const void *k_new, const void *v_new,
+                  const int64_t *slots, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,
+                  int32_t max_blocks, float scale, void *workspace, size_t workspace_bytes,
+                  int32_t *status, const pa_pool_desc *d, void *stream) {
     std::string why;
     if (!d) return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: NULL desc");
     if (!device_geometry_ok(d, &why))
@@ -1083,6 +1141,11 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
         return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: out/q/caches must be 16-byte aligned");
     if (!std::isfinite(scale))
         return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: scale is not finite");
+    if (slots && (!k_new || !v_new || mis16(k_new) || mis16(v_new) ||
+                  (reinterpret_cast<uintptr_t>(slots) & 7)))
+        return fail(PA_ERR_INVALID_ARG,
+                    "pa_decode_step_attention: k_new / v_new NULL or not 16-byte aligned, or "
+                    "slot_mapping not 8-byte aligned");
     const int part_tokens = partition_tokens_of(d);
     const int part_blocks = part_tokens / d->block_size;
     const int mp = max_parts_of(max_blocks, part_blocks);
@@ -1115,16 +1178,44 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
     prm.part_blocks = part_blocks;
     prm.max_parts = mp;
     prm.qscale = scale * kLog2e;
+    prm.k_new = static_cast<const __half *>(k_new);
+    prm.v_new = static_cast<const __half *>(v_new);
+    prm.slots = slots;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (d->head_dim) {
-        case 8: return launch_d<8>(d->block_size, prm, part_tokens, st);
-        case 16: return launch_d<16>(d->block_size, prm, part_tokens, st);
-        case 32: return launch_d<32>(d->block_size, prm, part_tokens, st);
-        case 64: return launch_d<64>(d->block_size, prm, part_tokens, st);
-        case 128: return launch_d<128>(d->block_size, prm, part_tokens, st);
-        case 256: return launch_d<256>(d->block_size, prm, part_tokens, st);
+        case 8: return launch_d<8>(d->block_size, prm, part_tokens, d, st);
+        case 16: return launch_d<16>(d->block_size, prm, part_tokens, d, st);
+        case 32: return launch_d<32>(d->block_size, prm, part_tokens, d, st);
+        case 64: return launch_d<64>(d->block_size, prm, part_tokens, d, st);
+        case 128: return launch_d<128>(d->block_size, prm, part_tokens, d, st);
+        case 256: return launch_d<256>(d->block_size, prm, part_tokens, d, st);
     }
     return fail(PA_ERR_INVALID_ARG, "pa_decode_attention: unsupported head_dim %d", d->head_dim);
+}
+
+}  // namespace
+
+int launch_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, const int32_t *ctx_lens, int32_t n_seqs,
+                            int32_t max_blocks, float scale, void *workspace,
+                            size_t workspace_bytes, int32_t *status, const pa_pool_desc *d,
+                            void *stream) {
+    return launch_decode(out, q, nullptr, nullptr, nullptr, k_cache, v_cache, block_tables,
+                         ctx_lens, n_seqs, max_blocks, scale, workspace, workspace_bytes, status,
+                         d, stream);
+}
+
+int launch_decode_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                 const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 const int32_t *block_tables, const int32_t *ctx_lens,
+                                 int32_t n_seqs, int32_t max_blocks, float scale, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, const pa_pool_desc *d,
+                                 void *stream) {
+    if (n_seqs > 0 && !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_step_attention: NULL slot_mapping");
+    return launch_decode(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                         ctx_lens, n_seqs, max_blocks, scale, workspace, workspace_bytes, status,
+                         d, stream);
 }
 
 }  // namespace pagedkv

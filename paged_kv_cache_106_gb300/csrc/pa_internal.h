@@ -39,6 +39,12 @@ int launch_decode_attention(void *out, const void *q, const void *k_cache, const
                             int32_t max_blocks, float scale, void *workspace,
                             size_t workspace_bytes, int32_t *status, const pa_pool_desc *d,
                             void *stream);
+int launch_decode_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                 const int64_t *slot_mapping, void *k_cache, void *v_cache,
+                                 const int32_t *block_tables, const int32_t *ctx_lens,
+                                 int32_t n_seqs, int32_t max_blocks, float scale, void *workspace,
+                                 size_t workspace_bytes, int32_t *status, const pa_pool_desc *d,
+                                 void *stream);
 int launch_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *block_tables, const int32_t *ctx_lens,
                              const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,

@@ -12,7 +12,9 @@ execution loop; §4.6: the scheduler hands block tables to the worker):
    block tables and copy pairs (double-buffered staging, so the host can
    prepare step t+1 while the GPU still runs step t);
 3. ``pa_copy_blocks``      copy-on-write copies, every layer (only if any);
-4. per layer ``pa_write_kv`` then ``pa_decode_attention``.
+4. per layer ``pa_decode_step_attention``: the new token's slot write and
+   decode attention in one call (one launch where the persistent kernel
+   writes the rows itself).
 
 Everything is enqueued on one stream.  This module only sequences library
 calls and owns the staging buffers; the work runs in libpagedkv.so.
@@ -25,8 +27,8 @@ import time
 import numpy as np
 import torch
 
-from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_prepare_rows_into,
-               pa_decode_workspace_bytes, pa_write_kv)
+from . import (PoolDesc, pa_copy_blocks, pa_decode_attention, pa_decode_step_attention,
+               pa_decode_step_prepare_rows_into, pa_decode_workspace_bytes, pa_write_kv)
 
 
 def _align(x, a=256):
@@ -128,13 +130,18 @@ class DecodeStepRunner:
         pa_decode_attention(out, q, k_cache, v_cache, self.d_tables, self.d_ctx, scale, self.desc,
                             workspace=self.workspace, status=self.status, stream=self.stream)
 
+    def step_attention(self, out, q, k_new, v_new, k_cache, v_cache, scale: float):
+        """The new tokens' slot write and attention of one layer, one call."""
+        pa_decode_step_attention(out, q, k_new, v_new, self.d_slots, k_cache, v_cache,
+                                 self.d_tables, self.d_ctx, scale, self.desc,
+                                 workspace=self.workspace, status=self.status, stream=self.stream)
+
     def step(self, q, k_new, v_new, out, k_caches, v_caches, scale: float):
         """A whole decode step over all layers (lists of per-layer tensors)."""
         self.prepare()
         self.copy_blocks(k_caches, v_caches)
         for l in range(len(k_caches)):
-            self.write_kv(k_new[l], v_new[l], k_caches[l], v_caches[l])
-            self.attention(out[l], q[l], k_caches[l], v_caches[l], scale)
+            self.step_attention(out[l], q[l], k_new[l], v_new[l], k_caches[l], v_caches[l], scale)
 
 
 def admit_workload(pool, w) -> list:
