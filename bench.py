@@ -481,11 +481,16 @@ def run_ours(args):
         extra["decode_opt13b_b64"] = decode_b64_stats(dev)
         extra["parallel_sampling"] = parallel_sampling_stats(dev)
         pb = PrefillBatch(dev)
+        pf_work = (f"causal prefill of {len(pb.lens)} whole prompts (lognormal, median 200, "
+                   f"cap 1536; {pb.T} tokens), OPT-13B layer 40x128, block 16")
+        _, fs_ms = pb.time_fused(20, 3)
+        fs = pb.roofline(fs_ms, fused=True)
+        fs.update({"workload": pf_work + "; the prompts' slot write and attention in one launch",
+                   "launches": 20, "prompt_tokens_per_s": pb.T / (fs_ms / 1e3)})
+        extra["pa_prefill_step_attention"] = fs
         _, pf_ms, pf_wkv_ms = pb.time_steps(20, 3)
         pf = pb.roofline(pf_ms)
-        pf.update({"workload": f"causal prefill of {len(pb.lens)} whole prompts (lognormal, "
-                               f"median 200, cap 1536; {pb.T} tokens), OPT-13B layer 40x128, "
-                               "block 16", "launches": 20,
+        pf.update({"workload": pf_work + "; attention alone (after pa_write_kv)", "launches": 20,
                    "prompt_tokens_per_s": pb.T / (pf_ms / 1e3),
                    "slot_write_us_for_the_prompts": pf_wkv_ms * 1e3})
         extra["pa_prefill_attention"] = pf
@@ -1107,6 +1112,9 @@ class PrefillBatch:
         # bytes the attention must move at least: K and V of every prompt
         # token read, q read, o written, tables and lengths read
         self.unique_bytes = 4 * T * H * D * 2 + int(((lens + B - 1) // B).sum()) * 4 + 12 * len(lens)
+        # the one-call step (pa_prefill_step_attention) also stores every
+        # prompt token's K and V into the cache
+        self.write_bytes = 2 * T * H * D * 2
 
     def write(self, k=None, v=None):
         self.pk.pa_write_kv(self.k_new if k is None else k, self.v_new if v is None else v,
@@ -1118,6 +1126,34 @@ class PrefillBatch:
                                      self.kc, self.vc, self.d_tables, self.d_ctx, self.d_qs,
                                      self.w.scale, self.desc, max_q_len=self.mql,
                                      status=self.status, stream=self.stream)
+
+    def fused(self, q=None, out=None, k=None, v=None):
+        self.pk.pa_prefill_step_attention(
+            self.out if out is None else out, self.q if q is None else q,
+            self.k_new if k is None else k, self.v_new if v is None else v, self.kc, self.vc,
+            self.d_tables, self.d_ctx, self.d_qs, self.w.scale, self.desc, max_q_len=self.mql,
+            status=self.status, stream=self.stream)
+
+    def time_fused(self, steps: int, warmup: int):
+        """The one-call step (slot write and attention in one launch); returns
+        (elapsed s, ms per launch) from CUDA events on the stream."""
+        import torch
+
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):
+                self.fused()
+        torch.cuda.synchronize()
+        evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for i in range(steps):
+            evs[i][0].record(self.stream)
+            self.fused()
+            evs[i][1].record(self.stream)
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        assert self.status.item() == 0, self.status.item()
+        return t0.elapsed_time(t1) / 1e3, sum(a.elapsed_time(b) for a, b in evs) / steps
 
     def time_steps(self, steps: int, warmup: int):
         """Slot write + attention per step; returns (elapsed s, attention ms per
@@ -1146,29 +1182,32 @@ class PrefillBatch:
         wkv_ms = sum(c.elapsed_time(a) for a, _, c in evs) / steps
         return t0.elapsed_time(t1) / 1e3, attn_ms, wkv_ms
 
-    def roofline(self, attn_ms: float) -> dict:
-        """The binding roof of the attention call: the larger of the HBM time
-        of its unique bytes and the tensor time of its causal flops."""
+    def roofline(self, attn_ms: float, fused: bool = False) -> dict:
+        """The binding roof of the attention call (with ``fused``, of the
+        one-call step, whose bytes include the cache writes): the larger of
+        the HBM time of its unique bytes and the tensor time of its causal
+        flops."""
         hbm, hbm_kind = _peaks()
         tf, tf_kind = _tensor_peak()
-        t_hbm = self.unique_bytes / (hbm * 1e9) * 1e3
+        ub = self.unique_bytes + (self.write_bytes if fused else 0)
+        t_hbm = ub / (hbm * 1e9) * 1e3
         t_tc = self.flops / (tf * 1e12) * 1e3
         bound = "hbm" if t_hbm >= t_tc else "tensor"
         if bound == "hbm":
-            achieved, peak, unit = self.unique_bytes / (attn_ms / 1e3) / 1e9, hbm, "GB/s"
+            achieved, peak, unit = ub / (attn_ms / 1e3) / 1e9, hbm, "GB/s"
             kind = f"{hbm_kind} hbm_gbs"
         else:
             achieved, peak, unit = self.flops / (attn_ms / 1e3) / 1e12, tf, "TFLOP/s"
             kind = tf_kind
         return {"bound": bound, "achieved": achieved, "peak": peak, "peak_kind": kind, "unit": unit,
                 "frac": achieved / peak, "ms_per_launch": attn_ms,
-                "unique_bytes_per_launch": self.unique_bytes, "hbm_floor_ms": t_hbm,
+                "unique_bytes_per_launch": ub, "hbm_floor_ms": t_hbm,
                 "algorithmic_flops_per_launch": self.flops, "tensor_floor_ms": t_tc,
                 "tflops": self.flops / (attn_ms / 1e3) / 1e12,
-                "GB/s": self.unique_bytes / (attn_ms / 1e3) / 1e9,
-                **self.traffic()}
+                "GB/s": ub / (attn_ms / 1e3) / 1e9,
+                **self.traffic(fused)}
 
-    def traffic(self) -> dict:
+    def traffic(self, fused: bool = False) -> dict:
         """DRAM bytes per launch from the committed ncu capture of the full
         256-prompt batch (its DRAM bytes over unique bytes, times this batch's
         unique bytes), if it was taken on the current kernel code and this is
@@ -1176,8 +1215,16 @@ class PrefillBatch:
         t = _kernel_traffic(os.path.join(ROOT, "paged_kv_cache_106_gb300", "csrc", "prefill_attention.cu"),
                             "prefill_attention_traffic.json")
         full = t is not None and t.get("prompt_tokens") == self.T
-        return {"kernel": "paged_prefill_tc<128> (pa_prefill_attention)",
-                "traffic": t["traffic_over_algorithmic"] * self.unique_bytes if full else None,
+        if fused:   # the one-call step's kernel, captured on its own
+            t = t.get("fused") if full else None
+            full = t is not None
+            ub = self.unique_bytes + self.write_bytes
+            name = "paged_prefill_tc<128, true> (pa_prefill_step_attention)"
+        else:
+            ub = self.unique_bytes
+            name = "paged_prefill_tc<128, false> (pa_prefill_attention)"
+        return {"kernel": name,
+                "traffic": t["traffic_over_algorithmic"] * ub if full else None,
                 "traffic_over_algorithmic": t["traffic_over_algorithmic"] if full else None,
                 "traffic_from": t["capture"] if full else None}
 
@@ -1186,9 +1233,10 @@ class PrefillBatch:
 
 
 def run_prefill(args):
-    """Prompt phase of the mixed batch: every step writes the K/V of all 256
-    prompts into the pool (pa_write_kv, one slot per prompt token) and runs
-    causal paged prefill attention over them (one OPT-13B layer)."""
+    """Prompt phase of the mixed batch: every step stores the K/V of all 256
+    prompts into the pool and runs causal paged prefill attention over them
+    (one OPT-13B layer), in one call (pa_prefill_step_attention); the same
+    step as two calls (pa_write_kv, pa_prefill_attention) is timed beside it."""
     import torch
 
     ws, rank, local = _dist_env()
@@ -1201,8 +1249,9 @@ def run_prefill(args):
     stream, status = pb.stream, pb.status
     clocks = ClockSampler(local)
     clocks.start()
-    el, attn_ms, wkv_ms = pb.time_steps(args.steps, args.warmup)
+    el, fused_ms = pb.time_fused(args.steps, args.warmup)   # the step: one call
     clk = clocks.stop()
+    el_sep, attn_ms, wkv_ms = pb.time_steps(args.steps, args.warmup)   # the same, as two calls
     # end to end through the same calls: the step's new K/V and queries come
     # from pinned host memory, the output goes back to it
     h_k, h_v, h_q = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
@@ -1234,8 +1283,7 @@ def run_prefill(args):
         stream.wait_event(ev["in"][s])
         if used[s]:
             stream.wait_event(ev["out"][s])    # step i - 2's output has left this set
-        pb.write(kn, vn)
-        pb.attend(qq, oo)
+        pb.fused(qq, oo, kn, vn)
         ev["comp"][s].record(stream)
         s_out.wait_event(ev["comp"][s])
         with torch.cuda.stream(s_out):
@@ -1261,7 +1309,7 @@ def run_prefill(args):
     (tok_all, e2e_tok), (el_max, e2e_max) = reduce_across_ranks(
         [T * args.steps, T * e2e_steps], [el, e2e_s * e2e_steps], dev)
     if rank == 0:
-        roof = pb.roofline(attn_ms)
+        roof = pb.roofline(fused_ms, fused=True)
         line = {
             "metric": PREFILL_METRIC, "value": tok_all / el_max, "unit": PREFILL_UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -1271,10 +1319,14 @@ def run_prefill(args):
                                    "lognormal (median 200, cap 1536), OPT-13B layer 40x128, block 16",
                        "prompt_tokens": T, "pool_blocks": w.num_blocks,
                        "l2": "K/V written and read back per step ~1.7 GB >> 129 MB L2, no flush"},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": args.steps,
             "roofline": roof,
-            "kernels": {"pa_write_kv": {"us_per_launch": wkv_ms * 1e3,
-                                        "tokens": T, "algorithmic_bytes": T * H * D * 2 * 4}},
+            "kernels": {"separate_calls": {
+                            "ms_per_step": el_sep * 1e3 / args.steps,
+                            "prompt_tokens_per_s": T * args.steps / el_sep,
+                            "pa_write_kv_us_per_launch": wkv_ms * 1e3,
+                            "pa_prefill_attention": pb.roofline(attn_ms),
+                            "note": "the same step as pa_write_kv then pa_prefill_attention"}},
             "e2e": {"value": e2e_tok / e2e_max, "unit": PREFILL_UNIT,
                     "h2d_bytes_per_step": 3 * T * H * D * 2, "d2h_bytes_per_step": T * H * D * 2,
                     "steps": e2e_steps, "timing": "wall clock over the loop, after 3 untimed steps; two steps in flight "

@@ -446,6 +446,27 @@ int pa_prefill_attention(void *out, const void *q, const void *k_cache, const vo
                          int32_t max_q_len, int32_t q_rows, float scale, int32_t *status,
                          const pa_pool_desc *desc, void *stream);
 
+/* The prompt phase's slot write and causal prefill attention in one call,
+ * for whole prompts ([review] §4.3 prompt phase; §5.1 (1) fused reshape and
+ * block write): every sequence s must have q_len == ctx_lens[s] (its
+ * prompt, with blocks already allocated through pa_seq_add /
+ * pa_alloc_slots_n), and k_new, v_new (device, [q_rows][num_heads][head_dim]
+ * fp16, 16-byte aligned, finite) hold its keys and values on the same rows as
+ * q.  The result is that of pa_write_kv of those rows into the prompts'
+ * slots (positions 0 .. q_len - 1 through block_tables) followed by
+ * pa_prefill_attention; the kernel reads the keys and values from k_new and
+ * v_new (once per query-tile pair, no read back from the cache) and the unit
+ * that reaches a prompt's last key stores every key tile's blocks into the
+ * cache as it goes.  block_size 8, 16 or 32; other arguments and errors as
+ * pa_prefill_attention; a sequence with q_len != ctx is reported as
+ * PA_ERR_INVALID_ARG in *status (that sequence is neither written nor
+ * attended). */
+int pa_prefill_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, const int32_t *block_tables,
+                              const int32_t *ctx_lens, const int32_t *q_starts, int32_t n_seqs,
+                              int32_t max_blocks, int32_t max_q_len, int32_t q_rows, float scale,
+                              int32_t *status, const pa_pool_desc *desc, void *stream);
+
 /* ---- decode attention without a caller-provided workspace ------------------
  * No counterpart on the pages: this entry point exists for callers that
  * cannot allocate device memory when they run attention -- for instance a

@@ -103,6 +103,8 @@ def _load():
                                               vp, P(pa_pool_desc), vp]),
         "pa_prefill_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                        ctypes.c_float, vp, P(pa_pool_desc), vp]),
+        "pa_prefill_step_attention": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                            i32, ctypes.c_float, vp, P(pa_pool_desc), vp]),
         "pa_selftest_bounded_wait": (i32, [vp, vp]),
     }
     for name, (res, args) in sig.items():
@@ -486,6 +488,22 @@ def pa_prefill_attention(out, q, k_cache, v_cache, block_tables, ctx_lens, q_sta
                                      _dev(block_tables), _dev(ctx_lens), _dev(q_starts), n, mb,
                                      int(max_q_len), rows, ctypes.c_float(scale), _dev(status),
                                      desc.ref, _stream(stream)))
+
+
+def pa_prefill_step_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables, ctx_lens,
+                              q_starts, scale: float, desc: PoolDesc, max_q_len: int, status=None,
+                              stream=None, n_seqs: int | None = None, max_blocks: int | None = None,
+                              q_rows: int | None = None) -> None:
+    """Whole prompts: their keys and values (k_new, v_new, rows as q) stored
+    into their blocks and causal prefill attention over them, one call."""
+    n = int(ctx_lens.shape[0]) if n_seqs is None else int(n_seqs)
+    mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
+    rows = min(int(q.shape[0]), int(out.shape[0])) if q_rows is None else int(q_rows)
+    _check(_lib.pa_prefill_step_attention(_dev(out), _dev(q), _dev(k_new), _dev(v_new),
+                                          _dev(k_cache), _dev(v_cache), _dev(block_tables),
+                                          _dev(ctx_lens), _dev(q_starts), n, mb, int(max_q_len),
+                                          rows, ctypes.c_float(scale), _dev(status), desc.ref,
+                                          _stream(stream)))
 
 
 def pa_selftest_bounded_wait(status, stream=None) -> None:

@@ -115,6 +115,16 @@ int pa_decode_step_attention(void *out, const void *q, const void *k_new, const 
                                         workspace, workspace_bytes, status, desc, stream);
 }
 
+int pa_prefill_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, const int32_t *block_tables,
+                              const int32_t *ctx_lens, const int32_t *q_starts, int32_t n_seqs,
+                              int32_t max_blocks, int32_t max_q_len, int32_t q_rows, float scale,
+                              int32_t *status, const pa_pool_desc *desc, void *stream) {
+    return launch_prefill_step_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                         ctx_lens, q_starts, n_seqs, max_blocks, max_q_len, q_rows,
+                                         scale, status, desc, stream);
+}
+
 int pa_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_tables, const int32_t *ctx_lens,
                          const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,

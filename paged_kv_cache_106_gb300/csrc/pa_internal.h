@@ -51,4 +51,10 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
                              int32_t max_q_len, int32_t q_rows, float scale, int32_t *status,
                              const pa_pool_desc *d, void *stream);
 
+int launch_prefill_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const int32_t *block_tables,
+                                  const int32_t *ctx_lens, const int32_t *q_starts, int32_t n_seqs,
+                                  int32_t max_blocks, int32_t max_q_len, int32_t q_rows,
+                                  float scale, int32_t *status, const pa_pool_desc *d, void *stream);
+
 }  // namespace pagedkv

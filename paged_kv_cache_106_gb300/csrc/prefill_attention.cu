@@ -181,6 +181,7 @@ constexpr int TBM = 128;          // queries per query tile (= tensor-memory lan
 constexpr int TBN = 128;          // key positions per key tile
 constexpr int NSK = 2;            // K ring stages
 constexpr int NSV = 2;            // V ring stages
+static_assert(NSK == NSV, "the K and V rings advance together");
 constexpr int NU = 4;             // unit descriptors in flight
 constexpr int kLookahead = 2;     // units a block takes before its readers have fetched them all
 // warps 0-7: softmax and epilogue of slot 0, 8-15: of slot 1
@@ -231,6 +232,12 @@ struct Unit {
 // [rows][H][D] tensor with one box of 128 rows.
 struct TcMaps {
     CUtensorMap k, v, v_part[kVPartMaps], q;
+    // whole prompts written and attended in one call: the new keys and values
+    // as 3-D [rows][H][D] tensors (boxes of 128 rows, like q), and the cache as
+    // rows of D values with a box of 64 x B (one store per block and panel);
+    // a prompt's last, partial block is stored in boxes of 8, 4, 2 and 1 rows
+    // (v_part for values, k_part for keys)
+    CUtensorMap kn, vn, ks, vs, k_part[kVPartMaps];
 };
 
 struct TcBars {
@@ -283,13 +290,34 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// Persistent: one CTA per SM walks the units v = blockIdx.x + i * gridDim.x
-// of the list ordered by sequence, then query-tile pair (the last, with the
-// most keys, first), then head; a scheduler warp skips the empty ones.  All
-// heads of a pair run side by side on different SMs (different keys and
-// values), and the next pair of the same (sequence, head), which re-reads a
-// prefix of its keys and values, follows while they are still in L2.
-template <int D>
+// 2-D tensor copy shared -> global (box of the tensor map at element
+// coordinates x, y), in this thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Waits until every bulk group of this thread is complete (its writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Persistent: one CTA per SM takes units one at a time from the launch's
+// counter, in the order sequence, then query-tile pair (the last, with the
+// most keys, first), then head.  All heads of a pair run side by side on
+// different SMs (different keys and values), and the next pair of the same
+// (sequence, head), which re-reads a prefix of its keys and values, follows
+// while they are still in L2.
+// KN: every sequence is a whole prompt whose keys and values are read from
+// the new rows (k_new, v_new) instead of the cache, and the unit that reaches
+// a prompt's last key also stores every key tile's blocks into the cache
+// (the prompt's slot write, done in the same pass).
+template <int D, bool KN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_prefill_tc(const PrefillParams p, const __grid_constant__ TcMaps maps, int32_t n_seqs) {
     using L = TcLayout<D>;
@@ -381,7 +409,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 unsigned long long n = 0;
                 if (s < n_seqs) {
                     const int q_beg = p.q_starts[s], ql = p.q_starts[s + 1] - q_beg, ctx = p.ctx_lens[s];
-                    const bool bad_len = ql < 0 || ql > ctx || ql > p.max_q_len || q_beg < 0 ||
+                    // KN: whole prompts only (their keys and values are the new rows)
+                    const bool bad_len = ql < 0 || ql > ctx || (KN && ql != ctx) || ql > p.max_q_len || q_beg < 0 ||
                                          (int64_t)q_beg + ql > p.q_rows;
                     const bool bad_ctx = (int64_t)ctx > ((int64_t)p.max_blocks << p.bshift);
                     // every block's cursor passes every sequence; one reports
@@ -504,6 +533,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 return (t < u.n_tiles && lane < nb && jt < u.n_end) ? __ldg(table + (jt >> p.bshift)) : -1;
             };
             int phys_next = entry(0);
+            // KN: the unit whose key range ends at the prompt's end writes it
+            const bool writer = KN && u.n_end == u.pos0 + u.ql;
             for (int t = 0; t < u.n_tiles; ++t, ++g) {
                 const int st = g % NS;
                 const int phys = phys_next;
@@ -516,6 +547,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const bool present = lane < nb && j < u.n_end;
                 const bool in_pool = present && phys >= 0 && phys < p.num_blocks;
                 if (present && !in_pool) report(p.status, PA_ERR_BAD_BLOCK);
+                if constexpr (KN) {
+                    // the tile's rows of the new keys (values), one box per panel
+                    // into the Q-like layout [panel][row][128 bytes]; rows past the
+                    // prompt belong to the next prompt (or read as zeros past the
+                    // last row) and meet masked scores or P = 0.  First, this
+                    // lane's stores from the stage (tile g - 2) have read it.
+                    bulk_wait_read<NSK - 1>();
+                    __syncwarp();
+                    const uint32_t tile = ring + st * L::TILE;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar(full, st), L::TILE);
+#pragma unroll
+                        for (int pn = 0; pn < NP; ++pn)
+                            tma_load_3d(tile + pn * kPanel, is_k ? &maps.kn : &maps.vn, pn * 64, u.h,
+                                        u.q_beg + n0, bar(full, st), keep);
+                    }
+                    __syncwarp();
+                    if (writer) {
+                        // the unit that reaches the prompt's last key stores each
+                        // tile's blocks into the cache, once the tile has landed
+                        ok = warp_all(mbar_wait_bounded(bar(full, st), (g / NS) & 1, p.status, true));
+                        if (!ok) break;
+                        if (in_pool) {
+                            const int y = (phys * H + u.h) << p.bshift;
+                            const uint32_t src = tile + ((uint32_t)lane << p.bshift) * 128u;
+                            const int nrow = min(B, u.n_end - j);   // the block's rows in the prompt
+                            if (nrow == B) {
+#pragma unroll
+                                for (int pn = 0; pn < NP; ++pn)
+                                    tma_store_2d(is_k ? &maps.ks : &maps.vs, pn * 64, y, src + pn * kPanel);
+                            } else {
+                                // the last block up to the prompt's end only (the slots
+                                // past it keep what they held, as with the slot write)
+                                int r = 0;
+                                auto piece = [&](int m) {
+#pragma unroll
+                                    for (int pn = 0; pn < NP; ++pn)
+                                        tma_store_2d(is_k ? &maps.k_part[m] : &maps.v_part[m], pn * 64,
+                                                     y + r, src + (uint32_t)r * 128u + pn * kPanel);
+                                    r += 8 >> m;
+                                };
+                                while (r + 8 <= nrow) piece(0);
+#pragma unroll
+                                for (int m = 1; m < kVPartMaps; ++m)
+                                    if (nrow & (8 >> m)) piece(m);
+                            }
+                        }
+                    }
+                    bulk_commit();   // one group per tile (empty when nothing was stored)
+                    continue;
+                }
                 // V: the block holding the context's last position is copied up to
                 // it, in boxes of 16, 8, 4, 2 and 1 rows (slots past it are never read)
                 const int nv = min(B, u.n_end - j);
@@ -562,6 +644,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
         }
+        if (KN) bulk_wait_all();   // this lane's cache stores done before the CTA exits
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
     } else if (warp == kMmaWarp) {
         // ---- one thread issues the MMAs in a fixed order, per key tile j of a
@@ -599,13 +682,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // are one base plus a constant.
             auto issue_s = [&](int x, int st) {
                 const uint64_t dq = tc::smem_desc(sQ + x * L::TILE, 16, 1024);
-                const uint64_t dk = tc::smem_desc(sK + st * L::TILE, 16, 1024u * NP);
+                // K: 8-row groups of NP panels, or (KN) laid out like Q
+                const uint64_t dk = tc::smem_desc(sK + st * L::TILE, 16, KN ? 1024u : 1024u * NP);
+                constexpr uint32_t kPanelStep = KN ? kPanel : 1024u;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    // Q: [panel][128 rows]; K: 8-row groups of NP panels
+                    // Q: [panel][128 rows]
                     const uint32_t col = (kk & 3) * 32;
                     tc::mma_ss(tmem + x * 128, dq + (((kk >> 2) * kPanel + col) >> 4),
-                               dk + (((kk >> 2) * 1024u + col) >> 4), idS, kk > 0 ? 1u : 0u);
+                               dk + (((kk >> 2) * kPanelStep + col) >> 4), idS, kk > 0 ? 1u : 0u);
                 }
                 tc::commit(bar(bars.s_full, x));
             };
@@ -636,13 +721,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // the slot's previous job
                         if (j == 0 && job[x] > 0 && !spin(bar(bars.o_free, x), (job[x] - 1) & 1)) break;
                         tc::fence_after();
-                        const uint64_t dv0 = tc::smem_desc(sV + (gj % NSV) * L::TILE, 1024, 1024u * NP);
+                        // V: 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart
+                        // (KN: panels kPanel apart, groups 1 KB apart)
+                        const uint64_t dv0 = KN ? tc::smem_desc(sV + (gj % NSV) * L::TILE, kPanel, 1024)
+                                                : tc::smem_desc(sV + (gj % NSV) * L::TILE, 1024, 1024u * NP);
 #pragma unroll
                         for (int kk = 0; kk < TBN / 16; ++kk) {
-                            // V: 16 rows = 2 groups; panels 1 KB apart, groups NP KB apart.
                             // P of keys 16 kk .. 16 kk + 15: column half (kk / 4) * 64, then
                             // 16 columns per 32 keys, 8 columns (16 fp16) per slice
-                            const uint64_t dv = dv0 + ((kk * 2048u * NP) >> 4);
+                            const uint64_t dv = dv0 + ((kk * (KN ? 2048u : 2048u * NP)) >> 4);
                             const uint32_t pa =
                                 tmem + x * 128 + (kk >> 2) * 64 + ((kk >> 1) & 1) * 16 + (kk & 1) * 8;
                             tc::mma_ts(tmem + kOCol + x * 128, pa, dv, idO, (j > 0 || kk > 0) ? 1u : 0u);
@@ -916,14 +1003,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool KN>
 cudaError_t set_prefill_smem_once() {
     static std::once_flag once[64];
     static cudaError_t err[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::call_once(once[dev], [&] {
-        err[dev] = cudaFuncSetAttribute(paged_prefill_tc<D>,
+        err[dev] = cudaFuncSetAttribute(paged_prefill_tc<D, KN>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)TcLayout<D>::BYTES);
     });
@@ -1018,9 +1105,10 @@ int encode_run_map(CUtensorMap *m, const void *base, uint64_t rows, int B) {
     return PA_OK;
 }
 
-template <int D>
-int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st) {
-    cudaError_t e = set_prefill_smem_once<D>();
+template <int D, bool KN>
+int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, const void *k_new,
+             const void *v_new, cudaStream_t st) {
+    cudaError_t e = set_prefill_smem_once<D, KN>();
     if (e != cudaSuccess)
         return fail(PA_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(e));
     const int sms = sm_count_of_current_device();
@@ -1039,12 +1127,23 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
     for (int m = 0; rc == PA_OK && m < kVPartMaps; ++m)
         rc = encode_map(&maps.v_part[m], p.v_cache, 2, cache_rows, H, D, 8 >> m);
     if (rc == PA_OK) rc = encode_map(&maps.q, p.q, 3, (uint64_t)p.q_rows, H, D, TBM);
+    if (KN) {   // the new rows, read like q; the cache, stored one block run and panel at a time
+        if (rc == PA_OK) rc = encode_map(&maps.kn, k_new, 3, (uint64_t)p.q_rows, H, D, TBM);
+        if (rc == PA_OK) rc = encode_map(&maps.vn, v_new, 3, (uint64_t)p.q_rows, H, D, TBM);
+        if (rc == PA_OK) rc = encode_map(&maps.ks, p.k_cache, 2, cache_rows, H, D, d->block_size);
+        if (rc == PA_OK) rc = encode_map(&maps.vs, p.v_cache, 2, cache_rows, H, D, d->block_size);
+        for (int m = 0; rc == PA_OK && m < kVPartMaps; ++m)
+            rc = encode_map(&maps.k_part[m], p.k_cache, 2, cache_rows, H, D, 8 >> m);
+    } else {
+        maps.kn = maps.vn = maps.ks = maps.vs = maps.q;   // unused
+        for (int m = 0; m < kVPartMaps; ++m) maps.k_part[m] = maps.q;
+    }
     if (rc != PA_OK) return rc;
     static std::atomic<uint32_t> calls{0};
     UnitCounter *ctrs = unit_counters_of_current_device();
     if (!ctrs) return fail(PA_ERR_CUDA, "prefill: cannot find the unit counters");
     p.units = ctrs + calls.fetch_add(1) % kUnitCounters;
-    paged_prefill_tc<D><<<sms, kTcThreads, TcLayout<D>::BYTES, st>>>(p, maps, n_seqs);
+    paged_prefill_tc<D, KN><<<sms, kTcThreads, TcLayout<D>::BYTES, st>>>(p, maps, n_seqs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
     return PA_OK;
@@ -1052,11 +1151,14 @@ int launch_d(PrefillParams p, int n_seqs, const pa_pool_desc *d, cudaStream_t st
 
 }  // namespace
 
-int launch_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
-                             const int32_t *block_tables, const int32_t *ctx_lens,
-                             const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,
-                             int32_t max_q_len, int32_t q_rows, float scale, int32_t *status,
-                             const pa_pool_desc *d, void *stream) {
+namespace {
+
+int launch_prefill(void *out, const void *q, const void *k_new, const void *v_new,
+                   const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                   const int32_t *ctx_lens, const int32_t *q_starts, int32_t n_seqs,
+                   int32_t max_blocks, int32_t max_q_len, int32_t q_rows, float scale,
+                   int32_t *status, const pa_pool_desc *d, void *stream) {
+    const bool kn = k_new != nullptr;
     if (!d) return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: desc is NULL");
     std::string why;
     if (!device_geometry_ok(d, &why)) return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: %s", why.c_str());
@@ -1073,6 +1175,10 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     if (((uintptr_t)out | (uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache) & 15)
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: out, q and caches must be 16-byte aligned");
     if (max_blocks < 1) return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: max_blocks < 1");
+    if (kn && (!v_new || (((uintptr_t)k_new | (uintptr_t)v_new) & 15)))
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_step_attention: k_new / v_new NULL or not 16-byte aligned");
+    if (kn && d->block_size < 8)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_step_attention: block_size %d < 8", d->block_size);
     if (!(scale > 0.f) || !std::isfinite(scale))
         return fail(PA_ERR_INVALID_ARG, "pa_prefill_attention: scale must be finite and > 0");
     int bshift = 0;
@@ -1095,7 +1201,33 @@ int launch_prefill_attention(void *out, const void *q, const void *k_cache, cons
     p.qscale = scale * 1.4426950408889634f;
     p.status = status;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return d->head_dim == 64 ? launch_d<64>(p, n_seqs, d, st) : launch_d<128>(p, n_seqs, d, st);
+    if (kn)
+        return d->head_dim == 64 ? launch_d<64, true>(p, n_seqs, d, k_new, v_new, st)
+                                 : launch_d<128, true>(p, n_seqs, d, k_new, v_new, st);
+    return d->head_dim == 64 ? launch_d<64, false>(p, n_seqs, d, nullptr, nullptr, st)
+                             : launch_d<128, false>(p, n_seqs, d, nullptr, nullptr, st);
+}
+
+}  // namespace
+
+int launch_prefill_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, const int32_t *ctx_lens,
+                             const int32_t *q_starts, int32_t n_seqs, int32_t max_blocks,
+                             int32_t max_q_len, int32_t q_rows, float scale, int32_t *status,
+                             const pa_pool_desc *d, void *stream) {
+    return launch_prefill(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, ctx_lens,
+                          q_starts, n_seqs, max_blocks, max_q_len, q_rows, scale, status, d, stream);
+}
+
+int launch_prefill_step_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const int32_t *block_tables,
+                                  const int32_t *ctx_lens, const int32_t *q_starts, int32_t n_seqs,
+                                  int32_t max_blocks, int32_t max_q_len, int32_t q_rows,
+                                  float scale, int32_t *status, const pa_pool_desc *d, void *stream) {
+    if (n_seqs > 0 && q_rows > 0 && !k_new)
+        return fail(PA_ERR_INVALID_ARG, "pa_prefill_step_attention: NULL k_new");
+    return launch_prefill(out, q, k_new, v_new, k_cache, v_cache, block_tables, ctx_lens, q_starts,
+                          n_seqs, max_blocks, max_q_len, q_rows, scale, status, d, stream);
 }
 
 }  // namespace pagedkv

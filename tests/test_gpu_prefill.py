@@ -384,6 +384,125 @@ def test_prefill_replayed_from_a_graph_repeated_and_on_two_streams():
     assert torch.equal(o1.view(torch.int16), bits) and torch.equal(o2.view(torch.int16), bits)
 
 
+def _fused_vs_separate(q, kn, vn, kc, vc, tables, ctxa, qs, scale, B, mql):
+    """Runs pa_write_kv + pa_prefill_attention and pa_prefill_step_attention
+    from the same caches; returns both outputs and cache images."""
+    T, H, D = q.shape
+    desc = pk.PoolDesc(kc.shape[0], B, num_heads=H, head_dim=D)
+    slots = np.concatenate([[tables[s][p // B] * B + p % B for p in range(int(ctxa[s]))]
+                            for s in range(len(ctxa))]).astype(np.int64)
+    res = []
+    for fused in (False, True):
+        dk, dv = _dev(kc), _dev(vc)
+        out = torch.full((T, H, D), float("nan"), dtype=torch.float16, device="cuda")
+        st = _status()
+        if fused:
+            pk.pa_prefill_step_attention(out, _dev(q), _dev(kn), _dev(vn), dk, dv, _dev(tables),
+                                         _dev(ctxa), _dev(qs), scale, desc, max_q_len=mql, status=st)
+        else:
+            pk.pa_write_kv(_dev(kn), _dev(vn), _dev(slots), dk, dv, desc, status=st)
+            pk.pa_prefill_attention(out, _dev(q), dk, dv, _dev(tables), _dev(ctxa), _dev(qs), scale,
+                                    desc, max_q_len=mql, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0, (fused, st.item())
+        res.append((out.cpu().numpy(), dk.cpu().numpy(), dv.cpu().numpy()))
+    return res, slots
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_fused_prefill_step_equals_write_then_prefill_and_the_oracle(D, B):
+    """pa_prefill_step_attention on whole prompts (keys and values read from
+    the new rows, written into the cache by the unit that reaches each
+    prompt's last key): the cache image and the output bitwise those of
+    pa_write_kv followed by pa_prefill_attention, the image that of the
+    oracle's slot write, the output within 2e-3 of the oracle.  Prompt
+    lengths cover one token, partial and full 128-query tiles, odd and even
+    tile counts, and blocks cut by tile edges."""
+    rng = np.random.default_rng(10 * D + B)
+    H = 3
+    ctx = [1, 7, B, 127, 128, 129, 300, 520, 64 + B // 2]
+    q, kc, vc, tables, ctxa, qs = _batch(rng, ctx, ctx, H, D, B)
+    T = int(qs[-1])
+    kn, vn = _f16(rng, (T, H, D)), _f16(rng, (T, H, D))
+    scale = 1.0 / math.sqrt(D)
+    (sep, fus), slots = _fused_vs_separate(q, kn, vn, kc, vc, tables, ctxa, qs, scale, B, max(ctx))
+    for a, b in zip(sep, fus):
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    okc, ovc = kc.copy(), vc.copy()
+    oc.write_kv(okc, ovc, kn, vn, slots)
+    assert np.array_equal(fus[1].view(np.uint16), okc.view(np.uint16))
+    assert np.array_equal(fus[2].view(np.uint16), ovc.view(np.uint16))
+    _check(fus[0], oa.paged_prefill(q, okc, ovc, tables, ctxa, qs, scale))
+
+
+def test_fused_prefill_step_full_size_batch():
+    """The benchmark's 256 prompts (81 539 tokens, 40 heads x 128, block 16):
+    fused and separate give bitwise the same output and cache."""
+    w = wl.prefill_b256()
+    H, D, B = w.num_heads, w.head_dim, w.block_size
+    lens = np.array(w.prompt_lens)
+    desc = pk.PoolDesc(w.num_blocks, B, num_heads=H, head_dim=D, free_order=w.free_order)
+    pool = pk.pa_pool_create(desc)
+    try:
+        slots = np.concatenate([pk.pa_seq_add(pool, i, int(n)) for i, n in enumerate(lens)])
+        tables, ctx = pk.pa_get_block_tables(pool, list(range(len(lens))), -(-int(lens.max()) // B))
+    finally:
+        pk.pa_pool_destroy(pool)
+    T = int(lens.sum())
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q, kn, vn = (torch.randn((T, H, D), generator=g, device="cuda", dtype=torch.float16) for _ in range(3))
+    kc0 = torch.randn((w.num_blocks, H, B, D), generator=g, device="cuda", dtype=torch.float16)
+    vc0 = torch.randn_like(kc0)
+    qs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    d_tab, d_ctx, d_qs = _dev(tables), _dev(ctx), _dev(qs)
+    outs, caches = [], []
+    for fused in (False, True):
+        kc, vc = kc0.clone(), vc0.clone()
+        out = torch.full_like(q, float("nan"))
+        st = _status()
+        if fused:
+            pk.pa_prefill_step_attention(out, q, kn, vn, kc, vc, d_tab, d_ctx, d_qs, w.scale, desc,
+                                         max_q_len=int(lens.max()), status=st)
+        else:
+            pk.pa_write_kv(kn, vn, _dev(slots), kc, vc, desc, status=st)
+            pk.pa_prefill_attention(out, q, kc, vc, d_tab, d_ctx, d_qs, w.scale, desc,
+                                    max_q_len=int(lens.max()), status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        outs.append(out)
+        caches.append((kc, vc))
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(caches[0][0].view(torch.int16), caches[1][0].view(torch.int16))
+    assert torch.equal(caches[0][1].view(torch.int16), caches[1][1].view(torch.int16))
+
+
+def test_fused_prefill_step_refusals():
+    """A sequence that is not a whole prompt (q_len < ctx) is reported in the
+    status word; block size 4 and a NULL k_new are refused on the host."""
+    rng = np.random.default_rng(43)
+    H, D, B = 2, 128, 16
+    q, kc, vc, tables, ctxa, qs = _batch(rng, [40, 90], [40, 60], H, D, B)
+    T = int(qs[-1])
+    kn, vn = _f16(rng, (T, H, D)), _f16(rng, (T, H, D))
+    desc = pk.PoolDesc(kc.shape[0], B, num_heads=H, head_dim=D)
+    out = torch.empty((T, H, D), dtype=torch.float16, device="cuda")
+    st = _status()
+    pk.pa_prefill_step_attention(out, _dev(q), _dev(kn), _dev(vn), _dev(kc), _dev(vc), _dev(tables),
+                                 _dev(ctxa), _dev(qs), 0.1, desc, max_q_len=60, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == pk.PA_ERR_INVALID_ARG
+    desc4 = pk.PoolDesc(kc.shape[0], 4, num_heads=H, head_dim=D)
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_prefill_step_attention(out, _dev(q), _dev(kn), _dev(vn), _dev(kc), _dev(vc),
+                                     _dev(tables), _dev(ctxa), _dev(qs), 0.1, desc4, max_q_len=60)
+    assert e.value.code == pk.PA_ERR_INVALID_ARG
+    with pytest.raises(pk.PagedKVError) as e:
+        pk.pa_prefill_step_attention(out, _dev(q), None, _dev(vn), _dev(kc), _dev(vc),
+                                     _dev(tables), _dev(ctxa), _dev(qs), 0.1, desc, max_q_len=60)
+    assert e.value.code == pk.PA_ERR_INVALID_ARG
+
+
 def test_prefill_status_reports_bad_lengths_and_blocks():
     rng = np.random.default_rng(13)
     H, D, B = 2, 64, 4
