@@ -535,6 +535,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int phys_next = entry(0);
             // KN: the unit whose key range ends at the prompt's end writes it
             const bool writer = KN && u.n_end == u.pos0 + u.ql;
+            int phys_prev = -1;   // block of this lane in the tile before (KN stores)
+            // KN: stores key tile tt (ring position gg; this lane's block phys_t)
+            // into the cache once it has landed; one bulk group per call
+            auto store_tile = [&](int tt, int gg, int phys_t) {
+                const int sg = gg % NS;
+                if (!warp_all(mbar_wait_bounded(bar(full, sg), (gg / NS) & 1, p.status, true))) {
+                    ok = false;
+                    return false;
+                }
+                const int jt = tt * TBN + (lane << p.bshift);   // first position of block `lane`
+                if (lane < nb && jt < u.n_end && phys_t >= 0 && phys_t < p.num_blocks) {
+                    const int y = (phys_t * H + u.h) << p.bshift;
+                    const uint32_t src = ring + sg * L::TILE + ((uint32_t)lane << p.bshift) * 128u;
+                    const int nrow = min(B, u.n_end - jt);   // the block's rows in the prompt
+                    if (nrow == B) {
+#pragma unroll
+                        for (int pn = 0; pn < NP; ++pn)
+                            tma_store_2d(is_k ? &maps.ks : &maps.vs, pn * 64, y, src + pn * kPanel);
+                    } else {
+                        // the last block up to the prompt's end only (the slots past
+                        // it keep what they held, as with the slot write)
+                        int r = 0;
+                        auto piece = [&](int m) {
+#pragma unroll
+                            for (int pn = 0; pn < NP; ++pn)
+                                tma_store_2d(is_k ? &maps.k_part[m] : &maps.v_part[m], pn * 64, y + r,
+                                             src + (uint32_t)r * 128u + pn * kPanel);
+                            r += 8 >> m;
+                        };
+                        while (r + 8 <= nrow) piece(0);
+#pragma unroll
+                        for (int m = 1; m < kVPartMaps; ++m)
+                            if (nrow & (8 >> m)) piece(m);
+                    }
+                }
+                bulk_commit();
+                return true;
+            };
             for (int t = 0; t < u.n_tiles; ++t, ++g) {
                 const int st = g % NS;
                 const int phys = phys_next;
@@ -552,50 +590,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // into the Q-like layout [panel][row][128 bytes]; rows past the
                     // prompt belong to the next prompt (or read as zeros past the
                     // last row) and meet masked scores or P = 0.  First, this
-                    // lane's stores from the stage (tile g - 2) have read it.
-                    bulk_wait_read<NSK - 1>();
+                    // lane's stores from the stage (tile g - 2, stored while tile
+                    // g - 1 loaded) have read it.
+                    bulk_wait_read<0>();
                     __syncwarp();
-                    const uint32_t tile = ring + st * L::TILE;
                     if (lane == 0) {
                         mbar_arrive_expect_tx(bar(full, st), L::TILE);
 #pragma unroll
                         for (int pn = 0; pn < NP; ++pn)
-                            tma_load_3d(tile + pn * kPanel, is_k ? &maps.kn : &maps.vn, pn * 64, u.h,
-                                        u.q_beg + n0, bar(full, st), keep);
+                            tma_load_3d(ring + st * L::TILE + pn * kPanel, is_k ? &maps.kn : &maps.vn,
+                                        pn * 64, u.h, u.q_beg + n0, bar(full, st), keep);
                     }
                     __syncwarp();
-                    if (writer) {
-                        // the unit that reaches the prompt's last key stores each
-                        // tile's blocks into the cache, once the tile has landed
-                        ok = warp_all(mbar_wait_bounded(bar(full, st), (g / NS) & 1, p.status, true));
-                        if (!ok) break;
-                        if (in_pool) {
-                            const int y = (phys * H + u.h) << p.bshift;
-                            const uint32_t src = tile + ((uint32_t)lane << p.bshift) * 128u;
-                            const int nrow = min(B, u.n_end - j);   // the block's rows in the prompt
-                            if (nrow == B) {
-#pragma unroll
-                                for (int pn = 0; pn < NP; ++pn)
-                                    tma_store_2d(is_k ? &maps.ks : &maps.vs, pn * 64, y, src + pn * kPanel);
-                            } else {
-                                // the last block up to the prompt's end only (the slots
-                                // past it keep what they held, as with the slot write)
-                                int r = 0;
-                                auto piece = [&](int m) {
-#pragma unroll
-                                    for (int pn = 0; pn < NP; ++pn)
-                                        tma_store_2d(is_k ? &maps.k_part[m] : &maps.v_part[m], pn * 64,
-                                                     y + r, src + (uint32_t)r * 128u + pn * kPanel);
-                                    r += 8 >> m;
-                                };
-                                while (r + 8 <= nrow) piece(0);
-#pragma unroll
-                                for (int m = 1; m < kVPartMaps; ++m)
-                                    if (nrow & (8 >> m)) piece(m);
-                            }
-                        }
-                    }
-                    bulk_commit();   // one group per tile (empty when nothing was stored)
+                    // the unit that reaches the prompt's last key stores each tile's
+                    // blocks into the cache, one tile behind its loads
+                    if (writer && t > 0 && !store_tile(t - 1, g - 1, phys_prev)) break;
+                    phys_prev = phys;
                     continue;
                 }
                 // V: the block holding the context's last position is copied up to
@@ -643,6 +653,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     (uint32_t)B * D * 2);
                 }
             }
+            if (KN && writer && ok) store_tile(u.n_tiles - 1, g - 1, phys_prev);   // the last tile
         }
         if (KN) bulk_wait_all();   // this lane's cache stores done before the CTA exits
         if (!ok) report(p.status, PA_ERR_TIMEOUT);
