@@ -519,15 +519,11 @@ def run_ours(args):
             "dtype": "f16 (fp32 accumulate)",
             "data": "synthetic (seeded N(0,1) fp16 K/V/q; lognormal length mix)",
             "config": {
-                "workload": f"mixed-length serving batch, OPT-13B-shaped layer 40x128, block 16, "
-                            f"batch {S}/GPU, ctx<=2048, split>512, steady-state continuous batch",
-                "batch_per_gpu": S, "num_heads": H, "head_dim": D, "block_size": B,
-                "partition_tokens": w.split_tokens, "pool_blocks": w.num_blocks,
+                **_decode_config(w, ws),
                 "mean_ctx": stats["tokens"] / args.steps / S,
                 "sequences_replaced": batch.replaced,
                 "l2": "working set ~%.1f GB per step >> 129 MB L2, no flush"
                       % (stats["attn_bytes"] / args.steps / 1e9),
-                "parallelism": f"replicas x{ws} (sequences independent, no collective)",
             },
             "gpu_launches": stats["launches"],
             "roofline": {
@@ -1339,6 +1335,16 @@ def run_prefill(args):
     pb.close()
 
 
+def _decode_config(w, ws):
+    """The fixed part of the decode bench's config (both arms)."""
+    return {"workload": f"mixed-length serving batch, OPT-13B-shaped layer 40x128, block 16, "
+                        f"batch {len(w.prompt_lens)}/GPU, ctx<=2048, split>512, steady-state continuous batch",
+            "batch_per_gpu": len(w.prompt_lens), "num_heads": w.num_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "partition_tokens": w.split_tokens,
+            "pool_blocks": w.num_blocks,
+            "parallelism": f"replicas x{ws} (sequences independent, no collective)"}
+
+
 def _oracle_sample(n_seqs):
     """Host data for the first n_seqs sequences of the same workload, laid
     out by the oracle's own block manager."""
@@ -1389,6 +1395,7 @@ def run_reference(args):
     ws, rank, _ = _dist_env()
     if rank != 0:
         return
+    import workloads as wl
     from oracle import attention as oa
 
     q, kc, vc, tables, ctx, scale = _oracle_sample(args.ref_seqs)
@@ -1405,7 +1412,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "mixed-length serving batch (bounded sample)"},
+        "data": "synthetic", "config": _decode_config(wl.mixed_b256(steady_state=True), ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oa.max_threads(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
