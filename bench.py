@@ -528,7 +528,7 @@ def run_ours(args):
             "gpu_launches": stats["launches"],
             "roofline": {
                 "bound": "hbm",
-                "kernel": "paged_decode_persistent + paged_merge_kernel (pa_decode_attention)",
+                "kernel": "paged_decode_persistent + paged_merge_kernel (pa_decode_step_attention: the new tokens' slot write and attention)",
                 "achieved": achieved,
                 "peak": peak,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
