@@ -267,12 +267,15 @@ def test_attention_large_batch_grid_fallback_path():
 
 
 def test_attention_repeated_calls_reuse_workspace():
-    """The scheduling word in the workspace is cleared by every call."""
+    """The workspace needs no initialisation and may be reused: every call
+    clears its scheduling word itself, and partial results are written
+    before they are read.  A workspace of all-ones bytes, used three times,
+    gives the oracle's result each time."""
     rng = np.random.default_rng(27)
     q, kc, vc, tables, ctxa = _random_paged_batch(rng, [600, 5, 1300, 64], 4, 128, 16)
     desc = pk.PoolDesc(kc.shape[0], 16, num_heads=4, head_dim=128)
-    ws = torch.zeros(pk.pa_decode_workspace_bytes(4, tables.shape[1], desc), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.full((pk.pa_decode_workspace_bytes(4, tables.shape[1], desc),), 255, dtype=torch.uint8,
+                    device="cuda")
     ref = oa.paged_attention(q, kc, vc, tables, ctxa, 0.1)
     dq, dk, dv, dt, dc = _dev(q), _dev(kc), _dev(vc), _dev(tables), _dev(ctxa)
     st = _status()
