@@ -130,6 +130,14 @@ def _check(rc: int):
         raise PagedKVError(rc, msg)
 
 
+def _need_elems(n_elems: int, **tensors):
+    """Refuses a tensor holding fewer elements than the call reads from it
+    (None is left to the library, which refuses a NULL it needs)."""
+    for name, t in tensors.items():
+        if t is not None and t.numel() < n_elems:
+            raise ValueError(f"{name} holds {t.numel()} elements, the call reads {n_elems}")
+
+
 def _host_i32(a):
     return np.ascontiguousarray(a, dtype=np.int32)
 
@@ -466,6 +474,8 @@ def pa_decode_step_attention(out, q, k_new, v_new, slot_mapping, k_cache, v_cach
     and decode attention in one call."""
     n = int(q.shape[0]) if n_seqs is None else int(n_seqs)
     mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
+    _need_elems(n * desc.num_heads * desc.head_dim, k_new=k_new, v_new=v_new)
+    _need_elems(n, slot_mapping=slot_mapping)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.pa_decode_step_attention(_dev(out), _dev(q), _dev(k_new), _dev(v_new),
                                          _dev(slot_mapping), _dev(k_cache), _dev(v_cache),
@@ -499,6 +509,8 @@ def pa_prefill_step_attention(out, q, k_new, v_new, k_cache, v_cache, block_tabl
     n = int(ctx_lens.shape[0]) if n_seqs is None else int(n_seqs)
     mb = int(block_tables.shape[1]) if max_blocks is None else int(max_blocks)
     rows = min(int(q.shape[0]), int(out.shape[0])) if q_rows is None else int(q_rows)
+    # the new rows are read as [rows][num_heads][head_dim] tensors, like q
+    _need_elems(rows * desc.num_heads * desc.head_dim, k_new=k_new, v_new=v_new)
     _check(_lib.pa_prefill_step_attention(_dev(out), _dev(q), _dev(k_new), _dev(v_new),
                                           _dev(k_cache), _dev(v_cache), _dev(block_tables),
                                           _dev(ctx_lens), _dev(q_starts), n, mb, int(max_q_len),
