@@ -84,6 +84,27 @@ def test_bounded_wait_selftest_refuses_a_null_status_before_any_launch():
     assert "status is NULL" in pk.pa_last_error_string()
 
 
+def test_one_call_step_bindings_refuse_short_new_rows_before_any_device_call():
+    """The bindings of the one-call steps check that the new rows (and, for
+    decode, the slot mapping) hold what the library will read, before any
+    pointer reaches the library: host tensors suffice to see the refusal."""
+    import torch
+    H, D = 2, 64
+    d = pk.PoolDesc(8, 16, num_heads=H, head_dim=D)
+    q = torch.empty((3, H, D), dtype=torch.float16)
+    short = torch.empty((2, H, D), dtype=torch.float16)
+    slots = torch.zeros(3, dtype=torch.int64)
+    t = torch.empty(1)
+    tables = torch.zeros((3, 4), dtype=torch.int32)
+    ctx = torch.ones(3, dtype=torch.int32)
+    with pytest.raises(ValueError, match="k_new"):
+        pk.pa_decode_step_attention(q, q, short, q, slots, t, t, tables, ctx, 0.1, d)
+    with pytest.raises(ValueError, match="slot_mapping"):
+        pk.pa_decode_step_attention(q, q, q, q, slots[:2], t, t, tables, ctx, 0.1, d)
+    with pytest.raises(ValueError, match="v_new"):
+        pk.pa_prefill_step_attention(q, q, q, short, t, t, tables, ctx, t, 0.1, d, max_q_len=3)
+
+
 @pytest.mark.parametrize("name", GOLDEN)
 def test_golden_examples_through_abi(golden_dir, name):
     doc = load(golden_dir, name)
